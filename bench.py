@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""Throughput of the DFlash KV-injection draft step on GB300.
+
+A step is one draft round of the batched serving workload (32 sequences,
+cached context U[256, 4096], block 16, 2 draft layers, d=4096, 32 query / 8
+KV heads of 128, k=5 target layers): one context projection of the 16 new
+context rows of every sequence, then per layer a KV inject and a block
+attention, then a crop back to the step's starting lengths so that every
+step sees the same cache (crop moves no data). The metric is draft blocks
+per second per layer = batch * layers / step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+path shards by sequence with no exchange) and rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft blocks/sec per layer at B=32, ctx≤4K, block 16; attn HBM GB/s vs roofline"
+UNIT = "blocks/s/layer"
+WORKLOAD = "serve_b32"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes and flops (per launch) for the roofline
+# ---------------------------------------------------------------------------
+
+def attention_bytes(w, starts):
+    """K/V rows read + Q read + output written, per layer launch (bf16)."""
+    e = 2
+    ends = starts + w.bs
+    rows = 0
+    for s, t in zip(starts, ends):
+        lo = 0
+        rows += t - lo
+    kv = rows * w.n_kv * w.d_h * 2 * e
+    q = w.batch * w.n_h * w.bs * w.d_h * e
+    out = w.batch * w.bs * w.n_h * w.d_h * e
+    return kv + q + out
+
+
+def gemm_cost(M, K, N):
+    flops = 2.0 * M * K * N
+    bytes_ = 2.0 * (M * K + N * K) + 4.0 * M * N
+    return flops, bytes_
+
+
+# ---------------------------------------------------------------------------
+# reference arm / CPU baseline: the float64 oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample_rate(w, budget_s=12.0, max_steps=None):
+    """Times the oracle on whole-sequence rounds (all layers) until the budget is spent.
+
+    Returns (blocks/s/layer, seconds, sequences done, per-step seconds).
+    """
+    from oracle import dflash_oracle as O
+    from speculative_decoding_draft_dflash_gb300 import synth
+
+    L0 = synth.prefill_lens(w)
+    W_fc, g_h = synth.W_fc(w), synth.gamma_h(w)
+    Wq = [synth.W_Q(w, l) for l in range(w.n_layers)]
+    Wk = [synth.W_K(w, l) for l in range(w.n_layers)]
+    Wv = [synth.W_V(w, l) for l in range(w.n_layers)]
+    gq = [synth.gamma_q(w, l) for l in range(w.n_layers)]
+    gk = [synth.gamma_k(w, l) for l in range(w.n_layers)]
+    steps = []
+    total = 0.0
+    b = 0
+    while (max_steps is None and total < budget_s) or (max_steps is not None and len(steps) < max_steps):
+        cache = O.DraftKVCache(w.n_layers, 1, w.n_kv, w.d_h)
+        for l in range(w.n_layers):
+            K, V = synth.cache_rows(w, l, b, int(L0[b]))
+            cache.set_rows(l, 0, K, V)
+        hid = synth.hidden_states_rows(w, 1, b, w.new_ctx)
+        H = [synth.block_embeddings(w, 1, l, b)[None] for l in range(w.n_layers)]
+        t0 = time.perf_counter()
+        C = O.ctx_project(hid, W_fc, g_h, w.eps)
+        for l in range(w.n_layers):
+            O.kv_inject(cache, l, C, [0, w.new_ctx], Wk[l], Wv[l], gk[l], w.n_kv, w.d_h, w.eps,
+                        w.theta)
+            O.block_attn(cache, l, H[l], Wq[l], Wk[l], Wv[l], gq[l], gk[l], w.n_h, w.n_kv, w.d_h,
+                         w.eps, w.theta, w.windows[l])
+        O.cache_crop(cache, [int(L0[b]) + w.new_ctx])
+        dt = time.perf_counter() - t0
+        steps.append(dt)
+        total += dt
+        b = (b + 1) % w.batch
+    rate = len(steps) * w.n_layers / total
+    return rate, total, len(steps), steps
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cores = os.cpu_count()
+    _, _, _, warm = oracle_sample_rate(w, max_steps=max(1, args.warmup))
+    rate, total, n, steps = oracle_sample_rate(w, max_steps=max(1, args.steps))
+    ms = 1e3 * total / n
+    sample = (f"{n} whole-sequence rounds (ctx_project of {w.new_ctx} rows + {w.n_layers} x "
+              f"(kv_inject + block_attn) + crop) of {w.name}, one sequence per step")
+    line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w),
+            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": w.name, "batch": w.batch, "context": f"U[{w.prefill_lo},{w.prefill_hi}]",
+            "new_context_rows": w.new_ctx, "block_size": w.bs, "draft_layers": w.n_layers,
+            "d": w.d, "n_h": w.n_h, "n_kv": w.n_kv, "d_h": w.d_h, "k_target_layers": w.k,
+            "windows": list(w.windows),
+            "l2": "inputs larger than L2: every step reads the whole KV cache (~0.6 GB) and "
+                  "~0.3 GB of weights, well over the 129 MB L2"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev_index = torch.cuda.current_device()
+
+    from speculative_decoding_draft_dflash_gb300 import build
+    build.build()
+    from speculative_decoding_draft_dflash_gb300 import dflash as D
+    from speculative_decoding_draft_dflash_gb300 import synth
+    from speculative_decoding_draft_dflash_gb300.runner import DeviceWorkload
+
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    dev = DeviceWorkload(w)
+    L0 = synth.prefill_lens(w)
+    counts = np.full(w.batch, w.new_ctx, dtype=np.int64)
+    x = dev.round_inputs(1, L0, counts=counts, crop_to=L0)
+    torch.cuda.synchronize()
+    assert D.dflash_status_get(stream) == 0
+
+    def step():
+        dev.run_round(x, crop=True, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert D.dflash_status_get(stream) == 0, "device status after warm-up"
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- timed region: K steps, CUDA events on the launching stream ----
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = D.dflash_launch_count()
+    D.dflash_trace_start(["attention", "gemm", "combine", "head_epilogue", "rmsnorm"],
+                         64 * args.steps)
+    with ClockSampler(dev_index) as clk:
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        barrier()
+    trace = D.dflash_trace_stop()
+    launches = D.dflash_launch_count() - launches0
+    t_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        tt = torch.tensor([t_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_ms = float(tt.item())
+    ms_per_step = t_ms / args.steps
+    value = world * w.batch * w.n_layers / (ms_per_step * 1e-3)
+    assert D.dflash_status_get(stream) == 0, "device status after the timed region"
+
+    # ---- per-kernel times from the trace (same timed region) ----
+    per = {}
+    for name, ms in trace:
+        per.setdefault(name, []).append(ms)
+    # the gemm kinds in launch order within a step: fc, then per layer (kv, qkv)
+    gemm_names = ["gemm_fc"] + [n for _ in range(w.n_layers) for n in ("gemm_kv", "gemm_qkv")]
+    gemm_times = per.pop("gemm", [])
+    for i, ms in enumerate(gemm_times):
+        per.setdefault(gemm_names[i % len(gemm_names)], []).append(ms)
+    kernels = {k: {"launches": len(v), "avg_us": 1e3 * sum(v) / len(v),
+                   "share_of_step": sum(v) / t_ms} for k, v in per.items() if v}
+    pk = peaks()
+    starts = L0 + w.new_ctx
+    attn_bytes = attention_bytes(w, starts)
+    M = w.batch * w.new_ctx
+    costs = {"gemm_fc": gemm_cost(M, w.k * w.d, w.d),
+             "gemm_kv": gemm_cost(M, w.d, 2 * w.n_kv * w.d_h),
+             "gemm_qkv": gemm_cost(w.batch * w.bs, w.d, (w.n_h + 2 * w.n_kv) * w.d_h)}
+    ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+
+    def roofline_for(name):
+        k = kernels[name]
+        dur = k["avg_us"] * 1e-6
+        if name == "attention":
+            ach = attn_bytes / dur / 1e9
+            return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                    "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": None,
+                    "algorithmic_bytes_per_launch": attn_bytes,
+                    "frac_of_nominal_8TBs": ach / 8000.0, "peak_source": pk["source"]}
+        if name in costs:
+            fl, by = costs[name]
+            if fl / by > ridge:
+                ach = fl / dur / 1e12
+                return {"kernel": name, "bound": "tensor", "achieved": ach,
+                        "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                        "frac": ach / pk["bf16_tflops_sustained"], "traffic": None,
+                        "algorithmic_flops_per_launch": fl, "peak_source": pk["source"] + " sustained"}
+            ach = by / dur / 1e9
+            return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                    "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": None,
+                    "algorithmic_bytes_per_launch": by, "peak_source": pk["source"]}
+        return None
+
+    dominant = max(kernels, key=lambda k: kernels[k]["share_of_step"] * (k in costs or k == "attention"))
+    roofline = roofline_for(dominant)
+    others = {k: roofline_for(k) for k in kernels if k != dominant and (k in costs or k == "attention")}
+
+    # ---- end to end: host inputs in, host results out, through the same calls ----
+    e2e = run_e2e(args, w, dev, x, stream, D)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(w), "clocks": clk.summary(), "e2e": e2e,
+            "gpu_launches": int(launches), "roofline": roofline, "roofline_other": others,
+            "kernels": kernels}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, total, n, _ = oracle_sample_rate(w, budget_s=12.0)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": f"{n} whole-sequence rounds of {w.name} "
+                                          f"({total:.1f} s, float64 NumPy, default BLAS threads)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, dev, x, stream, D):
+    """The same steps with inputs copied from pinned host memory and outputs read back each step."""
+    import torch
+    hid_h = [t.cpu().pin_memory() for t in x.hidden]
+    H_h = [t.cpu().pin_memory() for t in x.H]
+    cu_h = x.cu_rows.cpu().pin_memory()
+    crop_h = x.crop_to.cpu().pin_memory()
+    out_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in dev.out]
+    h2d = sum(t.numel() * t.element_size() for t in hid_h + H_h + [cu_h, crop_h])
+    d2h = sum(t.numel() * t.element_size() for t in out_h)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for dst, src in zip(x.hidden, hid_h):
+                dst.copy_(src, non_blocking=True)
+            for dst, src in zip(x.H, H_h):
+                dst.copy_(src, non_blocking=True)
+            x.cu_rows.copy_(cu_h, non_blocking=True)
+            x.crop_to.copy_(crop_h, non_blocking=True)
+            dev.run_round(x, crop=True, stream=stream)
+            for dst, src in zip(out_h, dev.out):
+                dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    assert D.dflash_status_get(stream) == 0
+    ms = ev0.elapsed_time(ev1) / args.steps
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return {"value": world * w.batch * w.n_layers / (ms * 1e-3), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}
+
+
+def main():
+    args = parse()
+    from speculative_decoding_draft_dflash_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

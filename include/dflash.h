@@ -1,0 +1,238 @@
+/*
+ * dflash.h - C ABI of the DFlash KV-injection draft attention step on GB300 (sm_103a).
+ *
+ * The step (DFlash KV Injection Walkthrough, Steps 1-4 and 7; DFlash source
+ * guide (II): Qwen3DFlashAttention, parts 1-5):
+ *
+ *   C      = RMSNorm_gh( concat[h^(l1) .. h^(lk)] W_fc^T )             dflash_ctx_project
+ *   cache += RoPE(KNorm(C W_K^T)), C W_V^T  at the rows' positions     dflash_kv_inject
+ *   Q, Kb, Vb = RoPE(QNorm(H W_Q^T)), RoPE(KNorm(H W_K^T)), H W_V^T
+ *   out    = softmax(Q [cache K || Kb]^T d_h^-0.5) [cache V || Vb]      dflash_block_attn
+ *   lens   = accepted prefix                                            dflash_cache_crop
+ *
+ * Conventions shared by every call:
+ *  - Every pointer argument named "device" is CUDA device memory owned by the
+ *    caller. The library never allocates or frees memory.
+ *  - Every call enqueues kernels on the given stream and returns without
+ *    synchronising, except dflash_status_get.
+ *  - Matrices are row-major. Weights use the nn.Linear layout
+ *    [out_features, in_features]; a projection is x W^T. (The walkthrough's
+ *    "W_fc in R^{1536x512}" is the transpose of the fc array passed here.)
+ *  - Element type of every activation, weight, gamma and cache buffer is
+ *    dims->dtype (float32 or bfloat16). Arithmetic is fp32 throughout; bf16
+ *    results are rounded once, when stored.
+ *  - Errors the host can see (null pointers, unsupported dims, a workspace
+ *    that is too small, a misaligned pointer) are returned at once and
+ *    nothing is launched. Errors only the device can see (an append beyond
+ *    the cache capacity or the RoPE table, a crop beyond the current length)
+ *    set bits of a sticky per-device status word and skip the offending
+ *    sequence, leaving its lengths unchanged; dflash_status_get reads them.
+ *  - A launch failure returns DFLASH_ERR_CUDA.
+ *  - Slot j of a sequence's cache holds the row at absolute position j.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DFLASH_OK = 0,
+  DFLASH_ERR_INVALID_ARG = 1,  /* null or misaligned pointer, negative size, bad layer index */
+  DFLASH_ERR_UNSUPPORTED = 2,  /* dims outside the supported set (see dflash_dims) */
+  DFLASH_ERR_WORKSPACE = 3,    /* workspace smaller than dflash_workspace_bytes() asks */
+  DFLASH_ERR_CUDA = 4,         /* a CUDA runtime error while launching */
+  DFLASH_ERR_DEVICE = 5        /* dflash_status_get: the device status word is non-zero */
+} dflash_status;
+
+typedef enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 } dflash_dtype;
+
+/* Bits of the device status word (dflash_status_get). */
+#define DFLASH_DEV_CAPACITY  1u  /* append beyond the cache capacity: sequence skipped */
+#define DFLASH_DEV_ROPE      2u  /* a position beyond the RoPE table: sequence skipped */
+#define DFLASH_DEV_CROP      4u  /* crop to a negative length or beyond the current one */
+#define DFLASH_DEV_ROWS      8u  /* cu_rows not non-decreasing or beyond M */
+
+/*
+ * Model dimensions.
+ *   d          hidden size
+ *   n_h, n_kv  query and key/value heads; G = n_h / n_kv query heads share a
+ *              KV head, query head h reading KV head h / G (DFlash source
+ *              guide (II), part 1: num_key_value_groups)
+ *   d_h        head dimension
+ *   k_layers   number of target layers whose hidden states are concatenated
+ *   block_size block length bs (anchor + mask tokens)
+ *   eps        RMSNorm epsilon (hidden_norm, q_norm, k_norm)
+ *   dtype      dflash_dtype of all tensors
+ * Supported: 1 <= k_layers <= 8; n_h % n_kv == 0; d % 8 == 0.
+ *   bf16: d_h == 128, d % 64 == 0, G * block_size <= 128.
+ *   Both: block_size <= 16.
+ *   f32:  d_h even and <= 256.
+ */
+typedef struct {
+  int d, n_h, n_kv, d_h, k_layers, block_size;
+  float eps;
+  int dtype;
+} dflash_dims;
+
+/*
+ * Draft KV cache, all device memory owned by the caller.
+ *   k, v      [n_layers][batch][n_kv][capacity][d_h] elements of dims->dtype,
+ *             16-byte aligned
+ *   lens      int32 [n_layers][batch]: rows held per layer and sequence
+ * (DFlash source guide (II), part 4: the DynamicCache that update() appends
+ * to and crop(start) truncates.)
+ */
+typedef struct {
+  void* k;
+  void* v;
+  int32_t* lens;
+  int n_layers, batch, capacity;
+} dflash_kv_cache;
+
+/*
+ * Fills a RoPE table: table[p][i] = (cos(p w_i), sin(p w_i)) as float2,
+ * w_i = theta^(-2 i / d_h), for p < max_pos and i < d_h / 2. Angles and
+ * cosines are evaluated in double precision on the device.
+ * (DFlash KV Injection Walkthrough, Step 4.3: cos/sin over the whole window;
+ * Interview Cheat Sheet, section 6.3: the inverse-frequency formula.)
+ *   table  device float [max_pos][d_h/2][2], 8-byte aligned
+ */
+dflash_status dflash_rope_table_build(double theta, int d_h, int max_pos, float* table,
+                                      cudaStream_t stream);
+
+/*
+ * Bytes of scratch memory the calls below need for a cache of `batch`
+ * sequences and `capacity` rows and for at most `max_rows` context rows per
+ * ctx_project / kv_inject call. Pass at least this much as `workspace`.
+ */
+size_t dflash_workspace_bytes(const dflash_dims* dims, int batch, int capacity, int max_rows);
+
+/*
+ * Context signal C = RMSNorm_{gamma_h}(concat[hidden[0] .. hidden[k-1]] W_fc^T).
+ * (DFlash KV Injection Walkthrough, Step 1: extract_context_feature, layers
+ * concatenated on the feature axis in ascending order; Step 2: fc without
+ * bias, then hidden_norm.) The concatenation is never formed: each hidden[j]
+ * is read as the j-th K-segment of the projection.
+ *   hidden     host array of k_layers device pointers, each [M][d]
+ *   M          rows (>= 0; 0 is a no-op)
+ *   W_fc       device [d][k_layers * d]
+ *   gamma_h    device [d]
+ *   C_out      device [M][d]
+ *   workspace  device scratch of ws_bytes bytes, 256-byte aligned
+ */
+dflash_status dflash_ctx_project(const dflash_dims* dims, const void* const* hidden, int M,
+                                 const void* W_fc, const void* gamma_h, void* C_out,
+                                 void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Injects context rows into one layer of the draft cache: for sequence b,
+ * rows cu_rows[b] .. cu_rows[b+1]-1 of C give K = RoPE(KNorm(C W_K^T)) and
+ * V = C W_V^T, written at slots lens[layer][b] .. lens[layer][b] + n_b - 1
+ * (their absolute positions), then lens[layer][b] += n_b.
+ * (DFlash KV Injection Walkthrough, Step 4.2: the same k_proj / v_proj serve
+ * context and block, KNorm per head, V not normalised; Step 4.3: keys rotated
+ * at their true positions; Step 7: accepted rows join the cache as new context.)
+ *   C          device [M][d]
+ *   cu_rows    device int32 [batch + 1], non-decreasing, cu_rows[0] = 0, cu_rows[batch] = M
+ *   W_K, W_V   device [n_kv * d_h][d]
+ *   gamma_k    device [d_h], shared by all heads
+ *   rope_table device table of dflash_rope_table_build, table_len positions
+ * Device errors: capacity or table overflow of a sequence -> status bit, that
+ * sequence is skipped and its length unchanged.
+ */
+dflash_status dflash_kv_inject(const dflash_dims* dims, const dflash_kv_cache* cache, int layer,
+                               const void* C, const int32_t* cu_rows, int M, const void* W_K,
+                               const void* W_V, const void* gamma_k, const float* rope_table,
+                               int table_len, void* workspace, size_t ws_bytes,
+                               cudaStream_t stream);
+
+/*
+ * Block attention of one draft layer. For every sequence b, with start =
+ * lens[layer][b]: the block occupies positions start .. start + bs - 1;
+ * Q = RoPE(QNorm(H_b W_Q^T)), Kb = RoPE(KNorm(H_b W_K^T)), Vb = H_b W_V^T at
+ * those positions; Kb, Vb are appended to the cache (lens += bs, the
+ * reference's update(); the caller crops them away after verification); then
+ * out_b = softmax(Q K^T * scaling) V over every cached row 0 .. start + bs - 1,
+ * non-causal, query head h reading KV head h / G.
+ * (DFlash KV Injection Walkthrough, Steps 4.1-4.4; DFlash source guide (II),
+ * non-causal design note: is_causal False, no mask; part 5: sliding window.)
+ *   H              device [batch][bs][d]
+ *   W_Q            device [n_h * d_h][d];  W_K, W_V device [n_kv * d_h][d]
+ *   gamma_q, gamma_k device [d_h]
+ *   sliding_window 0 = full attention; W > 0: key j is visible to the query
+ *                  at position p iff p - j < W (requires W >= bs)
+ *   scaling        <= 0 selects d_h^-0.5
+ *   out            device [batch][bs][n_h * d_h] (heads concatenated, the
+ *                  layout o_proj consumes, walkthrough Step 4.5)
+ * Device errors: as dflash_kv_inject; a skipped sequence's out rows are zero.
+ */
+dflash_status dflash_block_attn(const dflash_dims* dims, const dflash_kv_cache* cache, int layer,
+                                const void* H, const void* W_Q, const void* W_K, const void* W_V,
+                                const void* gamma_q, const void* gamma_k, const float* rope_table,
+                                int table_len, int sliding_window, float scaling, void* out,
+                                void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * crop(start) on every layer: lens[l][b] = new_lens[b] for all l. No cache
+ * data moves. (DFlash source guide (II), part 4; DFlash KV Injection
+ * Walkthrough, Step 7.) A target that is negative or above a layer's current
+ * length sets DFLASH_DEV_CROP and leaves that layer's length unchanged.
+ *   new_lens  device int32 [batch]
+ */
+dflash_status dflash_cache_crop(const dflash_kv_cache* cache, const int32_t* new_lens,
+                                cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's sticky
+ * status word into *device_status (a mask of DFLASH_DEV_* bits). Returns
+ * DFLASH_OK when the word was zero, DFLASH_ERR_DEVICE when not, and
+ * DFLASH_ERR_CUDA if the synchronisation itself failed.
+ */
+dflash_status dflash_status_get(unsigned int* device_status, cudaStream_t stream);
+
+/* Human-readable name of a dflash_status value (static string). */
+const char* dflash_status_string(dflash_status s);
+
+/*
+ * Kernel tracing (no counterpart on the pages: a measurement aid).
+ * Kernel kinds the library launches, as bit positions of a trace mask:
+ */
+#define DFLASH_KERNEL_GEMM          1  /* projection GEMM (fc, K/V, Q/K/V) */
+#define DFLASH_KERNEL_RMSNORM       2  /* hidden_norm of the context signal */
+#define DFLASH_KERNEL_HEAD_EPILOGUE 3  /* per-head norm, RoPE, cache scatter */
+#define DFLASH_KERNEL_ATTENTION     4  /* block attention over the cache */
+#define DFLASH_KERNEL_COMBINE       5  /* merge of the attention chunks */
+#define DFLASH_KERNEL_LENS          6  /* cache length update */
+#define DFLASH_KERNEL_CROP          7  /* crop */
+#define DFLASH_KERNEL_ROPE_TABLE    8  /* RoPE table fill */
+
+/*
+ * Starts recording a CUDA event pair around every launch whose kind bit
+ * (1u << kind) is set in kernel_mask, on the launch's own stream, for at most
+ * max_launches launches (later ones are not recorded). The events are created
+ * on the first call and kept for the process. Not thread-safe with respect to
+ * concurrent launches from several host threads.
+ */
+dflash_status dflash_trace_start(unsigned int kernel_mask, int max_launches);
+
+/*
+ * Stops recording, waits for the recorded events and writes, for each recorded
+ * launch i < *count, its kind into kinds[i] and its duration in milliseconds
+ * into ms[i] (at most `capacity` entries; *count is the number recorded).
+ */
+dflash_status dflash_trace_stop(int* kinds, float* ms, int capacity, int* count);
+
+/* Number of kernels the library has launched in this process so far. */
+unsigned long long dflash_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_H */

@@ -1,0 +1,357 @@
+// The C ABI: argument checks, scratch carving and kernel launches.
+//
+// Every entry point validates what the host can see, carves its scratch out
+// of the caller's workspace and enqueues kernels on the caller's stream. No
+// entry point allocates, frees or synchronises (dflash_status_get excepted).
+#include <mutex>
+
+#include "dflash_internal.cuh"
+
+namespace dflash {
+
+__device__ unsigned int g_status_word;
+
+unsigned* status_word() {
+  static std::mutex mu;
+  static unsigned* ptr[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptr[dev] = (unsigned*)p;
+  }
+  return ptr[dev];
+}
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+dflash_status check_dims(const dflash_dims* d) {
+  if (!d) return DFLASH_ERR_INVALID_ARG;
+  if (d->d <= 0 || d->n_h <= 0 || d->n_kv <= 0 || d->d_h <= 0 || d->k_layers <= 0 ||
+      d->block_size <= 0 || !(d->eps >= 0.f))
+    return DFLASH_ERR_INVALID_ARG;
+  if (d->dtype != DFLASH_F32 && d->dtype != DFLASH_BF16) return DFLASH_ERR_UNSUPPORTED;
+  if (d->k_layers > 8 || d->n_h % d->n_kv != 0 || d->d % 8 != 0 || d->d_h % 2 != 0)
+    return DFLASH_ERR_UNSUPPORTED;
+  if (d->block_size > 16) return DFLASH_ERR_UNSUPPORTED;
+  if (d->dtype == DFLASH_F32) {
+    if (d->d_h > 256) return DFLASH_ERR_UNSUPPORTED;
+  } else {
+    if (d->d_h != 128 || d->d % 64 != 0 || (d->n_h / d->n_kv) * d->block_size > 128)
+      return DFLASH_ERR_UNSUPPORTED;
+  }
+  return DFLASH_OK;
+}
+
+dflash_status check_cache(const dflash_kv_cache* c, int layer) {
+  if (!c || !c->k || !c->v || !c->lens) return DFLASH_ERR_INVALID_ARG;
+  if (c->n_layers <= 0 || c->batch <= 0 || c->capacity <= 0) return DFLASH_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= c->n_layers) return DFLASH_ERR_INVALID_ARG;
+  if (!aligned16(c->k) || !aligned16(c->v) || ((uintptr_t)c->lens & 3)) return DFLASH_ERR_INVALID_ARG;
+  return DFLASH_OK;
+}
+
+size_t esize(const dflash_dims* d) { return d->dtype == DFLASH_F32 ? 4 : 2; }
+
+dflash_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA; }
+
+// Attention chunking for a cache of `capacity` rows and an optional window.
+void attn_chunks(const dflash_dims* d, int capacity, int window, int* chunk, int* n_chunks) {
+  int range = capacity;
+  if (window > 0 && window + d->block_size - 1 < range) range = window + d->block_size - 1;
+  *chunk = attn_chunk(d->dtype);
+  *n_chunks = (range + *chunk - 1) / *chunk;
+  if (*n_chunks < 1) *n_chunks = 1;
+}
+
+// Scratch of each call, carved in a fixed order (base == nullptr only sizes it).
+struct CtxScratch { float* Y; };
+struct InjectScratch { float* Y; };
+struct BlockScratch { float* Y; void* q; float* part_acc; float2* part_ml; int* counters; };
+
+CtxScratch carve_ctx(Carver& cv, const dflash_dims* d, int M) {
+  CtxScratch s;
+  s.Y = cv.take<float>((size_t)gemm_splits(d->dtype, M, d->d, d->k_layers * d->d) * M * d->d);
+  return s;
+}
+
+InjectScratch carve_inject(Carver& cv, const dflash_dims* d, int M) {
+  InjectScratch s;
+  const int N = 2 * d->n_kv * d->d_h;
+  s.Y = cv.take<float>((size_t)gemm_splits(d->dtype, M, N, d->d) * M * N);
+  return s;
+}
+
+BlockScratch carve_block(Carver& cv, const dflash_dims* d, int batch, int capacity, int window) {
+  BlockScratch s;
+  const int rows = batch * d->block_size;
+  const int N = (d->n_h + 2 * d->n_kv) * d->d_h;
+  int chunk, n_chunks;
+  attn_chunks(d, capacity, window, &chunk, &n_chunks);
+  s.Y = cv.take<float>((size_t)gemm_splits(d->dtype, rows, N, d->d) * rows * N);
+  s.q = cv.take<char>((size_t)batch * d->n_h * d->block_size * d->d_h * esize(d));
+  const size_t part_rows = (size_t)batch * d->n_h * n_chunks * d->block_size;
+  s.part_acc = cv.take<float>(part_rows * d->d_h);
+  s.part_ml = cv.take<float2>(part_rows);
+  s.counters = cv.take<int>((size_t)batch * d->n_kv);
+  return s;
+}
+
+}  // namespace
+}  // namespace dflash
+
+using namespace dflash;
+
+DFLASH_API const char* dflash_status_string(dflash_status s) {
+  switch (s) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_ERR_INVALID_ARG: return "invalid argument";
+    case DFLASH_ERR_UNSUPPORTED: return "unsupported dimensions";
+    case DFLASH_ERR_WORKSPACE: return "workspace too small";
+    case DFLASH_ERR_CUDA: return "CUDA error";
+    case DFLASH_ERR_DEVICE: return "device status word set";
+  }
+  return "unknown status";
+}
+
+DFLASH_API size_t dflash_workspace_bytes(const dflash_dims* d, int batch, int capacity,
+                                         int max_rows) {
+  if (check_dims(d) != DFLASH_OK || batch < 0 || capacity < 0 || max_rows < 0) return 0;
+  size_t need = 256;
+  {
+    Carver cv(nullptr, ~size_t(0));
+    carve_ctx(cv, d, max_rows);
+    need = need > cv.off ? need : cv.off;
+  }
+  {
+    Carver cv(nullptr, ~size_t(0));
+    carve_inject(cv, d, max_rows);
+    need = need > cv.off ? need : cv.off;
+  }
+  {
+    Carver cv(nullptr, ~size_t(0));
+    carve_block(cv, d, batch, capacity, 0);
+    need = need > cv.off ? need : cv.off;
+  }
+  return need;
+}
+
+DFLASH_API dflash_status dflash_rope_table_build(double theta, int d_h, int max_pos, float* table,
+                                                 cudaStream_t stream) {
+  if (!table || d_h <= 0 || d_h % 2 != 0 || max_pos < 0 || !(theta > 0.0) ||
+      ((uintptr_t)table & 7))
+    return DFLASH_ERR_INVALID_ARG;
+  if (max_pos == 0) return DFLASH_OK;
+  return cuda_status(rope_table(theta, d_h, max_pos, table, stream));
+}
+
+DFLASH_API dflash_status dflash_ctx_project(const dflash_dims* d, const void* const* hidden, int M,
+                                            const void* W_fc, const void* gamma_h, void* C_out,
+                                            void* workspace, size_t ws_bytes,
+                                            cudaStream_t stream) {
+  dflash_status st = check_dims(d);
+  if (st != DFLASH_OK) return st;
+  if (M < 0) return DFLASH_ERR_INVALID_ARG;
+  if (M == 0) return DFLASH_OK;
+  if (!hidden || !W_fc || !gamma_h || !C_out || !workspace) return DFLASH_ERR_INVALID_ARG;
+  Segments A;
+  A.n = d->k_layers;
+  A.kseg = d->d;
+  for (int j = 0; j < d->k_layers; ++j) {
+    if (!hidden[j] || !aligned16(hidden[j])) return DFLASH_ERR_INVALID_ARG;
+    A.p[j] = hidden[j];
+  }
+  if (!aligned16(W_fc) || !aligned16(C_out) || ((uintptr_t)workspace & 255))
+    return DFLASH_ERR_INVALID_ARG;
+  Carver cv(workspace, ws_bytes);
+  CtxScratch s = carve_ctx(cv, d, M);
+  if (!cv.ok) return DFLASH_ERR_WORKSPACE;
+  const int splits = gemm_splits(d->dtype, M, d->d, d->k_layers * d->d);
+  Weights W;
+  W.count = 1;
+  W.p[0] = W_fc;
+  W.n[0] = d->d;
+  cudaError_t e = gemm(d->dtype, A, M, W, splits, s.Y, d->d, stream);
+  if (e == cudaSuccess) e = rmsnorm_rows(d->dtype, s.Y, splits, M, d->d, gamma_h, d->eps, C_out, stream);
+  return cuda_status(e);
+}
+
+DFLASH_API dflash_status dflash_kv_inject(const dflash_dims* d, const dflash_kv_cache* c, int layer,
+                                          const void* C, const int32_t* cu_rows, int M,
+                                          const void* W_K, const void* W_V, const void* gamma_k,
+                                          const float* rope, int table_len, void* workspace,
+                                          size_t ws_bytes, cudaStream_t stream) {
+  dflash_status st = check_dims(d);
+  if (st != DFLASH_OK) return st;
+  st = check_cache(c, layer);
+  if (st != DFLASH_OK) return st;
+  if (M < 0 || table_len < 0) return DFLASH_ERR_INVALID_ARG;
+  if (M == 0) return DFLASH_OK;
+  if (!C || !cu_rows || !W_K || !W_V || !gamma_k || !rope || !workspace) return DFLASH_ERR_INVALID_ARG;
+  if (!aligned16(C) || !aligned16(W_K) || !aligned16(W_V) || ((uintptr_t)workspace & 255) ||
+      ((uintptr_t)rope & 7))
+    return DFLASH_ERR_INVALID_ARG;
+  Carver cv(workspace, ws_bytes);
+  InjectScratch s = carve_inject(cv, d, M);
+  if (!cv.ok) return DFLASH_ERR_WORKSPACE;
+  unsigned* status = status_word();
+  if (!status) return DFLASH_ERR_CUDA;
+  const int N = 2 * d->n_kv * d->d_h;
+  const int splits = gemm_splits(d->dtype, M, N, d->d);
+  Segments A;
+  A.n = 1;
+  A.kseg = d->d;
+  A.p[0] = C;
+  const size_t layer_elems = (size_t)c->batch * d->n_kv * c->capacity * d->d_h;
+  const size_t es = esize(d);
+  const int32_t* lens = c->lens + (size_t)layer * c->batch;
+  Weights W;
+  W.count = 2;
+  W.p[0] = W_K;
+  W.p[1] = W_V;
+  W.n[0] = W.n[1] = d->n_kv * d->d_h;
+  cudaError_t e = gemm(d->dtype, A, M, W, splits, s.Y, N, stream);
+  HeadEpilogue ep;
+  ep.Y = s.Y;
+  ep.splits = splits;
+  ep.rows = M;
+  ep.ldY = N;
+  ep.n_q = 0;
+  ep.n_kv = d->n_kv;
+  ep.d_h = d->d_h;
+  ep.eps = d->eps;
+  ep.gamma_q = nullptr;
+  ep.gamma_k = gamma_k;
+  ep.rope = (const float2*)rope;
+  ep.table_len = table_len;
+  ep.cu_rows = cu_rows;
+  ep.batch = c->batch;
+  ep.bs = 0;
+  ep.lens = lens;
+  ep.q_out = nullptr;
+  ep.cache_k = (char*)c->k + (size_t)layer * layer_elems * es;
+  ep.cache_v = (char*)c->v + (size_t)layer * layer_elems * es;
+  ep.capacity = c->capacity;
+  ep.status = status;
+  if (e == cudaSuccess) e = head_epilogue(d->dtype, ep, stream);
+  if (e == cudaSuccess)
+    e = lens_advance(c->lens + (size_t)layer * c->batch, cu_rows, c->batch, 0, M, c->capacity,
+                     table_len, stream);
+  return cuda_status(e);
+}
+
+DFLASH_API dflash_status dflash_block_attn(const dflash_dims* d, const dflash_kv_cache* c,
+                                           int layer, const void* H, const void* W_Q,
+                                           const void* W_K, const void* W_V, const void* gamma_q,
+                                           const void* gamma_k, const float* rope, int table_len,
+                                           int window, float scaling, void* out, void* workspace,
+                                           size_t ws_bytes, cudaStream_t stream) {
+  dflash_status st = check_dims(d);
+  if (st != DFLASH_OK) return st;
+  st = check_cache(c, layer);
+  if (st != DFLASH_OK) return st;
+  if (table_len < 0 || window < 0) return DFLASH_ERR_INVALID_ARG;
+  if (window > 0 && window < d->block_size) return DFLASH_ERR_INVALID_ARG;
+  if (!H || !W_Q || !W_K || !W_V || !gamma_q || !gamma_k || !rope || !out || !workspace)
+    return DFLASH_ERR_INVALID_ARG;
+  if (!aligned16(H) || !aligned16(W_Q) || !aligned16(W_K) || !aligned16(W_V) || !aligned16(out) ||
+      ((uintptr_t)workspace & 255) || ((uintptr_t)rope & 7))
+    return DFLASH_ERR_INVALID_ARG;
+  Carver cv(workspace, ws_bytes);
+  BlockScratch s = carve_block(cv, d, c->batch, c->capacity, window);
+  if (!cv.ok) return DFLASH_ERR_WORKSPACE;
+  unsigned* status = status_word();
+  if (!status) return DFLASH_ERR_CUDA;
+  const int rows = c->batch * d->block_size;
+  const int nq = d->n_h * d->d_h, nkv = d->n_kv * d->d_h;
+  const int N = nq + 2 * nkv;
+  const int splits = gemm_splits(d->dtype, rows, N, d->d);
+  Segments A;
+  A.n = 1;
+  A.kseg = d->d;
+  A.p[0] = H;
+  const size_t layer_elems = (size_t)c->batch * d->n_kv * c->capacity * d->d_h;
+  const size_t es = esize(d);
+  void* ck = (char*)c->k + (size_t)layer * layer_elems * es;
+  void* cvv = (char*)c->v + (size_t)layer * layer_elems * es;
+  int32_t* lens = c->lens + (size_t)layer * c->batch;
+  Weights W;
+  W.count = 3;
+  W.p[0] = W_Q;
+  W.p[1] = W_K;
+  W.p[2] = W_V;
+  W.n[0] = nq;
+  W.n[1] = W.n[2] = nkv;
+  cudaError_t e = gemm(d->dtype, A, rows, W, splits, s.Y, N, stream);
+  HeadEpilogue ep;
+  ep.Y = s.Y;
+  ep.splits = splits;
+  ep.rows = rows;
+  ep.ldY = N;
+  ep.n_q = d->n_h;
+  ep.n_kv = d->n_kv;
+  ep.d_h = d->d_h;
+  ep.eps = d->eps;
+  ep.gamma_q = gamma_q;
+  ep.gamma_k = gamma_k;
+  ep.rope = (const float2*)rope;
+  ep.table_len = table_len;
+  ep.cu_rows = nullptr;
+  ep.batch = c->batch;
+  ep.bs = d->block_size;
+  ep.lens = lens;
+  ep.q_out = s.q;
+  ep.cache_k = ck;
+  ep.cache_v = cvv;
+  ep.capacity = c->capacity;
+  ep.status = status;
+  if (e == cudaSuccess) e = head_epilogue(d->dtype, ep, stream);
+  AttnParams p;
+  p.q = s.q;
+  p.cache_k = ck;
+  p.cache_v = cvv;
+  p.lens = lens;
+  p.out = out;
+  p.part_acc = s.part_acc;
+  p.part_ml = s.part_ml;
+  p.counters = s.counters;
+  p.batch = c->batch;
+  p.n_h = d->n_h;
+  p.n_kv = d->n_kv;
+  p.d_h = d->d_h;
+  p.bs = d->block_size;
+  p.capacity = c->capacity;
+  p.window = window;
+  attn_chunks(d, c->capacity, window, &p.chunk, &p.n_chunks);
+  p.table_len = table_len;
+  p.scaling = scaling > 0.f ? scaling : 1.0f / sqrtf((float)d->d_h);
+  if (e == cudaSuccess)
+    e = attention(d->dtype, p, stream);
+  if (e == cudaSuccess)
+    e = lens_advance(lens, nullptr, c->batch, d->block_size, rows, c->capacity, table_len, stream);
+  return cuda_status(e);
+}
+
+DFLASH_API dflash_status dflash_cache_crop(const dflash_kv_cache* c, const int32_t* new_lens,
+                                           cudaStream_t stream) {
+  dflash_status st = check_cache(c, 0);
+  if (st != DFLASH_OK) return st;
+  if (!new_lens || ((uintptr_t)new_lens & 3)) return DFLASH_ERR_INVALID_ARG;
+  unsigned* status = status_word();
+  if (!status) return DFLASH_ERR_CUDA;
+  return cuda_status(crop_lens(c->lens, c->n_layers, c->batch, new_lens, status, stream));
+}
+
+DFLASH_API dflash_status dflash_status_get(unsigned int* out, cudaStream_t stream) {
+  if (!out) return DFLASH_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DFLASH_ERR_CUDA;
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return DFLASH_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return DFLASH_ERR_CUDA;
+  *out = v;
+  return v ? DFLASH_ERR_DEVICE : DFLASH_OK;
+}

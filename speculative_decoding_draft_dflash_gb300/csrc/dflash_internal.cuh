@@ -1,0 +1,160 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "dflash.h"
+
+#define DFLASH_API extern "C" __attribute__((visibility("default")))
+
+namespace dflash {
+
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------------------
+// element conversions
+// ---------------------------------------------------------------------------
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<bf16>(bf16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// scratch carving: every piece 256-byte aligned
+// ---------------------------------------------------------------------------
+struct Carver {
+  char* base;
+  size_t cap;
+  size_t off = 0;
+  bool ok = true;
+  Carver(void* b, size_t c) : base((char*)b), cap(c) {}
+  template <typename T> T* take(size_t count) {
+    size_t bytes = (count * sizeof(T) + 255) & ~size_t(255);
+    if (off + bytes > cap) { ok = false; return nullptr; }
+    T* p = base ? (T*)(base + off) : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+// per-device sticky status word (defined in dflash_api.cu)
+unsigned* status_word();
+
+// Brackets one kernel launch: counts it and, while tracing selects its kind,
+// records CUDA events around it on its stream (trace.cu).
+class LaunchScope {
+ public:
+  LaunchScope(int kind, cudaStream_t s);
+  ~LaunchScope();
+ private:
+  int kind_;
+  cudaStream_t stream_;
+  int slot_;
+};
+
+// ---------------------------------------------------------------------------
+// GEMM: Y[split][M][N] (fp32) = X[M][K] W[N][K]^T, X given as K-segments
+// ---------------------------------------------------------------------------
+struct Segments {
+  const void* p[8];  // n device pointers, each [M][kseg]
+  int n;
+  int kseg;
+};
+
+// Weights stacked along N: columns [off_i, off_i + N_i) of Y come from Ws[i] ([N_i][K]).
+struct Weights {
+  const void* p[3];
+  int n[3];
+  int count;
+  __host__ __device__ int total() const { int t = 0; for (int i = 0; i < count; ++i) t += n[i]; return t; }
+};
+
+// Number of K-splits the GEMM of this shape uses (partials summed by the epilogue).
+int gemm_splits(int dtype, int M, int N, int K);
+
+// Y[split][M][ldY] (fp32) = X W^T. f32: SIMT FFMA; bf16: tensor cores.
+cudaError_t gemm(int dtype, const Segments& A, int M, const Weights& W, int splits, float* Y,
+                 int ldY, cudaStream_t s);
+
+// SIMT fp32-accumulating GEMM for any M, N, K (the f32 path).
+cudaError_t gemm_simt(int dtype, const Segments& A, int M, const Weights& W, float* Y, int ldY,
+                      cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// epilogues
+// ---------------------------------------------------------------------------
+// C[row][:] = RMSNorm_gamma(sum_s Y[s][row][:])
+cudaError_t rmsnorm_rows(int dtype, const float* Y, int splits, int M, int N, const void* gamma,
+                         float eps, void* out, cudaStream_t s);
+
+// Per-head epilogue of a projection whose N axis is [n_q Q heads | n_kv K heads | n_kv V heads].
+struct HeadEpilogue {
+  const float* Y;       // [splits][rows][ldY]
+  int splits, rows, ldY;
+  int n_q, n_kv, d_h;
+  float eps;
+  const void* gamma_q;  // [d_h] (Q heads)
+  const void* gamma_k;  // [d_h] (K heads)
+  const float2* rope;   // [table_len][d_h/2]
+  int table_len;
+  // rows -> sequences: cu_rows != nullptr: rows grouped by cu_rows[batch+1];
+  // else row = b * bs + t
+  const int32_t* cu_rows;
+  int batch, bs;
+  const int32_t* lens;  // [batch] for this layer
+  void* q_out;          // [batch][n_q][bs][d_h]
+  void* cache_k;        // layer base [batch][n_kv][capacity][d_h]
+  void* cache_v;
+  int capacity;
+  unsigned* status;
+};
+cudaError_t head_epilogue(int dtype, const HeadEpilogue& e, cudaStream_t s);
+
+// lens[b] += n_b where the append fitted (same checks as the epilogue)
+cudaError_t lens_advance(int32_t* lens, const int32_t* cu_rows, int batch, int bs, int M,
+                         int capacity, int table_len, cudaStream_t s);
+
+cudaError_t crop_lens(int32_t* lens, int n_layers, int batch, const int32_t* new_lens,
+                      unsigned* status, cudaStream_t s);
+
+cudaError_t rope_table(double theta, int d_h, int max_pos, float* table, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// attention
+// ---------------------------------------------------------------------------
+struct AttnParams {
+  const void* q;          // [batch][n_h][bs][d_h]
+  const void* cache_k;    // layer base [batch][n_kv][capacity][d_h]
+  const void* cache_v;
+  const int32_t* lens;    // [batch], BEFORE the block's lens advance
+  void* out;              // [batch][bs][n_h * d_h]
+  float* part_acc;        // partial accumulators, per chunk
+  float2* part_ml;        // partial (max, sum), per chunk
+  int* counters;          // [batch][n_kv] chunk-completion counters (zero between calls)
+  int batch, n_h, n_kv, d_h, bs, capacity, window, chunk, n_chunks, table_len;
+  float scaling;
+};
+int attn_simt_chunk();
+cudaError_t attn_simt(int dtype, const AttnParams& p, cudaStream_t s);
+
+// Keys per attention chunk and the attention launch for a dtype.
+int attn_chunk(int dtype);
+cudaError_t attention(int dtype, const AttnParams& p, cudaStream_t s);
+
+}  // namespace dflash

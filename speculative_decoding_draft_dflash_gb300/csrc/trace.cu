@@ -1,0 +1,85 @@
+// Kernel tracing: CUDA event pairs around selected launches, and a launch counter.
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "dflash_internal.cuh"
+
+namespace dflash {
+namespace {
+
+struct TraceState {
+  std::mutex mu;
+  bool active = false;
+  unsigned mask = 0;
+  int max_launches = 0;
+  int count = 0;
+  std::vector<cudaEvent_t> events;  // 2 per launch
+  std::vector<int> kinds;
+};
+
+TraceState& state() {
+  static TraceState s;
+  return s;
+}
+
+std::atomic<unsigned long long> g_launches{0};
+
+}  // namespace
+
+LaunchScope::LaunchScope(int kind, cudaStream_t s) : kind_(kind), stream_(s), slot_(-1) {
+  TraceState& t = state();
+  if (!t.active || !(t.mask & (1u << kind))) return;
+  std::lock_guard<std::mutex> lock(t.mu);
+  if (!t.active || t.count >= t.max_launches) return;
+  slot_ = t.count++;
+  t.kinds[slot_] = kind;
+  cudaEventRecord(t.events[2 * slot_], s);
+}
+
+LaunchScope::~LaunchScope() {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (slot_ < 0) return;
+  cudaEventRecord(state().events[2 * slot_ + 1], stream_);
+}
+
+}  // namespace dflash
+
+using namespace dflash;
+
+DFLASH_API dflash_status dflash_trace_start(unsigned int kernel_mask, int max_launches) {
+  if (max_launches < 0) return DFLASH_ERR_INVALID_ARG;
+  TraceState& t = state();
+  std::lock_guard<std::mutex> lock(t.mu);
+  while ((int)t.events.size() < 2 * max_launches) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return DFLASH_ERR_CUDA;
+    t.events.push_back(e);
+  }
+  if ((int)t.kinds.size() < max_launches) t.kinds.resize(max_launches);
+  t.mask = kernel_mask;
+  t.max_launches = max_launches;
+  t.count = 0;
+  t.active = true;
+  return DFLASH_OK;
+}
+
+DFLASH_API dflash_status dflash_trace_stop(int* kinds, float* ms, int capacity, int* count) {
+  TraceState& t = state();
+  std::lock_guard<std::mutex> lock(t.mu);
+  t.active = false;
+  if (count) *count = t.count;
+  for (int i = 0; i < t.count && i < capacity; ++i) {
+    if (cudaEventSynchronize(t.events[2 * i + 1]) != cudaSuccess) return DFLASH_ERR_CUDA;
+    float v = 0.f;
+    if (cudaEventElapsedTime(&v, t.events[2 * i], t.events[2 * i + 1]) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+    if (kinds) kinds[i] = t.kinds[i];
+    if (ms) ms[i] = v;
+  }
+  return DFLASH_OK;
+}
+
+DFLASH_API unsigned long long dflash_launch_count(void) {
+  return g_launches.load(std::memory_order_relaxed);
+}

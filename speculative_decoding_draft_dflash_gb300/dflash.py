@@ -1,0 +1,221 @@
+"""ctypes binding of libdflash.so: the C ABI of include/dflash.h, call for call.
+
+Each function marshals torch tensors (device memory) into the C call with the
+same name and raises ``DFlashError`` on a non-OK status. Nothing here
+computes: every step runs in the library's CUDA kernels. There is no CPU
+fallback; if libdflash.so is missing the import fails.
+
+Streams: every call runs on ``torch.cuda.current_stream()`` unless a
+``stream`` (a torch.cuda.Stream or a raw handle) is given.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_double, c_float, c_int, c_size_t, c_uint, c_void_p
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdflash.so")
+
+DFLASH_F32, DFLASH_BF16 = 0, 1
+DEV_CAPACITY, DEV_ROPE, DEV_CROP, DEV_ROWS = 1, 2, 4, 8
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE = range(6)
+KERNEL_NAMES = {1: "gemm", 2: "rmsnorm", 3: "head_epilogue", 4: "attention", 5: "combine",
+                6: "lens", 7: "crop", 8: "rope_table"}
+KERNEL_IDS = {v: k for k, v in KERNEL_NAMES.items()}
+
+
+class DFlashError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+class dflash_dims(ctypes.Structure):
+    _fields_ = [("d", c_int), ("n_h", c_int), ("n_kv", c_int), ("d_h", c_int),
+                ("k_layers", c_int), ("block_size", c_int), ("eps", c_float), ("dtype", c_int)]
+
+
+class dflash_kv_cache(ctypes.Structure):
+    _fields_ = [("k", c_void_p), ("v", c_void_p), ("lens", c_void_p), ("n_layers", c_int),
+                ("batch", c_int), ("capacity", c_int)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libdflash.so is not built ({LIB_PATH}); run "
+                          "speculative_decoding_draft_dflash_gb300.build.build() first")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = c_void_p
+    sig = {
+        "dflash_rope_table_build": (c_int, [c_double, c_int, c_int, P, P]),
+        "dflash_workspace_bytes": (c_size_t, [P, c_int, c_int, c_int]),
+        "dflash_ctx_project": (c_int, [P, P, c_int, P, P, P, P, c_size_t, P]),
+        "dflash_kv_inject": (c_int, [P, P, c_int, P, P, c_int, P, P, P, P, c_int, P, c_size_t, P]),
+        "dflash_block_attn": (c_int, [P, P, c_int, P, P, P, P, P, P, P, c_int, c_int, c_float, P, P,
+                                      c_size_t, P]),
+        "dflash_cache_crop": (c_int, [P, P, P]),
+        "dflash_status_get": (c_int, [POINTER(c_uint), P]),
+        "dflash_status_string": (ctypes.c_char_p, [c_int]),
+        "dflash_trace_start": (c_int, [c_uint, c_int]),
+        "dflash_trace_stop": (c_int, [P, P, c_int, P]),
+        "dflash_launch_count": (ctypes.c_ulonglong, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _stream(stream):
+    if stream is None:
+        return c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return c_void_p(stream.cuda_stream)
+    return c_void_p(int(stream))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return c_void_p(t)
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return c_void_p(t.data_ptr())
+
+
+def _check(st, where):
+    if st != OK:
+        raise DFlashError(st, where)
+
+
+def dtype_code(dtype):
+    if dtype in (torch.float32, "f32", DFLASH_F32):
+        return DFLASH_F32
+    if dtype in (torch.bfloat16, "bf16", DFLASH_BF16):
+        return DFLASH_BF16
+    raise ValueError(f"unsupported dtype {dtype}")
+
+
+def torch_dtype(code):
+    return torch.float32 if code == DFLASH_F32 else torch.bfloat16
+
+
+def make_dims(d, n_h, n_kv, d_h, k_layers, block_size, eps=1e-6, dtype=DFLASH_BF16):
+    return dflash_dims(d, n_h, n_kv, d_h, k_layers, block_size, eps, dtype_code(dtype))
+
+
+class KVCache:
+    """Device buffers of a draft KV cache (allocated by torch) and their C descriptor.
+
+    k, v: [n_layers][batch][n_kv][capacity][d_h]; lens: int32 [n_layers][batch].
+    """
+
+    def __init__(self, n_layers, batch, n_kv, capacity, d_h, dtype, device="cuda"):
+        td = torch_dtype(dtype_code(dtype))
+        shape = (n_layers, batch, n_kv, capacity, d_h)
+        self.k = torch.zeros(shape, dtype=td, device=device)
+        self.v = torch.zeros(shape, dtype=td, device=device)
+        self.lens = torch.zeros((n_layers, batch), dtype=torch.int32, device=device)
+        self.n_layers, self.batch, self.capacity = n_layers, batch, capacity
+        self.desc = dflash_kv_cache(self.k.data_ptr(), self.v.data_ptr(), self.lens.data_ptr(),
+                                    n_layers, batch, capacity)
+
+
+# ---------------------------------------------------------------------------
+# the C calls
+# ---------------------------------------------------------------------------
+
+def status_string(st):
+    return _lib.dflash_status_string(int(st)).decode()
+
+
+def dflash_rope_table_build(theta, d_h, max_pos, table, stream=None):
+    _check(_lib.dflash_rope_table_build(float(theta), int(d_h), int(max_pos), _ptr(table),
+                                        _stream(stream)), "dflash_rope_table_build")
+
+
+def dflash_workspace_bytes(dims, batch, capacity, max_rows):
+    return int(_lib.dflash_workspace_bytes(ctypes.byref(dims), int(batch), int(capacity),
+                                           int(max_rows)))
+
+
+def dflash_ctx_project(dims, hidden, M, W_fc, gamma_h, C_out, workspace, stream=None):
+    ptrs = (c_void_p * max(1, len(hidden)))(*[t.data_ptr() if hasattr(t, "data_ptr") else int(t)
+                                             for t in hidden])
+    _check(_lib.dflash_ctx_project(ctypes.byref(dims), ptrs, int(M), _ptr(W_fc), _ptr(gamma_h),
+                                   _ptr(C_out), _ptr(workspace), workspace.numel() *
+                                   workspace.element_size(), _stream(stream)),
+           "dflash_ctx_project")
+
+
+def dflash_kv_inject(dims, cache, layer, C, cu_rows, M, W_K, W_V, gamma_k, rope_table, table_len,
+                     workspace, stream=None):
+    desc = cache.desc if isinstance(cache, KVCache) else cache
+    _check(_lib.dflash_kv_inject(ctypes.byref(dims), ctypes.byref(desc), int(layer), _ptr(C),
+                                 _ptr(cu_rows), int(M), _ptr(W_K), _ptr(W_V), _ptr(gamma_k),
+                                 _ptr(rope_table), int(table_len), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)),
+           "dflash_kv_inject")
+
+
+def dflash_block_attn(dims, cache, layer, H, W_Q, W_K, W_V, gamma_q, gamma_k, rope_table,
+                      table_len, sliding_window, scaling, out, workspace, stream=None):
+    desc = cache.desc if isinstance(cache, KVCache) else cache
+    _check(_lib.dflash_block_attn(ctypes.byref(dims), ctypes.byref(desc), int(layer), _ptr(H),
+                                  _ptr(W_Q), _ptr(W_K), _ptr(W_V), _ptr(gamma_q), _ptr(gamma_k),
+                                  _ptr(rope_table), int(table_len), int(sliding_window),
+                                  float(scaling), _ptr(out), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)),
+           "dflash_block_attn")
+
+
+def dflash_cache_crop(cache, new_lens, stream=None):
+    desc = cache.desc if isinstance(cache, KVCache) else cache
+    _check(_lib.dflash_cache_crop(ctypes.byref(desc), _ptr(new_lens), _stream(stream)),
+           "dflash_cache_crop")
+
+
+def dflash_status_get(stream=None):
+    """Synchronises the stream; returns the device status bits (0 = clean) and clears them."""
+    v = c_uint(0)
+    st = _lib.dflash_status_get(ctypes.byref(v), _stream(stream))
+    if st not in (OK, ERR_DEVICE):
+        raise DFlashError(st, "dflash_status_get")
+    return int(v.value)
+
+
+def dflash_trace_start(kinds, max_launches):
+    """Records CUDA events around launches of the given kernel kinds (names or ids)."""
+    mask = 0
+    for k in kinds:
+        mask |= 1 << (KERNEL_IDS[k] if isinstance(k, str) else int(k))
+    _check(_lib.dflash_trace_start(mask, int(max_launches)), "dflash_trace_start")
+
+
+def dflash_trace_stop(capacity=1 << 16):
+    """Returns [(kernel name, milliseconds)] of the launches recorded since dflash_trace_start."""
+    kinds = (c_int * capacity)()
+    ms = (c_float * capacity)()
+    n = c_int(0)
+    _check(_lib.dflash_trace_stop(kinds, ms, capacity, ctypes.byref(n)), "dflash_trace_stop")
+    return [(KERNEL_NAMES.get(kinds[i], str(kinds[i])), float(ms[i]))
+            for i in range(min(n.value, capacity))]
+
+
+def dflash_launch_count():
+    return int(_lib.dflash_launch_count())

@@ -1,0 +1,73 @@
+"""Device (C ABI) against the float64 oracle, element by element, on seeded inputs.
+
+Small workloads run every sequence through the oracle; the full-size workloads
+run the same launch configuration as the benchmark and check a seeded sample
+of sequences (every output row depends on its own sequence only).
+"""
+import numpy as np
+import pytest
+
+from speculative_decoding_draft_dflash_gb300 import synth
+import harness
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+
+SMALL = {
+    # G = 4, two layers (one windowed at 64), several 256-key chunks with ragged tails,
+    # an empty cache (length 0) among them, random gammas.
+    "small_gqa_bf16": W["serve_b32"].replace(
+        name="small_gqa_bf16", d=512, n_h=8, n_kv=2, k=2, batch=4, n_layers=2, windows=(0, 64),
+        prefill_lo=0, prefill_hi=700, seed=3, random_gamma=True),
+    # G = 1 (MHA), odd block size, prefill by projection + inject of real rows.
+    "small_mha_bf16": W["qwen3_8b_b1"].replace(
+        name="small_mha_bf16", d=256, n_h=4, n_kv=4, k=1, bs=5, batch=2, prefill_lo=300,
+        prefill_hi=300, new_ctx=7, rounds=2, seed=4, random_gamma=True),
+    # G = 8, block of 16 -> 128 stacked query rows; block size 1 in the f32 variant below.
+    "small_g8_bf16": W["serve_b32"].replace(
+        name="small_g8_bf16", d=256, n_h=16, n_kv=2, k=3, batch=3, n_layers=1, windows=(16,),
+        prefill_lo=1, prefill_hi=513, seed=5),
+    "small_gqa_f32": W["walkthrough_f32"].replace(
+        name="small_gqa_f32", d=96, n_h=6, n_kv=2, d_h=32, k=2, bs=3, batch=3, n_layers=2,
+        windows=(0, 5), prefill_lo=0, prefill_hi=600, new_ctx=4, rounds=2, seed=6,
+        random_gamma=True),
+    "small_bs1_f32": W["walkthrough_f32"].replace(
+        name="small_bs1_f32", d=64, n_h=2, n_kv=1, d_h=64, k=1, bs=1, batch=2, n_layers=1,
+        windows=(0,), prefill_lo=255, prefill_hi=257, new_ctx=1, rounds=2, seed=7),
+}
+
+
+def _run(w, seqs):
+    dev_res, dev = harness.device_rounds(w, seqs)
+    ora_res = harness.oracle_rounds(w, seqs)
+    return harness.compare(w, dev_res, ora_res, seqs)
+
+
+def test_walkthrough_f32():
+    """The walkthrough's example end to end: lengths 0 -> 3 -> 7 -> 3 -> 6 -> 10 -> 6."""
+    w = W["walkthrough_f32"]
+    _run(w, [0])
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_workloads(name):
+    w = SMALL[name]
+    _run(w, list(range(w.batch)))
+
+
+def _sample(w, n, seed=11):
+    L = synth.prefill_lens(w)
+    picks = {int(np.argmin(L)), int(np.argmax(L))}
+    rng = np.random.default_rng(seed)
+    while len(picks) < min(n, w.batch):
+        picks.add(int(rng.integers(0, w.batch)))
+    return sorted(picks)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,n", [("qwen3_8b_b1", 1), ("serve_b32", 4), ("long_ctx_b4", 2),
+                                    ("hybrid_swa_b64", 3)])
+def test_full_size(name, n):
+    w = W[name]
+    _run(w, _sample(w, n))
