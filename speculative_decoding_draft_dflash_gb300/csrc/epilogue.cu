@@ -62,7 +62,7 @@ __global__ void head_epilogue_kernel(HeadEpilogue e) {
     b = lo;
     t = row - e.cu_rows[b];
     n_b = e.cu_rows[b + 1] - e.cu_rows[b];
-    if (n_b < 0 || e.cu_rows[b + 1] > e.rows || e.cu_rows[0] != 0) {
+    if (n_b < 0 || e.cu_rows[b + 1] > e.rows || e.cu_rows[0] != 0 || t < 0 || t >= n_b) {
       if (threadIdx.x == 0) atomicOr(e.status, DFLASH_DEV_ROWS);
       return;
     }
