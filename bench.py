@@ -135,7 +135,7 @@ def attention_bytes(w, starts):
     kv = rows * w.n_kv * w.d_h * 2 * e
     q = w.batch * w.n_h * w.bs * w.d_h * e
     out = w.batch * w.bs * w.n_h * w.d_h * e
-    return kv + q + out
+    return int(kv + q + out)
 
 
 def gemm_cost(M, K, N):
@@ -206,7 +206,13 @@ def run_reference(args, w):
             "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
+    print(json.dumps(line, default=_json_default), flush=True)
+
+
+def _json_default(o):
+    if hasattr(o, "item"):
+        return o.item()
+    raise TypeError(f"not JSON serialisable: {type(o)}")
 
 
 def config_of(w):
@@ -348,7 +354,7 @@ def run_ours(args, w):
                                 "sample": f"{n} whole-sequence rounds of {w.name} "
                                           f"({total:.1f} s, float64 NumPy, default BLAS threads)"}
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        print(json.dumps(line, default=_json_default), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
