@@ -131,6 +131,31 @@ dflash_status dflash_ctx_project(const dflash_dims* dims, const void* const* hid
                                  void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * dflash_ctx_project for callers that cannot allocate device memory: the
+ * source pages have no counterpart to this call; it exists for code that runs
+ * inside another runtime's launch path (a custom operator's enqueue in an
+ * inference server, for example), where that runtime owns all device memory
+ * and a cudaMalloc would break its accounting and stall the device. Same
+ * arguments and results as dflash_ctx_project, minus the workspace: the
+ * scratch is a fixed array of DFLASH_NOALLOC_SCRATCH_BYTES inside the library,
+ * held on every GPU that loads it until the process exits (about 4M fp32
+ * values: 1024 rows at d = 4096 in one pass).
+ *  - No allocation of any kind happens in this call.
+ *  - A call needing more scratch than the array returns DFLASH_ERR_WORKSPACE
+ *    and launches nothing.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array, which keeps whatever the
+ *    previous call left in it (nothing in it needs to start at zero). Calls
+ *    that can run at the same time on the GPU (other streams, other host
+ *    threads) race on it: serialise them.
+ */
+#define DFLASH_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+dflash_status dflash_ctx_project_noalloc(const dflash_dims* dims, const void* const* hidden, int M,
+                                         const void* W_fc, const void* gamma_h, void* C_out,
+                                         cudaStream_t stream);
+
+/*
  * Injects context rows into one layer of the draft cache: for sequence b,
  * rows cu_rows[b] .. cu_rows[b+1]-1 of C give K = RoPE(KNorm(C W_K^T)) and
  * V = C W_V^T, written at slots lens[layer][b] .. lens[layer][b] + n_b - 1

@@ -54,6 +54,7 @@ def _load():
         "dflash_rope_table_build": (c_int, [c_double, c_int, c_int, P, P]),
         "dflash_workspace_bytes": (c_size_t, [P, c_int, c_int, c_int]),
         "dflash_ctx_project": (c_int, [P, P, c_int, P, P, P, P, c_size_t, P]),
+        "dflash_ctx_project_noalloc": (c_int, [P, P, c_int, P, P, P, P]),
         "dflash_kv_inject": (c_int, [P, P, c_int, P, P, c_int, P, P, P, P, c_int, P, c_size_t, P]),
         "dflash_block_attn": (c_int, [P, P, c_int, P, P, P, P, P, P, P, c_int, c_int, c_float, P, P,
                                       c_size_t, P]),
@@ -161,6 +162,15 @@ def dflash_ctx_project(dims, hidden, M, W_fc, gamma_h, C_out, workspace, stream=
                                    _ptr(C_out), _ptr(workspace), workspace.numel() *
                                    workspace.element_size(), _stream(stream)),
            "dflash_ctx_project")
+
+
+def dflash_ctx_project_noalloc(dims, hidden, M, W_fc, gamma_h, C_out, stream=None):
+    """dflash_ctx_project with the library's fixed scratch array instead of a workspace."""
+    ptrs = (c_void_p * max(1, len(hidden)))(*[t.data_ptr() if hasattr(t, "data_ptr") else int(t)
+                                             for t in hidden])
+    _check(_lib.dflash_ctx_project_noalloc(ctypes.byref(dims), ptrs, int(M), _ptr(W_fc),
+                                           _ptr(gamma_h), _ptr(C_out), _stream(stream)),
+           "dflash_ctx_project_noalloc")
 
 
 def dflash_kv_inject(dims, cache, layer, C, cu_rows, M, W_K, W_V, gamma_k, rope_table, table_len,
