@@ -57,6 +57,7 @@ typedef enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 } dflash_dtype;
 #define DFLASH_DEV_ROPE      2u  /* a position beyond the RoPE table: sequence skipped */
 #define DFLASH_DEV_CROP      4u  /* crop to a negative length or beyond the current one */
 #define DFLASH_DEV_ROWS      8u  /* cu_rows not non-decreasing or beyond M */
+#define DFLASH_DEV_TIMEOUT  16u  /* an internal pipeline wait gave up (kernel returned early) */
 
 /*
  * Model dimensions.

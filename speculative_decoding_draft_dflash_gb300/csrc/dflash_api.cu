@@ -68,21 +68,50 @@ void attn_chunks(const dflash_dims* d, int capacity, int window, int* chunk, int
   if (*n_chunks < 1) *n_chunks = 1;
 }
 
+// Shapes of the stacked weights of each projection (pointers filled by the caller).
+Weights ctx_weights(const dflash_dims* d, const void* W_fc) {
+  Weights W;
+  W.count = 1;
+  W.p[0] = W_fc;
+  W.n[0] = d->d;
+  return W;
+}
+Weights kv_weights(const dflash_dims* d, const void* W_K, const void* W_V) {
+  Weights W;
+  W.count = 2;
+  W.p[0] = W_K;
+  W.p[1] = W_V;
+  W.n[0] = W.n[1] = d->n_kv * d->d_h;
+  return W;
+}
+Weights qkv_weights(const dflash_dims* d, const void* W_Q, const void* W_K, const void* W_V) {
+  Weights W;
+  W.count = 3;
+  W.p[0] = W_Q;
+  W.p[1] = W_K;
+  W.p[2] = W_V;
+  W.n[0] = d->n_h * d->d_h;
+  W.n[1] = W.n[2] = d->n_kv * d->d_h;
+  return W;
+}
+
 // Scratch of each call, carved in a fixed order (base == nullptr only sizes it).
-struct CtxScratch { float* Y; };
-struct InjectScratch { float* Y; };
-struct BlockScratch { float* Y; void* q; float* part_acc; float2* part_ml; int* counters; };
+struct CtxScratch { float* Y; int splits; };
+struct InjectScratch { float* Y; int splits; };
+struct BlockScratch { float* Y; int splits; void* q; float* part_acc; float2* part_ml; int* counters; };
 
 CtxScratch carve_ctx(Carver& cv, const dflash_dims* d, int M) {
   CtxScratch s;
-  s.Y = cv.take<float>((size_t)gemm_splits(d->dtype, M, d->d, d->k_layers * d->d) * M * d->d);
+  s.splits = gemm_splits(d->dtype, M, ctx_weights(d, nullptr), d->k_layers * d->d);
+  s.Y = cv.take<float>((size_t)s.splits * M * d->d);
   return s;
 }
 
 InjectScratch carve_inject(Carver& cv, const dflash_dims* d, int M) {
   InjectScratch s;
   const int N = 2 * d->n_kv * d->d_h;
-  s.Y = cv.take<float>((size_t)gemm_splits(d->dtype, M, N, d->d) * M * N);
+  s.splits = gemm_splits(d->dtype, M, kv_weights(d, nullptr, nullptr), d->d);
+  s.Y = cv.take<float>((size_t)s.splits * M * N);
   return s;
 }
 
@@ -92,7 +121,8 @@ BlockScratch carve_block(Carver& cv, const dflash_dims* d, int batch, int capaci
   const int N = (d->n_h + 2 * d->n_kv) * d->d_h;
   int chunk, n_chunks;
   attn_chunks(d, capacity, window, &chunk, &n_chunks);
-  s.Y = cv.take<float>((size_t)gemm_splits(d->dtype, rows, N, d->d) * rows * N);
+  s.splits = gemm_splits(d->dtype, rows, qkv_weights(d, nullptr, nullptr, nullptr), d->d);
+  s.Y = cv.take<float>((size_t)s.splits * rows * N);
   s.q = cv.take<char>((size_t)batch * d->n_h * d->block_size * d->d_h * esize(d));
   const size_t part_rows = (size_t)batch * d->n_h * n_chunks * d->block_size;
   s.part_acc = cv.take<float>(part_rows * d->d_h);
@@ -170,13 +200,11 @@ DFLASH_API dflash_status dflash_ctx_project(const dflash_dims* d, const void* co
   Carver cv(workspace, ws_bytes);
   CtxScratch s = carve_ctx(cv, d, M);
   if (!cv.ok) return DFLASH_ERR_WORKSPACE;
-  const int splits = gemm_splits(d->dtype, M, d->d, d->k_layers * d->d);
-  Weights W;
-  W.count = 1;
-  W.p[0] = W_fc;
-  W.n[0] = d->d;
-  cudaError_t e = gemm(d->dtype, A, M, W, splits, s.Y, d->d, stream);
-  if (e == cudaSuccess) e = rmsnorm_rows(d->dtype, s.Y, splits, M, d->d, gamma_h, d->eps, C_out, stream);
+  unsigned* status = status_word();
+  if (!status) return DFLASH_ERR_CUDA;
+  cudaError_t e = gemm(d->dtype, A, M, ctx_weights(d, W_fc), s.Y, d->d, status, stream);
+  if (e == cudaSuccess)
+    e = rmsnorm_rows(d->dtype, s.Y, s.splits, M, d->d, gamma_h, d->eps, C_out, stream);
   return cuda_status(e);
 }
 
@@ -201,7 +229,7 @@ DFLASH_API dflash_status dflash_kv_inject(const dflash_dims* d, const dflash_kv_
   unsigned* status = status_word();
   if (!status) return DFLASH_ERR_CUDA;
   const int N = 2 * d->n_kv * d->d_h;
-  const int splits = gemm_splits(d->dtype, M, N, d->d);
+  const int splits = s.splits;
   Segments A;
   A.n = 1;
   A.kseg = d->d;
@@ -209,12 +237,7 @@ DFLASH_API dflash_status dflash_kv_inject(const dflash_dims* d, const dflash_kv_
   const size_t layer_elems = (size_t)c->batch * d->n_kv * c->capacity * d->d_h;
   const size_t es = esize(d);
   const int32_t* lens = c->lens + (size_t)layer * c->batch;
-  Weights W;
-  W.count = 2;
-  W.p[0] = W_K;
-  W.p[1] = W_V;
-  W.n[0] = W.n[1] = d->n_kv * d->d_h;
-  cudaError_t e = gemm(d->dtype, A, M, W, splits, s.Y, N, stream);
+  cudaError_t e = gemm(d->dtype, A, M, kv_weights(d, W_K, W_V), s.Y, N, status, stream);
   HeadEpilogue ep;
   ep.Y = s.Y;
   ep.splits = splits;
@@ -269,7 +292,7 @@ DFLASH_API dflash_status dflash_block_attn(const dflash_dims* d, const dflash_kv
   const int rows = c->batch * d->block_size;
   const int nq = d->n_h * d->d_h, nkv = d->n_kv * d->d_h;
   const int N = nq + 2 * nkv;
-  const int splits = gemm_splits(d->dtype, rows, N, d->d);
+  const int splits = s.splits;
   Segments A;
   A.n = 1;
   A.kseg = d->d;
@@ -279,14 +302,7 @@ DFLASH_API dflash_status dflash_block_attn(const dflash_dims* d, const dflash_kv
   void* ck = (char*)c->k + (size_t)layer * layer_elems * es;
   void* cvv = (char*)c->v + (size_t)layer * layer_elems * es;
   int32_t* lens = c->lens + (size_t)layer * c->batch;
-  Weights W;
-  W.count = 3;
-  W.p[0] = W_Q;
-  W.p[1] = W_K;
-  W.p[2] = W_V;
-  W.n[0] = nq;
-  W.n[1] = W.n[2] = nkv;
-  cudaError_t e = gemm(d->dtype, A, rows, W, splits, s.Y, N, stream);
+  cudaError_t e = gemm(d->dtype, A, rows, qkv_weights(d, W_Q, W_K, W_V), s.Y, N, status, stream);
   HeadEpilogue ep;
   ep.Y = s.Y;
   ep.splits = splits;

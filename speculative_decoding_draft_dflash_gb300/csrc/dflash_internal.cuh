@@ -86,11 +86,16 @@ struct Weights {
 };
 
 // Number of K-splits the GEMM of this shape uses (partials summed by the epilogue).
-int gemm_splits(int dtype, int M, int N, int K);
+int gemm_splits(int dtype, int M, const Weights& W, int K);
 
-// Y[split][M][ldY] (fp32) = X W^T. f32: SIMT FFMA; bf16: tensor cores.
-cudaError_t gemm(int dtype, const Segments& A, int M, const Weights& W, int splits, float* Y,
-                 int ldY, cudaStream_t s);
+// Y[split][M][ldY] (fp32) = X W^T. f32: SIMT FFMA; bf16: tcgen05 tensor cores.
+cudaError_t gemm(int dtype, const Segments& A, int M, const Weights& W, float* Y, int ldY,
+                 unsigned* status, cudaStream_t s);
+
+// tcgen05 / TMA GEMM (bf16 inputs, fp32 accumulation); gemm_tc.cu
+int gemm_tc_splits(int M, const Weights& W, int K);
+cudaError_t gemm_tc(const Segments& A, int M, const Weights& W, float* Y, int ldY,
+                    unsigned* status, cudaStream_t s);
 
 // SIMT fp32-accumulating GEMM for any M, N, K (the f32 path).
 cudaError_t gemm_simt(int dtype, const Segments& A, int M, const Weights& W, float* Y, int ldY,

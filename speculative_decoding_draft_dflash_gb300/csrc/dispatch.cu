@@ -3,15 +3,14 @@
 
 namespace dflash {
 
-int gemm_splits(int dtype, int M, int N, int K) {
-  (void)dtype; (void)M; (void)N; (void)K;
-  return 1;
+int gemm_splits(int dtype, int M, const Weights& W, int K) {
+  return dtype == DFLASH_F32 ? 1 : gemm_tc_splits(M, W, K);
 }
 
-cudaError_t gemm(int dtype, const Segments& A, int M, const Weights& W, int splits, float* Y,
-                 int ldY, cudaStream_t s) {
-  (void)splits;
-  return gemm_simt(dtype, A, M, W, Y, ldY, s);
+cudaError_t gemm(int dtype, const Segments& A, int M, const Weights& W, float* Y, int ldY,
+                 unsigned* status, cudaStream_t s) {
+  if (dtype == DFLASH_F32) return gemm_simt(dtype, A, M, W, Y, ldY, s);
+  return gemm_tc(A, M, W, Y, ldY, status, s);
 }
 
 int attn_chunk(int dtype) {

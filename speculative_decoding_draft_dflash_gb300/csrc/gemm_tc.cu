@@ -1,0 +1,275 @@
+// Tensor-core projection GEMM for sm_103a: Y = X W^T with bf16 inputs and an
+// fp32 accumulator in tensor memory.
+//
+// One CTA computes a 128 x BN tile of Y over its share of K (split-K across
+// gridDim.z; the epilogue kernels sum the splits):
+//   warp 0      TMA producer: 128 x 64 activation tile + BN x 64 weight tile
+//               per stage, 128-byte swizzle, completion on a "full" mbarrier;
+//   warp 1      allocates BN TMEM columns and issues tcgen05.mma (M=128,
+//               N=BN, K=16, four per stage) from one thread; tcgen05.commit
+//               frees each stage ("empty" mbarrier) and finally signals "done";
+//   warps 2-5   epilogue: tcgen05.ld of their 32 TMEM lanes, fp32 stores.
+// The activations arrive as up to eight K-segments (the k target layers'
+// hidden states of the context projection), each with its own tensor map;
+// the weights as up to three matrices stacked along N (W_Q | W_K | W_V).
+#include <mutex>
+
+#include "sm100_ptx.cuh"
+
+namespace dflash {
+namespace {
+
+constexpr int BM = 128, BK = 64, kThreads = 192;
+
+struct TcGemmParams {
+  CUtensorMap a[8];   // activation segments [M][kseg], box {64, 128}
+  CUtensorMap b[3];   // weights [N_i][K], box {64, BN}
+  int kseg_blocks;    // 64-wide K blocks per activation segment
+  int w_count;
+  int w_off[4];       // prefix offsets of the stacked weights along N
+  int M, ldY;
+  int kb_total, kb_per_split;
+  float* Y;
+  unsigned* status;
+};
+
+template <int BN>
+struct Cfg {
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + 256;
+};
+
+// Waits without honouring the abort flag (used to drain in-flight work before exit).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned* status) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+      atomicOr(status, DFLASH_DEV_TIMEOUT);
+      return;
+    }
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcGemmParams p) {
+  using C = Cfg<BN>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + (size_t)STAGES * C::STAGE);
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+  const int kb0 = blockIdx.z * p.kb_per_split;
+  const int nkb = min(p.kb_total, kb0 + p.kb_per_split) - kb0;
+  const uint32_t full0 = ptx::smem_u32(bars);
+  const uint32_t empty0 = ptx::smem_u32(bars + STAGES);
+  const uint32_t done = ptx::smem_u32(bars + 2 * STAGES);
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(full0 + 8 * s, 1);
+      ptx::mbar_init(empty0 + 8 * s, 1);
+    }
+    ptx::mbar_init(done, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < 8; ++i) ptx::prefetch_tmap(&p.a[i]);
+    for (int i = 0; i < p.w_count; ++i) ptx::prefetch_tmap(&p.b[i]);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), BN);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  int wi = 0;
+  while (wi + 1 < p.w_count && n0 >= p.w_off[wi + 1]) ++wi;
+  const int nb = n0 - p.w_off[wi];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (i / STAGES) & 1;
+        if (i >= STAGES && !ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, &abort_flag, p.status)) break;
+        const int kb = kb0 + i;
+        const int seg = kb / p.kseg_blocks;
+        const int kx = (kb - seg * p.kseg_blocks) * BK;
+        const uint32_t sa = ptx::smem_u32(smem + (size_t)s * C::STAGE);
+        ptx::mbar_arrive_expect_tx(full0 + 8 * s, C::STAGE);
+        ptx::tma_load_2d(sa, &p.a[seg], full0 + 8 * s, kx, m0);
+        ptx::tma_load_2d(sa + C::A_BYTES, &p.b[wi], full0 + 8 * s, kb * BK, nb);
+        ++issued;
+      }
+      // no copy of ours may still be landing when the CTA exits
+      for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
+        drain_wait(full0 + 8 * (i % STAGES), (i / STAGES) & 1, p.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (i / STAGES) & 1;
+        if (!ptx::mbar_wait(full0 + 8 * s, ph, &abort_flag, p.status)) break;
+        ptx::tc_fence_after();
+        const uint32_t sa = ptx::smem_u32(smem + (size_t)s * C::STAGE);
+        const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          ptx::mma_bf16(tmem, ptx::smem_desc_sw128(sa + 32 * k), ptx::smem_desc_sw128(sb + 32 * k),
+                        idesc, (i > 0 || k > 0) ? 1u : 0u);
+        ptx::mma_commit(empty0 + 8 * s);
+      }
+      ptx::mma_commit(done);
+      drain_wait(done, 0, p.status);  // every MMA has finished before TMEM can be freed
+    }
+  } else {
+    const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 are this warp's
+    const int row = q * 32 + lane;
+    // warp-uniform: tcgen05.ld below is a .sync.aligned instruction
+    const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(done, 0, &abort_flag, p.status));
+    ptx::tc_fence_after();
+    if (ok) {
+      float* y = p.Y + (size_t)blockIdx.z * p.M * p.ldY + (size_t)(m0 + row) * p.ldY + n0;
+      const bool in = (m0 + row) < p.M;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
+        ptx::tmem_ld_wait();
+        if (in) {
+          float4* dst = reinterpret_cast<float4*>(y + c * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, BN);
+  }
+}
+
+// ---- host side ---------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)f;
+  });
+  return fn;
+}
+
+// bf16 row-major [rows][cols] matrix, box {64 columns, box_rows rows}, 128-byte swizzle.
+bool encode_2d(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Plan {
+  int bn, kb_total, kb_per_split, splits;
+};
+
+Plan plan(int M, const Weights& W, int K) {
+  Plan pl;
+  pl.bn = 256;
+  for (int i = 0; i < W.count; ++i)
+    while (W.n[i] % pl.bn) pl.bn >>= 1;
+  pl.kb_total = K / BK;
+  const int tiles = ((M + BM - 1) / BM) * (W.total() / pl.bn);
+  int splits = 148 / (tiles > 0 ? tiles : 1);
+  const int max_splits = pl.kb_total / 4 > 0 ? pl.kb_total / 4 : 1;
+  if (splits > max_splits) splits = max_splits;
+  if (splits < 1) splits = 1;
+  pl.kb_per_split = (pl.kb_total + splits - 1) / splits;
+  pl.splits = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
+  return pl;
+}
+
+template <int BN>
+cudaError_t launch(const TcGemmParams& p, dim3 grid, cudaStream_t s) {
+  const size_t smem = Cfg<BN>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  LaunchScope ls_(DFLASH_KERNEL_GEMM, s);
+  gemm_tc_kernel<BN><<<grid, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_tc_splits(int M, const Weights& W, int K) { return plan(M, W, K).splits; }
+
+cudaError_t gemm_tc(const Segments& A, int M, const Weights& W, float* Y, int ldY,
+                    unsigned* status, cudaStream_t s) {
+  const int N = W.total();
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  const int K = A.n * A.kseg;
+  const Plan pl = plan(M, W, K);
+  if (pl.bn < 64 || A.kseg % BK) return cudaErrorInvalidValue;
+  TcGemmParams p;
+  memset(&p, 0, sizeof(p));
+  for (int i = 0; i < A.n; ++i)
+    if (!encode_2d(&p.a[i], A.p[i], M, A.kseg, BM)) return cudaErrorInvalidValue;
+  for (int i = A.n; i < 8; ++i) p.a[i] = p.a[0];
+  int off = 0;
+  for (int i = 0; i < W.count; ++i) {
+    if (!encode_2d(&p.b[i], W.p[i], W.n[i], K, pl.bn)) return cudaErrorInvalidValue;
+    p.w_off[i] = off;
+    off += W.n[i];
+  }
+  p.w_off[W.count] = off;
+  p.w_count = W.count;
+  p.kseg_blocks = A.kseg / BK;
+  p.M = M;
+  p.ldY = ldY;
+  p.kb_total = pl.kb_total;
+  p.kb_per_split = pl.kb_per_split;
+  p.Y = Y;
+  p.status = status;
+  dim3 grid((M + BM - 1) / BM, N / pl.bn, pl.splits);
+  switch (pl.bn) {
+    case 256: return launch<256>(p, grid, s);
+    case 128: return launch<128>(p, grid, s);
+    default: return launch<64>(p, grid, s);
+  }
+}
+
+}  // namespace dflash
