@@ -335,6 +335,7 @@ DFLASH_API dflash_status dflash_block_attn(const dflash_dims* d, const dflash_kv
   p.part_acc = s.part_acc;
   p.part_ml = s.part_ml;
   p.counters = s.counters;
+  p.status = status;
   p.batch = c->batch;
   p.n_h = d->n_h;
   p.n_kv = d->n_kv;

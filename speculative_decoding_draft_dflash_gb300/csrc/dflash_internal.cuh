@@ -151,12 +151,17 @@ struct AttnParams {
   void* out;              // [batch][bs][n_h * d_h]
   float* part_acc;        // partial accumulators, per chunk
   float2* part_ml;        // partial (max, sum), per chunk
-  int* counters;          // [batch][n_kv] chunk-completion counters (zero between calls)
+  int* counters;          // [batch][n_kv] chunk-completion counters
+  unsigned* status;       // device status word
   int batch, n_h, n_kv, d_h, bs, capacity, window, chunk, n_chunks, table_len;
   float scaling;
 };
 int attn_simt_chunk();
 cudaError_t attn_simt(int dtype, const AttnParams& p, cudaStream_t s);
+
+// tcgen05 attention (bf16, d_h = 128); attn_tc.cu
+int attn_tc_chunk();
+cudaError_t attn_tc(const AttnParams& p, cudaStream_t s);
 
 // Keys per attention chunk and the attention launch for a dtype.
 int attn_chunk(int dtype);

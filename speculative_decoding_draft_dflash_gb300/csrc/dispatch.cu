@@ -13,13 +13,10 @@ cudaError_t gemm(int dtype, const Segments& A, int M, const Weights& W, float* Y
   return gemm_tc(A, M, W, Y, ldY, status, s);
 }
 
-int attn_chunk(int dtype) {
-  (void)dtype;
-  return attn_simt_chunk();
-}
+int attn_chunk(int dtype) { return dtype == DFLASH_F32 ? attn_simt_chunk() : attn_tc_chunk(); }
 
 cudaError_t attention(int dtype, const AttnParams& p, cudaStream_t s) {
-  return attn_simt(dtype, p, s);
+  return dtype == DFLASH_F32 ? attn_simt(dtype, p, s) : attn_tc(p, s);
 }
 
 }  // namespace dflash

@@ -189,19 +189,6 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 row-major [rows][cols] matrix, box {64 columns, box_rows rows}, 128-byte swizzle.
-bool encode_2d(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 struct Plan {
   int bn, kb_total, kb_per_split, splits;
 };
@@ -221,6 +208,24 @@ Plan plan(int M, const Weights& W, int K) {
   pl.splits = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
   return pl;
 }
+
+}  // namespace
+
+// bf16 row-major [rows][cols] matrix, box {64 columns, box_rows rows}, 128-byte swizzle,
+// zero fill outside the matrix.
+bool encode_2d_bf16(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
 
 template <int BN>
 cudaError_t launch(const TcGemmParams& p, dim3 grid, cudaStream_t s) {
@@ -247,11 +252,11 @@ cudaError_t gemm_tc(const Segments& A, int M, const Weights& W, float* Y, int ld
   TcGemmParams p;
   memset(&p, 0, sizeof(p));
   for (int i = 0; i < A.n; ++i)
-    if (!encode_2d(&p.a[i], A.p[i], M, A.kseg, BM)) return cudaErrorInvalidValue;
+    if (!encode_2d_bf16(&p.a[i], A.p[i], M, A.kseg, BM)) return cudaErrorInvalidValue;
   for (int i = A.n; i < 8; ++i) p.a[i] = p.a[0];
   int off = 0;
   for (int i = 0; i < W.count; ++i) {
-    if (!encode_2d(&p.b[i], W.p[i], W.n[i], K, pl.bn)) return cudaErrorInvalidValue;
+    if (!encode_2d_bf16(&p.b[i], W.p[i], W.n[i], K, pl.bn)) return cudaErrorInvalidValue;
     p.w_off[i] = off;
     off += W.n[i];
   }
