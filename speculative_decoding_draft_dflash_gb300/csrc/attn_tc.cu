@@ -96,16 +96,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+template <bool DUP>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams p) {
+  constexpr int NCOL = DUP ? 64 : 128;  // S columns per softmax thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + OFF_BAR);
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ int last_flag;
+  __shared__ float xch[2][2][64];  // DUP: tile maxima exchanged between the two column halves
+  __shared__ float xl[2][64];      // DUP: row sums exchanged at the end of an item
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nsw = (p.R + 31) >> 5;  // softmax warps holding query rows
+  const int nsw = DUP ? 4 : (p.R + 31) >> 5;  // softmax warps holding query rows
   const uint32_t sbase = ptx::smem_u32(smem);
   // barriers
   const uint32_t q_full = ptx::smem_u32(bars + 0), q_empty = ptx::smem_u32(bars + 1);
@@ -160,8 +164,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (n > 0 && !ptx::mbar_wait(q_empty, (n - 1) & 1, &abort_flag, p.status)) break;
         const int qrow = (it.b * p.n_h + it.kvh * p.G) * p.bs;
         ptx::mbar_arrive_expect_tx(q_full, TILE);
-        ptx::tma_load_2d(sbase + OFF_Q, &p.q, q_full, 0, qrow);
-        ptx::tma_load_2d(sbase + OFF_Q + HALF, &p.q, q_full, 64, qrow);
+        if (DUP) {  // 64 query rows, loaded twice: lanes 0-63 and 64-127
+          ptx::tma_load_2d(sbase + OFF_Q, &p.q, q_full, 0, qrow);
+          ptx::tma_load_2d(sbase + OFF_Q + 64 * 128, &p.q, q_full, 0, qrow);
+          ptx::tma_load_2d(sbase + OFF_Q + HALF, &p.q, q_full, 64, qrow);
+          ptx::tma_load_2d(sbase + OFF_Q + HALF + 64 * 128, &p.q, q_full, 64, qrow);
+        } else {
+          ptx::tma_load_2d(sbase + OFF_Q, &p.q, q_full, 0, qrow);
+          ptx::tma_load_2d(sbase + OFF_Q + HALF, &p.q, q_full, 64, qrow);
+        }
         ++n;
         const int kvrow = (it.b * p.n_kv + it.kvh) * p.capacity + it.c0;
         for (int j = 0; j < it.ntiles; ++j) {
@@ -254,21 +265,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
   } else if (warp < nsw) {
     // ------------------------------------------------------------ softmax rows
-    const int r = warp * 32 + lane;
-    const bool rvalid = r < p.R;
-    const int gq = rvalid ? r / p.bs : 0, t = rvalid ? r - gq * p.bs : 0;
+    // DUP: the query rows fill TMEM lanes 0-63 and again 64-127; warps 0-1 take
+    // columns 0-63 of each row and warps 2-3 columns 64-127, and exchange the tile
+    // maximum and the final row sum through shared memory.
+    const int rt = warp * 32 + lane;                 // TMEM lane = S / O row
+    const int qr = DUP ? (rt & 63) : rt;             // query row (g * bs + t)
+    const int half = DUP ? (warp >> 1) : 0;
+    const int coff = half * NCOL;                    // first column this thread owns
+    const bool rvalid = qr < p.R;
+    const int gq = rvalid ? qr / p.bs : 0, t = rvalid ? qr - gq * p.bs : 0;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    uint8_t* prow = smem + OFF_P + r * 128;
+    const uint32_t nsync = 32 * nsw;
+    uint8_t* pbase = smem + OFF_P;
     int gt = 0;
-    float s[TK];
+    float s[NCOL];
     for (int i = blockIdx.x; i < p.total_items; i += gridDim.x) {
       const Item it = decode(p, i);
       if (!it.ok) {
         // a refused sequence (capacity / table): its output rows are zero
         if (it.c == 0 && rvalid) {
           uint4* o = reinterpret_cast<uint4*>(p.out + ((size_t)(it.b * p.bs + t) * p.n_h +
-                                                       it.kvh * p.G + gq) * 128);
-          for (int k = 0; k < 16; ++k) o[k] = make_uint4(0, 0, 0, 0);
+                                                       it.kvh * p.G + gq) * 128 + coff);
+          for (int k = 0; k < NCOL / 8; ++k) o[k] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -283,24 +301,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (!alive) break;
         ptx::tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < NCOL / 32; ++cc) {
           uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(tmem + lane_base + TM_S + sb * TK + cc * 32, v);
+          ptx::tmem_ld_32x32b_x32(tmem + lane_base + TM_S + sb * TK + coff + cc * 32, v);
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(v[e]);
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(s_free0 + 8 * sb);
-        const int k0 = it.c0 + j * TK;
-        float mx = -INFINITY;
+        // raw tile maximum over this thread's columns (masked keys -> -inf)
+        const int key0 = it.c0 + j * TK + coff;
+        const bool full = rvalid && key0 + NCOL <= it.c1 && (p.window <= 0 || qpos - key0 < p.window);
+        float mx;
+        if (full) {
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int e = 0; e < TK; ++e) {
-          const int key = k0 + e;
-          const bool vis = rvalid && key < it.c1 && (p.window <= 0 || qpos - key < p.window);
-          s[e] = vis ? s[e] * p.sl2 : -INFINITY;
-          mx = fmaxf(mx, s[e]);
+          for (int e = 0; e < NCOL; ++e) m4[e & 3] = fmaxf(m4[e & 3], s[e]);
+          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        } else {
+          mx = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < NCOL; ++e) {
+            const int key = key0 + e;
+            const bool vis = rvalid && key < it.c1 && (p.window <= 0 || qpos - key < p.window);
+            s[e] = vis ? s[e] : -INFINITY;
+            mx = fmaxf(mx, s[e]);
+          }
         }
+        if (DUP) {
+          xch[j & 1][half][qr] = mx;
+          ptx::named_sync(2, nsync);
+          mx = fmaxf(mx, xch[j & 1][half ^ 1][qr]);
+        }
+        mx *= p.sl2;  // log2 domain
         float alpha = 1.f;
         bool resc = false;
         if (m_ref == -INFINITY) {
@@ -311,13 +345,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           resc = true;
         }
         const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float sum = 0.f;
+        const float2 sl2v = make_float2(p.sl2, p.sl2), nmu = make_float2(-mu, -mu);
+        float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int e = 0; e < TK; ++e) {
-          s[e] = ptx::ex2(s[e] - mu);
-          sum += s[e];
+        for (int e = 0; e < NCOL; e += 2) {
+          const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), sl2v, nmu);
+          s[e] = ptx::ex2(x.x);
+          s[e + 1] = ptx::ex2(x.y);
+          acc2[(e >> 1) & 3] = __fadd2_rn(acc2[(e >> 1) & 3], make_float2(s[e], s[e + 1]));
         }
-        l = l * alpha + sum;
+        const float2 a01 = __fadd2_rn(acc2[0], acc2[1]), a23 = __fadd2_rn(acc2[2], acc2[3]);
+        l = l * alpha + ((a01.x + a01.y) + (a23.x + a23.y));
         if (j > 0) {
           // PV of the previous tile done: P may be overwritten, O holds tiles < j
           alive = __all_sync(0xffffffffu, ptx::mbar_wait(pv_done, (g - 1) & 1, &abort_flag, p.status));
@@ -325,37 +364,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           ptx::tc_fence_after();
           if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < NCOL / 32; ++cc) {
               uint32_t v[32];
-              ptx::tmem_ld_32x32b_x32(tmem + lane_base + TM_O + cc * 32, v);
+              ptx::tmem_ld_32x32b_x32(tmem + lane_base + TM_O + coff + cc * 32, v);
               ptx::tmem_ld_wait();
 #pragma unroll
               for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-              ptx::tmem_st_32x32b_x32(tmem + lane_base + TM_O + cc * 32, v);
+              ptx::tmem_st_32x32b_x32(tmem + lane_base + TM_O + coff + cc * 32, v);
             }
             ptx::tmem_st_wait();
           }
         }
-        // P row, bf16, in the 128-byte-swizzled K-major layout the MMA reads
+        // P, bf16, in the 128-byte-swizzled K-major layout the MMA reads: this thread's
+        // keys coff .. coff+NCOL-1 of query row qr (and of its copy qr + 64 under DUP)
 #pragma unroll
-        for (int cidx = 0; cidx < 16; ++cidx) {
-          const int kb = cidx >> 3, cc = cidx & 7;
+        for (int cidx = 0; cidx < NCOL / 8; ++cidx) {
+          const int key = coff + 8 * cidx, kb = key >> 6, cc = (key >> 3) & 7;
           uint4 w;
           w.x = pack_bf16(s[8 * cidx + 0], s[8 * cidx + 1]);
           w.y = pack_bf16(s[8 * cidx + 2], s[8 * cidx + 3]);
           w.z = pack_bf16(s[8 * cidx + 4], s[8 * cidx + 5]);
           w.w = pack_bf16(s[8 * cidx + 6], s[8 * cidx + 7]);
-          *reinterpret_cast<uint4*>(prow + kb * HALF + ((cc ^ (r & 7)) << 4)) = w;
+          *reinterpret_cast<uint4*>(pbase + kb * HALF + qr * 128 + ((cc ^ (qr & 7)) << 4)) = w;
+          if (DUP)
+            *reinterpret_cast<uint4*>(pbase + kb * HALF + (qr + 64) * 128 + ((cc ^ (qr & 7)) << 4)) = w;
         }
         // keys past the chunk end in the last tile: zero their V rows (slots past the
         // cache length may hold anything, and 0 * NaN would poison O)
-        const int nvalid = it.c1 - k0;
+        const int nvalid = it.c1 - (it.c0 + j * TK);
         if (j == T - 1 && nvalid < TK) {
           alive = __all_sync(0xffffffffu, ptx::mbar_wait(v_full0 + 8 * sb, u & 1, &abort_flag, p.status));
           if (!alive) break;
           uint4* vz = reinterpret_cast<uint4*>(smem + OFF_V + sb * TILE);
           const int per_half = (TK - nvalid) * 8;  // 16-byte chunks per half
-          for (int idx = r; idx < 2 * per_half; idx += 32 * nsw) {
+          for (int idx = rt; idx < 2 * per_half; idx += nsync) {
             const int h = idx / per_half, rem = idx - h * per_half;
             vz[(h * HALF) / 16 + nvalid * 8 + rem] = make_uint4(0, 0, 0, 0);
           }
@@ -366,25 +408,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       }
       if (!alive) break;
       gt += T;
-      // ---- epilogue: O for this item
+      // ---- epilogue: this thread's columns of O for this item
+      if (DUP) {
+        // row sum of both halves; the barrier also ends every read of xch for this item
+        xl[half][qr] = l;
+        ptx::named_sync(2, nsync);
+        l += xl[half ^ 1][qr];
+      }
       alive = __all_sync(0xffffffffu, ptx::mbar_wait(pv_done, (gt - 1) & 1, &abort_flag, p.status));
       if (!alive) break;
       ptx::tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < NCOL / 32; ++cc) {
         uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(tmem + lane_base + TM_O + cc * 32, v);
+        ptx::tmem_ld_32x32b_x32(tmem + lane_base + TM_O + coff + cc * 32, v);
         ptx::tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(v[e]);
       }
       const int bk = it.b * p.n_kv + it.kvh;
-      bf16* orow = p.out + ((size_t)(it.b * p.bs + t) * p.n_h + it.kvh * p.G + gq) * 128;
+      bf16* orow = p.out + ((size_t)(it.b * p.bs + t) * p.n_h + it.kvh * p.G + gq) * 128 + coff;
       if (it.nchunks == 1) {
         if (rvalid) {
           const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
+          for (int k = 0; k < NCOL / 8; ++k) {
             uint4 w;
             w.x = pack_bf16(s[8 * k + 0] * inv, s[8 * k + 1] * inv);
             w.y = pack_bf16(s[8 * k + 2] * inv, s[8 * k + 3] * inv);
@@ -396,35 +444,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         continue;
       }
       // several chunks: publish this chunk's partial, the last one merges
-      const size_t prow_idx = ((size_t)bk * p.max_chunks + it.c) * p.R + r;
+      const size_t prow_idx = ((size_t)bk * p.max_chunks + it.c) * p.R + qr;
       if (rvalid) {
-        float4* a = reinterpret_cast<float4*>(p.part_acc + prow_idx * 128);
+        float4* a = reinterpret_cast<float4*>(p.part_acc + prow_idx * 128 + coff);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) a[k] = make_float4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
-        p.part_ml[prow_idx] = make_float2(m_ref, l);
+        for (int k = 0; k < NCOL / 4; ++k) a[k] = make_float4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
+        if (half == 0) p.part_ml[prow_idx] = make_float2(m_ref, l);
       }
       __threadfence();
-      ptx::named_sync(1, 32 * nsw);
+      ptx::named_sync(1, nsync);
       if (threadIdx.x == 0) last_flag = (atomicAdd(p.counters + bk, 1) == it.nchunks - 1);
-      ptx::named_sync(1, 32 * nsw);
+      ptx::named_sync(1, nsync);
       if (!last_flag) continue;
       __threadfence();
       if (rvalid) {
-        const size_t base = (size_t)bk * p.max_chunks * p.R + r;
+        const size_t base = (size_t)bk * p.max_chunks * p.R + qr;
         float M = -INFINITY;
         for (int c = 0; c < it.nchunks; ++c) M = fmaxf(M, __ldcg(p.part_ml + base + (size_t)c * p.R).x);
         float L = 0.f;
-        float acc[128];
+        float acc[NCOL];
 #pragma unroll
-        for (int e = 0; e < 128; ++e) acc[e] = 0.f;
+        for (int e = 0; e < NCOL; ++e) acc[e] = 0.f;
         for (int c = 0; c < it.nchunks; ++c) {
           const float2 ml = __ldcg(p.part_ml + base + (size_t)c * p.R);
           if (ml.y == 0.f) continue;
           const float w = ptx::ex2(ml.x - M);
           L += w * ml.y;
-          const float4* a = reinterpret_cast<const float4*>(p.part_acc + (base + (size_t)c * p.R) * 128);
+          const float4* a = reinterpret_cast<const float4*>(p.part_acc + (base + (size_t)c * p.R) * 128 + coff);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
+          for (int k = 0; k < NCOL / 4; ++k) {
             const float4 x = __ldcg(a + k);
             acc[4 * k] += w * x.x;
             acc[4 * k + 1] += w * x.y;
@@ -434,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         }
         const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < NCOL / 8; ++k) {
           uint4 w;
           w.x = pack_bf16(acc[8 * k + 0] * inv, acc[8 * k + 1] * inv);
           w.y = pack_bf16(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
@@ -482,7 +530,9 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   if (a.d_h != 128) return cudaErrorInvalidValue;
   AttnTcParams p;
   memset(&p, 0, sizeof(p));
-  if (!encode_2d_bf16(&p.q, a.q, (long long)a.batch * a.n_h * a.bs, 128, 128) ||
+  const int R = (a.n_h / a.n_kv) * a.bs;
+  const bool dup = R <= 64;
+  if (!encode_2d_bf16(&p.q, a.q, (long long)a.batch * a.n_h * a.bs, 128, dup ? 64 : 128) ||
       !encode_2d_bf16(&p.k, a.cache_k, (long long)a.batch * a.n_kv * a.capacity, 128, 128) ||
       !encode_2d_bf16(&p.v, a.cache_v, (long long)a.batch * a.n_kv * a.capacity, 128, 128))
     return cudaErrorInvalidValue;
@@ -506,12 +556,19 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   p.sl2 = a.scaling * 1.4426950408889634f;
   cudaError_t e = cudaMemsetAsync(a.counters, 0, sizeof(int) * a.batch * a.n_kv, s);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
-  if (e != cudaSuccess) return e;
   int grid = sm_count();
   if (grid > p.total_items) grid = p.total_items;
-  LaunchScope ls_(DFLASH_KERNEL_ATTENTION, s);
-  attn_tc_kernel<<<grid, kThreads, SMEM, s>>>(p);
+  if (dup) {
+    e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+    if (e != cudaSuccess) return e;
+    LaunchScope ls_(DFLASH_KERNEL_ATTENTION, s);
+    attn_tc_kernel<true><<<grid, kThreads, SMEM, s>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+    if (e != cudaSuccess) return e;
+    LaunchScope ls_(DFLASH_KERNEL_ATTENTION, s);
+    attn_tc_kernel<false><<<grid, kThreads, SMEM, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

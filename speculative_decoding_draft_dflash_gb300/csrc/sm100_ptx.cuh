@@ -198,7 +198,7 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
 // 2^x on the special-function unit (flushes denormals; ex2.approx of -inf is +0).
 __device__ __forceinline__ float ex2(float x) {
   float y;
-  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
