@@ -237,6 +237,7 @@ const char* dflash_status_string(dflash_status s);
 #define DFLASH_KERNEL_LENS          6  /* cache length update */
 #define DFLASH_KERNEL_CROP          7  /* crop */
 #define DFLASH_KERNEL_ROPE_TABLE    8  /* RoPE table fill */
+#define DFLASH_KERNEL_SCHEDULE      9  /* attention work list */
 
 /*
  * Starts recording a CUDA event pair around every launch whose kind bit

@@ -1,24 +1,31 @@
 // Block attention on tcgen05 tensor cores (bf16 path).
 //
-// The G * bs queries of the block that share one KV head (G query heads x bs
-// block positions, at most 128 rows) are stacked into one M=128 MMA tile, so
-// every cached K/V row read from HBM serves all of them (DFlash KV Injection
-// Walkthrough, Step 4.4: non-causal, every block query sees every key; DFlash
-// source guide (II), part 1: query head h reads KV head h / G).
+// The R = G * bs block queries that share one KV head (G query heads x bs
+// block positions, at most 128) form the rows of one M=128 MMA tile, so every
+// cached K/V row read from HBM serves all of them (DFlash KV Injection
+// Walkthrough, Step 4.4: non-causal, every block query sees every key;
+// DFlash source guide (II), part 1: query head h reads KV head h / G).
 //
-// Persistent kernel, one CTA per SM. Work items are (chunk, sequence, KV
-// head) with chunks of 512 keys; CTAs take items round-robin. Per item:
-//   warp 4      TMA producer: the Q tile once, then 128-key K and V tiles
-//               into 2-stage rings (128-byte swizzle, L2 evict-first);
-//   warp 5      MMA issuer: S_j = Q K_j^T into one of two TMEM S buffers,
-//               O += P_j V_j into the TMEM O accumulator (V read MN-major);
-//   warps 0-3   softmax, one thread per query row: masks the tile (chunk
-//               end, sliding window), keeps a running max in the log2 domain,
-//               rescales O in TMEM only when the max grows by more than 2^8,
-//               writes P (bf16) into shared memory in the MMA's swizzled
-//               layout, and at the end either writes out = O / l or, when
-//               the sequence spans several chunks, a partial (m, l, O) that
-//               the last CTA to finish that sequence and head merges.
+// Three kernels:
+//   attn_schedule_kernel   one CTA: from the cache lengths, cuts every
+//                          (sequence, KV head) key range into work items of
+//                          near-equal 128-key tiles, sized so the GPU gets a
+//                          few items per SM, and lists them longest first;
+//   attn_tc_kernel         persistent, one CTA per SM, items fetched with an
+//                          atomic counter (greedy longest-first);
+//   attn_combine_kernel    merges the partial results of split ranges.
+//
+// attn_tc_kernel roles (warp: job):
+//   0-3, 4-7   softmax. Warp w serves TMEM lanes 32(w%4)..+31 (query rows)
+//              and S columns 64(w/4)..+63: two threads per row, exchanging the
+//              tile maximum and the row sum through shared memory. P (bf16) is
+//              stored into TMEM and read from there by the PV MMA.
+//   8          TMA: the Q tile of each item (double-buffered) and K tiles;
+//   9          MMA: S_j = Q K_j^T (two TMEM S buffers), O += P_j V_j (P from
+//              TMEM, V read MN-major from shared memory);
+//   10         TMA: V tiles (released later than K, so on their own thread).
+// O is rescaled in TMEM only when a row's running maximum grows by more than
+// 2^8, so almost every tile skips it.
 #include <float.h>
 
 #include <mutex>
@@ -29,57 +36,46 @@ namespace dflash {
 namespace {
 
 constexpr int TK = 128;                    // keys per tile
-constexpr int CHUNK_TILES = 4;
-constexpr int CHUNK = TK * CHUNK_TILES;    // keys per work item
-constexpr int kThreads = 192;
-constexpr uint32_t TILE = 128 * 128 * 2;   // 32 KB: Q, P, one K or one V tile
+constexpr uint32_t TILE = 128 * 128 * 2;   // 32 KB: one K or V tile (128 keys x 128 dims)
 constexpr uint32_t HALF = TILE / 2;        // one 64-column swizzled box
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_P = TILE;
-constexpr uint32_t OFF_K = 2 * TILE;       // 2 stages
-constexpr uint32_t OFF_V = 4 * TILE;       // 2 stages
-constexpr uint32_t OFF_BAR = 6 * TILE;
-constexpr size_t SMEM = 1024 + OFF_BAR + 256 + 4096;  // slack past the barriers
-constexpr uint32_t TM_S = 0, TM_O = 256;   // TMEM columns: S[2] at 0 and 128, O at 256
-constexpr float kRescaleLog2 = 8.0f;       // rescale O only when the max grows by > 2^8
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
+constexpr int WARP_KQ = 8, WARP_MMA = 9, WARP_V = 10;
+constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 384;  // TMEM columns: S[2], O, P[2] (64 each)
+constexpr float kRescaleLog2 = 8.0f;
+constexpr int kItemMinTiles = 4;
+constexpr int kRing = 4;                   // item ring slots
+
+// Shared-memory plan. NARROW (R <= 64): query rows 64-127 of an A tile are
+// padding, so the two Q buffers interleave (each only needs its rows 0-63 to
+// be its own) and V gets a third stage. WIDE (R > 64): plain double buffer.
+template <bool NARROW>
+struct Plan {
+  static constexpr int K_STAGES = 2;
+  static constexpr int V_STAGES = NARROW ? 3 : 2;
+  static constexpr uint32_t Q_BYTES = NARROW ? 40960 : 2 * TILE;
+  static constexpr uint32_t OFF_K = Q_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + K_STAGES * TILE;
+  static constexpr uint32_t OFF_BAR = OFF_V + V_STAGES * TILE;
+  static constexpr size_t SMEM = 1024 + OFF_BAR + 512;
+  __device__ static uint32_t q_base(int buf) { return NARROW ? buf * 8192u : buf * TILE; }
+};
 
 struct AttnTcParams {
-  CUtensorMap q;   // [B*n_h*bs][128] bf16
+  CUtensorMap q;   // [B*n_h*bs][128] bf16, box rows 64 (NARROW) or 128
   CUtensorMap k;   // [B*n_kv*capacity][128] bf16 (this layer)
   CUtensorMap v;
   const int32_t* lens;
   bf16* out;
-  float* part_acc;
-  float2* part_ml;
-  int* counters;
+  float* part_acc;       // [pair][max_splits][R][128]
+  float2* part_ml;       // [pair][max_splits][R]
+  const int4* items;     // {pair, k_begin, k_end, split (-1 = whole range)}
+  const int* n_items;
+  int* next_item;
   unsigned* status;
-  int batch, n_h, n_kv, bs, G, R, capacity, window, table_len, max_chunks, total_items;
+  int batch, n_h, n_kv, bs, G, R, capacity, window, table_len, max_splits;
   float sl2;  // scaling * log2(e)
 };
-
-struct Item {
-  int b, kvh, c, start, c0, c1, ntiles, nchunks;
-  bool ok, valid;
-};
-
-__device__ __forceinline__ Item decode(const AttnTcParams& p, int i) {
-  Item it;
-  const int per = p.batch * p.n_kv;
-  it.c = i / per;
-  const int rem = i - it.c * per;
-  it.b = rem / p.n_kv;
-  it.kvh = rem - it.b * p.n_kv;
-  it.start = p.lens[it.b];
-  const int end = it.start + p.bs;
-  const int lo = p.window > 0 ? max(0, it.start - p.window + 1) : 0;
-  it.ok = it.start >= 0 && end <= p.capacity && end <= p.table_len;
-  it.c0 = lo + it.c * CHUNK;
-  it.c1 = min(end, it.c0 + CHUNK);
-  it.valid = it.ok && it.c0 < it.c1;
-  it.ntiles = it.valid ? (it.c1 - it.c0 + TK - 1) / TK : 0;
-  it.nchunks = it.ok ? (end - lo + CHUNK - 1) / CHUNK : 0;
-  return it;
-}
 
 __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity, unsigned* status) {
   const uint64_t t0 = ptx::globaltimer();
@@ -96,51 +92,171 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <bool DUP>
+// TS form: A from tensor memory, B from a shared-memory descriptor.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+struct Range {
+  int start, end, lo;
+  bool ok;
+};
+
+__device__ __forceinline__ Range seq_range(const int32_t* lens, int b, int bs, int window,
+                                           int capacity, int table_len) {
+  Range r;
+  r.start = lens[b];
+  r.end = r.start + bs;
+  r.lo = window > 0 ? max(0, r.start - window + 1) : 0;
+  r.ok = r.start >= 0 && r.end <= capacity && r.end <= table_len;
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// scheduler: one CTA
+// ---------------------------------------------------------------------------
+struct SchedParams {
+  const int32_t* lens;
+  int4* items;
+  int* n_items;
+  int* next_item;
+  int* splits;      // [pair]: items of the pair (0 = refused sequence)
+  int batch, n_kv, bs, window, capacity, table_len, max_splits, n_sm;
+};
+
+constexpr int kMaxClass = 64;  // item sizes in tiles are bucketed up to this
+
+__device__ int block_sum_1024(int v, int* tmp) {
+  v = __reduce_add_sync(0xffffffffu, v);
+  if ((threadIdx.x & 31) == 0) tmp[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int t = 0;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += tmp[i];
+  __syncthreads();
+  return t;
+}
+
+__global__ void __launch_bounds__(1024) attn_schedule_kernel(SchedParams p) {
+  __shared__ int tmp[32];
+  __shared__ int s_class_base[kMaxClass + 1];
+  __shared__ int s_class_cnt[kMaxClass + 1];
+  const int pairs = p.batch * p.n_kv;
+  // total tiles -> item size: about three items per SM, at least kItemMinTiles tiles,
+  // and never more than max_splits items per range
+  int mine = 0;
+  for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
+    const Range r = seq_range(p.lens, b, p.bs, p.window, p.capacity, p.table_len);
+    if (r.ok) mine += p.n_kv * ((r.end - r.lo + TK - 1) / TK);
+  }
+  const int total_tiles = block_sum_1024(mine, tmp);
+  int item_tiles = (total_tiles + 3 * p.n_sm - 1) / (3 * p.n_sm);
+  if (item_tiles < kItemMinTiles) item_tiles = kItemMinTiles;
+  if (threadIdx.x <= kMaxClass) s_class_cnt[threadIdx.x] = 0;
+  if (threadIdx.x == 0) *p.next_item = 0;
+  __syncthreads();
+  // A range of t tiles becomes n = ceil(t / item_tiles) items of floor / ceil(t / n) tiles;
+  // count the items of each size
+  for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x) {
+    const Range r = seq_range(p.lens, pr / p.n_kv, p.bs, p.window, p.capacity, p.table_len);
+    int n = 0;
+    if (r.ok) {
+      const int t = (r.end - r.lo + TK - 1) / TK;
+      n = (t + item_tiles - 1) / item_tiles;
+      if (n > p.max_splits) n = p.max_splits;
+      const int small = t / n, big_cnt = t - small * n;  // big_cnt items of small + 1 tiles
+      if (big_cnt) atomicAdd(&s_class_cnt[min(small + 1, kMaxClass)], big_cnt);
+      if (n - big_cnt) atomicAdd(&s_class_cnt[min(small, kMaxClass)], n - big_cnt);
+    }
+    p.splits[pr] = n;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int c = kMaxClass; c >= 0; --c) {  // largest items first
+      s_class_base[c] = acc;
+      acc += s_class_cnt[c];
+    }
+    *p.n_items = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x <= kMaxClass) s_class_cnt[threadIdx.x] = 0;
+  __syncthreads();
+  for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x) {
+    const int n = p.splits[pr];
+    if (n == 0) continue;
+    const Range r = seq_range(p.lens, pr / p.n_kv, p.bs, p.window, p.capacity, p.table_len);
+    const int t = (r.end - r.lo + TK - 1) / TK;
+    const int small = t / n, big_cnt = t - small * n;
+    int k = r.lo;
+    for (int s = 0; s < n; ++s) {
+      const int tiles = small + (s < big_cnt ? 1 : 0);
+      const int c = min(tiles, kMaxClass);
+      const int slot = s_class_base[c] + atomicAdd(&s_class_cnt[c], 1);
+      const int k1 = min(r.end, k + tiles * TK);
+      p.items[slot] = make_int4(pr, k, k1, n == 1 ? -1 : s);
+      k = k1;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// attention
+// ---------------------------------------------------------------------------
+template <bool NARROW>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams p) {
-  constexpr int NCOL = DUP ? 64 : 128;  // S columns per softmax thread
+  using PL = Plan<NARROW>;
+  constexpr int NCOL = 64;  // S columns per softmax thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* bars = (uint64_t*)(smem + OFF_BAR);
+  uint64_t* bars = (uint64_t*)(smem + PL::OFF_BAR);
+  int4* ring = (int4*)(smem + PL::OFF_BAR + 256);
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ int last_flag;
-  __shared__ float xch[2][2][64];  // DUP: tile maxima exchanged between the two column halves
-  __shared__ float xl[2][64];      // DUP: row sums exchanged at the end of an item
+  __shared__ float xch[2][2][128];  // tile maxima of the two column halves
+  __shared__ float xl[2][128];      // row sums of the two column halves
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nsw = DUP ? 4 : (p.R + 31) >> 5;  // softmax warps holding query rows
+  const int nq = (p.R + 31) >> 5;                 // TMEM lane quarters holding query rows
+  const int n_soft = 64 * nq;                     // softmax threads
+  const bool soft = warp < kSoftmaxWarps && (warp & 3) < nq;
   const uint32_t sbase = ptx::smem_u32(smem);
-  // barriers
-  const uint32_t q_full = ptx::smem_u32(bars + 0), q_empty = ptx::smem_u32(bars + 1);
-  const uint32_t k_full0 = ptx::smem_u32(bars + 2), k_empty0 = ptx::smem_u32(bars + 4);
-  const uint32_t v_full0 = ptx::smem_u32(bars + 6), v_empty0 = ptx::smem_u32(bars + 8);
-  const uint32_t s_full0 = ptx::smem_u32(bars + 10), s_free0 = ptx::smem_u32(bars + 12);
-  const uint32_t p_full = ptx::smem_u32(bars + 14), pv_done = ptx::smem_u32(bars + 15);
+  // barriers (8 bytes each)
+  const uint32_t q_full0 = ptx::smem_u32(bars + 0), q_empty0 = ptx::smem_u32(bars + 2);
+  const uint32_t k_full0 = ptx::smem_u32(bars + 4), k_empty0 = ptx::smem_u32(bars + 6);
+  const uint32_t v_full0 = ptx::smem_u32(bars + 8), v_empty0 = ptx::smem_u32(bars + 11);
+  const uint32_t s_full0 = ptx::smem_u32(bars + 14), s_free0 = ptx::smem_u32(bars + 16);
+  const uint32_t p_full = ptx::smem_u32(bars + 18), pv_done0 = ptx::smem_u32(bars + 19);
+  const uint32_t it_full0 = ptx::smem_u32(bars + 21), it_empty0 = ptx::smem_u32(bars + 25);
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    ptx::mbar_init(q_full, 1);
-    ptx::mbar_init(q_empty, 1);
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(k_full0 + 8 * s, 1);
-      ptx::mbar_init(k_empty0 + 8 * s, 1);
-      ptx::mbar_init(v_full0 + 8 * s, 1);
-      ptx::mbar_init(v_empty0 + 8 * s, 1);
-      ptx::mbar_init(s_full0 + 8 * s, 1);
-      ptx::mbar_init(s_free0 + 8 * s, 32 * nsw);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(q_full0 + 8 * i, 1);
+      ptx::mbar_init(q_empty0 + 8 * i, 1);
+      ptx::mbar_init(k_full0 + 8 * i, 1);
+      ptx::mbar_init(k_empty0 + 8 * i, 1);
+      ptx::mbar_init(s_full0 + 8 * i, 1);
+      ptx::mbar_init(s_free0 + 8 * i, n_soft);
+      ptx::mbar_init(pv_done0 + 8 * i, 1);
     }
-    ptx::mbar_init(p_full, 32 * nsw);
-    ptx::mbar_init(pv_done, 1);
+    for (int i = 0; i < PL::V_STAGES; ++i) {
+      ptx::mbar_init(v_full0 + 8 * i, 1);
+      ptx::mbar_init(v_empty0 + 8 * i, 1);
+    }
+    ptx::mbar_init(p_full, n_soft);
+    for (int i = 0; i < kRing; ++i) {
+      ptx::mbar_init(it_full0 + 8 * i, 1);
+      ptx::mbar_init(it_empty0 + 8 * i, 2 + n_soft);
+    }
     ptx::fence_mbar_init();
   }
-  // P rows no softmax thread writes must hold zeros (finite) for the PV MMA
-  {
-    uint4* pz = reinterpret_cast<uint4*>(smem + OFF_P);
-    for (int i = threadIdx.x; i < (int)(TILE / 16); i += blockDim.x) pz[i] = make_uint4(0, 0, 0, 0);
-    ptx::fence_proxy_async_smem();
-  }
-  if (warp == 5) {
+  if (warp == WARP_MMA) {
     ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), 512);
     ptx::tmem_relinquish();
   }
@@ -149,80 +265,114 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
+  if (warp == WARP_KQ) {
+    // ---------------------------------------------------- item fetch, Q and K loads
     if (lane == 0) {
       ptx::prefetch_tmap(&p.q);
       ptx::prefetch_tmap(&p.k);
       ptx::prefetch_tmap(&p.v);
       const uint64_t pol = ptx::policy_evict_first();
-      int gk = 0, gv = 0, n = 0;  // K tiles, V tiles, items issued
+      const int n_items = *p.n_items;
+      int gk = 0, n = 0, nq_loads = 0;
+      int idx = atomicAdd(p.next_item, 1);
       bool stop = false;
-      for (int i = blockIdx.x; i < p.total_items && !stop; i += gridDim.x) {
-        const Item it = decode(p, i);
-        if (!it.valid) continue;
-        if (n > 0 && !ptx::mbar_wait(q_empty, (n - 1) & 1, &abort_flag, p.status)) break;
-        const int qrow = (it.b * p.n_h + it.kvh * p.G) * p.bs;
-        ptx::mbar_arrive_expect_tx(q_full, TILE);
-        if (DUP) {  // 64 query rows, loaded twice: lanes 0-63 and 64-127
-          ptx::tma_load_2d(sbase + OFF_Q, &p.q, q_full, 0, qrow);
-          ptx::tma_load_2d(sbase + OFF_Q + 64 * 128, &p.q, q_full, 0, qrow);
-          ptx::tma_load_2d(sbase + OFF_Q + HALF, &p.q, q_full, 64, qrow);
-          ptx::tma_load_2d(sbase + OFF_Q + HALF + 64 * 128, &p.q, q_full, 64, qrow);
-        } else {
-          ptx::tma_load_2d(sbase + OFF_Q, &p.q, q_full, 0, qrow);
-          ptx::tma_load_2d(sbase + OFF_Q + HALF, &p.q, q_full, 64, qrow);
-        }
-        ++n;
-        const int kvrow = (it.b * p.n_kv + it.kvh) * p.capacity + it.c0;
-        for (int j = 0; j < it.ntiles; ++j) {
-          int s = gk & 1, u = gk >> 1;
+      for (;; ++n) {
+        const int slot = n % kRing;
+        if (n >= kRing &&
+            !ptx::mbar_wait(it_empty0 + 8 * slot, ((n / kRing) - 1) & 1, &abort_flag, p.status))
+          break;
+        const int4 it = idx < n_items ? p.items[idx] : make_int4(-1, 0, 0, 0);
+        ring[slot] = it;
+        ptx::mbar_arrive(it_full0 + 8 * slot);  // release: the ring entry is visible to waiters
+        if (it.x < 0) break;
+        idx = atomicAdd(p.next_item, 1);         // prefetch the next item's index
+        const int b = it.x / p.n_kv, kvh = it.x - b * p.n_kv;
+        const int qb = n & 1;
+        if (n >= 2 && !ptx::mbar_wait(q_empty0 + 8 * qb, ((n >> 1) - 1) & 1, &abort_flag, p.status))
+          break;
+        const int qrow = (b * p.n_h + kvh * p.G) * p.bs;
+        const uint32_t qd = sbase + PL::q_base(qb);
+        ptx::mbar_arrive_expect_tx(q_full0 + 8 * qb, NARROW ? TILE / 2 : TILE);
+        ptx::tma_load_2d(qd, &p.q, q_full0 + 8 * qb, 0, qrow);
+        ptx::tma_load_2d(qd + HALF, &p.q, q_full0 + 8 * qb, 64, qrow);
+        ++nq_loads;
+        const int kvrow = (b * p.n_kv + kvh) * p.capacity;
+        const int ntiles = (it.z - it.y + TK - 1) / TK;
+        for (int j = 0; j < ntiles; ++j) {
+          const int s = gk & 1, u = gk >> 1;
           if (gk >= 2 && !ptx::mbar_wait(k_empty0 + 8 * s, (u - 1) & 1, &abort_flag, p.status)) {
             stop = true;
             break;
           }
-          const uint32_t kd = sbase + OFF_K + s * TILE;
+          const uint32_t kd = sbase + PL::OFF_K + s * TILE;
           ptx::mbar_arrive_expect_tx(k_full0 + 8 * s, TILE);
-          ptx::tma_load_2d_hint(kd, &p.k, k_full0 + 8 * s, 0, kvrow + j * TK, pol);
-          ptx::tma_load_2d_hint(kd + HALF, &p.k, k_full0 + 8 * s, 64, kvrow + j * TK, pol);
+          ptx::tma_load_2d_hint(kd, &p.k, k_full0 + 8 * s, 0, kvrow + it.y + j * TK, pol);
+          ptx::tma_load_2d_hint(kd + HALF, &p.k, k_full0 + 8 * s, 64, kvrow + it.y + j * TK, pol);
           ++gk;
-          s = gv & 1;
-          u = gv >> 1;
-          if (gv >= 2 && !ptx::mbar_wait(v_empty0 + 8 * s, (u - 1) & 1, &abort_flag, p.status)) {
+        }
+        if (stop) break;
+      }
+      // nothing of ours may still be landing in shared memory when the CTA exits
+      for (int i = nq_loads > 2 ? nq_loads - 2 : 0; i < nq_loads; ++i)
+        drain(q_full0 + 8 * (i & 1), (i >> 1) & 1, p.status);
+      for (int g = gk > 2 ? gk - 2 : 0; g < gk; ++g) drain(k_full0 + 8 * (g & 1), (g >> 1) & 1, p.status);
+    }
+  } else if (warp == WARP_V) {
+    // ---------------------------------------------------- V loads
+    if (lane == 0) {
+      const uint64_t pol = ptx::policy_evict_first();
+      int gv = 0;
+      bool stop = false;
+      for (int n = 0; !stop; ++n) {
+        const int slot = n % kRing;
+        if (!ptx::mbar_wait(it_full0 + 8 * slot, (n / kRing) & 1, &abort_flag, p.status)) break;
+        const int4 it = ring[slot];
+        ptx::mbar_arrive(it_empty0 + 8 * slot);
+        if (it.x < 0) break;
+        const int b = it.x / p.n_kv, kvh = it.x - b * p.n_kv;
+        const int kvrow = (b * p.n_kv + kvh) * p.capacity;
+        const int ntiles = (it.z - it.y + TK - 1) / TK;
+        for (int j = 0; j < ntiles; ++j) {
+          const int s = gv % PL::V_STAGES, u = gv / PL::V_STAGES;
+          if (gv >= PL::V_STAGES &&
+              !ptx::mbar_wait(v_empty0 + 8 * s, (u - 1) & 1, &abort_flag, p.status)) {
             stop = true;
             break;
           }
-          const uint32_t vd = sbase + OFF_V + s * TILE;
+          const uint32_t vd = sbase + PL::OFF_V + s * TILE;
           ptx::mbar_arrive_expect_tx(v_full0 + 8 * s, TILE);
-          ptx::tma_load_2d_hint(vd, &p.v, v_full0 + 8 * s, 0, kvrow + j * TK, pol);
-          ptx::tma_load_2d_hint(vd + HALF, &p.v, v_full0 + 8 * s, 64, kvrow + j * TK, pol);
+          ptx::tma_load_2d_hint(vd, &p.v, v_full0 + 8 * s, 0, kvrow + it.y + j * TK, pol);
+          ptx::tma_load_2d_hint(vd + HALF, &p.v, v_full0 + 8 * s, 64, kvrow + it.y + j * TK, pol);
           ++gv;
         }
       }
-      // nothing of ours may still be landing in shared memory when the CTA exits
-      if (n > 0) drain(q_full, (n - 1) & 1, p.status);
-      for (int g = gk > 2 ? gk - 2 : 0; g < gk; ++g) drain(k_full0 + 8 * (g & 1), (g >> 1) & 1, p.status);
-      for (int g = gv > 2 ? gv - 2 : 0; g < gv; ++g) drain(v_full0 + 8 * (g & 1), (g >> 1) & 1, p.status);
+      for (int g = gv > PL::V_STAGES ? gv - PL::V_STAGES : 0; g < gv; ++g)
+        drain(v_full0 + 8 * (g % PL::V_STAGES), (g / PL::V_STAGES) & 1, p.status);
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == WARP_MMA) {
+    // ---------------------------------------------------- MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, TK);
-      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, 128) | (1u << 16);  // B (V) MN-major
-      int gt = 0, n = 0;
+      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, 128) | (1u << 16);  // V MN-major
+      int gt = 0;
       bool stop = false;
-      for (int i = blockIdx.x; i < p.total_items && !stop; i += gridDim.x) {
-        const Item it = decode(p, i);
-        if (!it.valid) continue;
-        if (!ptx::mbar_wait(q_full, n & 1, &abort_flag, p.status)) break;
-        const int T = it.ntiles, base = gt;
+      for (int n = 0; !stop; ++n) {
+        const int slot = n % kRing;
+        if (!ptx::mbar_wait(it_full0 + 8 * slot, (n / kRing) & 1, &abort_flag, p.status)) break;
+        const int4 it = ring[slot];
+        ptx::mbar_arrive(it_empty0 + 8 * slot);
+        if (it.x < 0) break;
+        const int qb = n & 1;
+        if (!ptx::mbar_wait(q_full0 + 8 * qb, (n >> 1) & 1, &abort_flag, p.status)) break;
+        const int T = (it.z - it.y + TK - 1) / TK, base = gt;
+        const uint32_t qa = sbase + PL::q_base(qb);
         auto issue_s = [&](int j) -> bool {
           const int g = base + j, s = g & 1, u = g >> 1;
           if (g >= 2 && !ptx::mbar_wait(s_free0 + 8 * s, (u - 1) & 1, &abort_flag, p.status))
             return false;
           if (!ptx::mbar_wait(k_full0 + 8 * s, u & 1, &abort_flag, p.status)) return false;
           ptx::tc_fence_after();
-          const uint32_t qa = sbase + OFF_Q, ka = sbase + OFF_K + s * TILE;
+          const uint32_t ka = sbase + PL::OFF_K + s * TILE;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
@@ -231,68 +381,56 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           }
           ptx::mma_commit(k_empty0 + 8 * s);
           ptx::mma_commit(s_full0 + 8 * s);
-          if (j == T - 1) ptx::mma_commit(q_empty);
+          if (j == T - 1) ptx::mma_commit(q_empty0 + 8 * qb);
           return true;
         };
         if (!issue_s(0) || (T > 1 && !issue_s(1))) break;
         for (int j = 0; j < T; ++j) {
-          const int g = base + j, s = g & 1, u = g >> 1;
+          const int g = base + j, vs = g % PL::V_STAGES, vu = g / PL::V_STAGES;
           if (!ptx::mbar_wait(p_full, g & 1, &abort_flag, p.status) ||
-              !ptx::mbar_wait(v_full0 + 8 * s, u & 1, &abort_flag, p.status)) {
+              !ptx::mbar_wait(v_full0 + 8 * vs, vu & 1, &abort_flag, p.status)) {
             stop = true;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t pa = sbase + OFF_P, va = sbase + OFF_V + s * TILE;
+          const uint32_t va = sbase + PL::OFF_V + vs * TILE;
+          const uint32_t pa = tmem + TM_P + (g & 1) * 64;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            ptx::mma_bf16(tmem + TM_O,
-                          ptx::smem_desc_sw128(pa + (kk >> 2) * HALF + (kk & 3) * 32),
-                          ptx::smem_desc_sw128_mn(va + kk * 2048, HALF), idesc_pv,
-                          (j > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(v_empty0 + 8 * s);
-          ptx::mma_commit(pv_done);
+            mma_bf16_ts(tmem + TM_O, pa + kk * 8, ptx::smem_desc_sw128_mn(va + kk * 2048, HALF),
+                        idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_commit(v_empty0 + 8 * vs);
+          ptx::mma_commit(pv_done0 + 8 * (g & 1));
           if (j + 2 < T && !issue_s(j + 2)) {
             stop = true;
             break;
           }
         }
         gt = base + T;
-        ++n;
       }
       // every MMA has finished before TMEM is released
-      if (gt > 0) drain(pv_done, (gt - 1) & 1, p.status);
+      for (int g = gt > 2 ? gt - 2 : 0; g < gt; ++g) drain(pv_done0 + 8 * (g & 1), (g >> 1) & 1, p.status);
     }
-  } else if (warp < nsw) {
-    // ------------------------------------------------------------ softmax rows
-    // DUP: the query rows fill TMEM lanes 0-63 and again 64-127; warps 0-1 take
-    // columns 0-63 of each row and warps 2-3 columns 64-127, and exchange the tile
-    // maximum and the final row sum through shared memory.
-    const int rt = warp * 32 + lane;                 // TMEM lane = S / O row
-    const int qr = DUP ? (rt & 63) : rt;             // query row (g * bs + t)
-    const int half = DUP ? (warp >> 1) : 0;
-    const int coff = half * NCOL;                    // first column this thread owns
-    const bool rvalid = qr < p.R;
-    const int gq = rvalid ? qr / p.bs : 0, t = rvalid ? qr - gq * p.bs : 0;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t nsync = 32 * nsw;
-    uint8_t* pbase = smem + OFF_P;
+  } else if (soft) {
+    // ---------------------------------------------------- softmax
+    const int rt = (warp & 3) * 32 + lane;          // TMEM lane = query row g * bs + t
+    const int half = warp >> 2;                      // S columns 64 * half .. + 63
+    const int coff = half * NCOL;
+    const bool rvalid = rt < p.R;
+    const int gq = rvalid ? rt / p.bs : 0, t = rvalid ? rt - gq * p.bs : 0;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     int gt = 0;
     float s[NCOL];
-    for (int i = blockIdx.x; i < p.total_items; i += gridDim.x) {
-      const Item it = decode(p, i);
-      if (!it.ok) {
-        // a refused sequence (capacity / table): its output rows are zero
-        if (it.c == 0 && rvalid) {
-          uint4* o = reinterpret_cast<uint4*>(p.out + ((size_t)(it.b * p.bs + t) * p.n_h +
-                                                       it.kvh * p.G + gq) * 128 + coff);
-          for (int k = 0; k < NCOL / 8; ++k) o[k] = make_uint4(0, 0, 0, 0);
-        }
-        continue;
-      }
-      if (!it.valid) continue;
-      const int T = it.ntiles;
-      const int qpos = it.start + t;
+    for (int n = 0;; ++n) {
+      const int slot = n % kRing;
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(it_full0 + 8 * slot, (n / kRing) & 1, &abort_flag, p.status)))
+        break;
+      const int4 it = ring[slot];
+      ptx::mbar_arrive(it_empty0 + 8 * slot);
+      if (it.x < 0) break;
+      const int b = it.x / p.n_kv, kvh = it.x - b * p.n_kv;
+      const int T = (it.z - it.y + TK - 1) / TK;
+      const int qpos = p.lens[b] + t;
       float m_ref = -INFINITY, l = 0.f;
       bool alive = true;
       for (int j = 0; j < T && alive; ++j) {
@@ -311,8 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         ptx::tc_fence_before();
         ptx::mbar_arrive(s_free0 + 8 * sb);
         // raw tile maximum over this thread's columns (masked keys -> -inf)
-        const int key0 = it.c0 + j * TK + coff;
-        const bool full = rvalid && key0 + NCOL <= it.c1 && (p.window <= 0 || qpos - key0 < p.window);
+        const int key0 = it.y + j * TK + coff;
+        const bool full = rvalid && key0 + NCOL <= it.z && (p.window <= 0 || qpos - key0 < p.window);
         float mx;
         if (full) {
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -324,17 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 #pragma unroll
           for (int e = 0; e < NCOL; ++e) {
             const int key = key0 + e;
-            const bool vis = rvalid && key < it.c1 && (p.window <= 0 || qpos - key < p.window);
+            const bool vis = rvalid && key < it.z && (p.window <= 0 || qpos - key < p.window);
             s[e] = vis ? s[e] : -INFINITY;
             mx = fmaxf(mx, s[e]);
           }
         }
-        if (DUP) {
-          xch[j & 1][half][qr] = mx;
-          ptx::named_sync(2, nsync);
-          mx = fmaxf(mx, xch[j & 1][half ^ 1][qr]);
-        }
-        mx *= p.sl2;  // log2 domain
+        xch[j & 1][half][rt] = mx;
+        ptx::named_sync(2, n_soft);
+        mx = fmaxf(mx, xch[j & 1][half ^ 1][rt]) * p.sl2;  // log2 domain
         float alpha = 1.f;
         bool resc = false;
         if (m_ref == -INFINITY) {
@@ -348,75 +483,68 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const float2 sl2v = make_float2(p.sl2, p.sl2), nmu = make_float2(-mu, -mu);
         float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                           make_float2(0.f, 0.f)};
+        uint32_t pk[NCOL / 2];
 #pragma unroll
         for (int e = 0; e < NCOL; e += 2) {
           const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), sl2v, nmu);
-          s[e] = ptx::ex2(x.x);
-          s[e + 1] = ptx::ex2(x.y);
-          acc2[(e >> 1) & 3] = __fadd2_rn(acc2[(e >> 1) & 3], make_float2(s[e], s[e + 1]));
+          const float2 y = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+          acc2[(e >> 1) & 3] = __fadd2_rn(acc2[(e >> 1) & 3], y);
+          pk[e >> 1] = pack_bf16(y.x, y.y);
         }
         const float2 a01 = __fadd2_rn(acc2[0], acc2[1]), a23 = __fadd2_rn(acc2[2], acc2[3]);
         l = l * alpha + ((a01.x + a01.y) + (a23.x + a23.y));
-        if (j > 0) {
-          // PV of the previous tile done: P may be overwritten, O holds tiles < j
-          alive = __all_sync(0xffffffffu, ptx::mbar_wait(pv_done, (g - 1) & 1, &abort_flag, p.status));
+        if (__any_sync(0xffffffffu, resc) && j > 0) {
+          // O holds tiles < j once the previous PV is done; scale this thread's columns
+          alive = __all_sync(0xffffffffu, ptx::mbar_wait(pv_done0 + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1, &abort_flag, p.status));
           if (!alive) break;
           ptx::tc_fence_after();
-          if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-            for (int cc = 0; cc < NCOL / 32; ++cc) {
-              uint32_t v[32];
-              ptx::tmem_ld_32x32b_x32(tmem + lane_base + TM_O + coff + cc * 32, v);
-              ptx::tmem_ld_wait();
+          for (int cc = 0; cc < NCOL / 32; ++cc) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(tmem + lane_base + TM_O + coff + cc * 32, v);
+            ptx::tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-              ptx::tmem_st_32x32b_x32(tmem + lane_base + TM_O + coff + cc * 32, v);
-            }
-            ptx::tmem_st_wait();
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            ptx::tmem_st_32x32b_x32(tmem + lane_base + TM_O + coff + cc * 32, v);
           }
+          ptx::tmem_st_wait();
         }
-        // P, bf16, in the 128-byte-swizzled K-major layout the MMA reads: this thread's
-        // keys coff .. coff+NCOL-1 of query row qr (and of its copy qr + 64 under DUP)
-#pragma unroll
-        for (int cidx = 0; cidx < NCOL / 8; ++cidx) {
-          const int key = coff + 8 * cidx, kb = key >> 6, cc = (key >> 3) & 7;
-          uint4 w;
-          w.x = pack_bf16(s[8 * cidx + 0], s[8 * cidx + 1]);
-          w.y = pack_bf16(s[8 * cidx + 2], s[8 * cidx + 3]);
-          w.z = pack_bf16(s[8 * cidx + 4], s[8 * cidx + 5]);
-          w.w = pack_bf16(s[8 * cidx + 6], s[8 * cidx + 7]);
-          *reinterpret_cast<uint4*>(pbase + kb * HALF + qr * 128 + ((cc ^ (qr & 7)) << 4)) = w;
-          if (DUP)
-            *reinterpret_cast<uint4*>(pbase + kb * HALF + (qr + 64) * 128 + ((cc ^ (qr & 7)) << 4)) = w;
-        }
-        // keys past the chunk end in the last tile: zero their V rows (slots past the
-        // cache length may hold anything, and 0 * NaN would poison O)
-        const int nvalid = it.c1 - (it.c0 + j * TK);
-        if (j == T - 1 && nvalid < TK) {
-          alive = __all_sync(0xffffffffu, ptx::mbar_wait(v_full0 + 8 * sb, u & 1, &abort_flag, p.status));
+        // P buffer g & 1 is free once the PV of tile g - 2 is done
+        if (g >= 2) {
+          alive = __all_sync(0xffffffffu, ptx::mbar_wait(pv_done0 + 8 * sb, ((g - 2) >> 1) & 1, &abort_flag, p.status));
           if (!alive) break;
-          uint4* vz = reinterpret_cast<uint4*>(smem + OFF_V + sb * TILE);
+          ptx::tc_fence_after();
+        }
+        ptx::tmem_st_32x32b_x32(tmem + lane_base + TM_P + sb * 64 + half * 32, pk);
+        ptx::tmem_st_wait();
+        // keys past the range end in the last tile: zero their V rows (slots past the
+        // cache length may hold anything, and 0 * NaN would poison O)
+        const int nvalid = it.z - (it.y + j * TK);
+        if (j == T - 1 && nvalid < TK) {
+          const int vs = g % PL::V_STAGES, vu = g / PL::V_STAGES;
+          alive = __all_sync(0xffffffffu, ptx::mbar_wait(v_full0 + 8 * vs, vu & 1, &abort_flag, p.status));
+          if (!alive) break;
+          uint4* vz = reinterpret_cast<uint4*>(smem + PL::OFF_V + vs * TILE);
           const int per_half = (TK - nvalid) * 8;  // 16-byte chunks per half
-          for (int idx = rt; idx < 2 * per_half; idx += nsync) {
+          const int me = half * 32 * nq + rt;
+          for (int idx = me; idx < 2 * per_half; idx += n_soft) {
             const int h = idx / per_half, rem = idx - h * per_half;
             vz[(h * HALF) / 16 + nvalid * 8 + rem] = make_uint4(0, 0, 0, 0);
           }
+          ptx::fence_proxy_async_smem();
         }
-        ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         ptx::mbar_arrive(p_full);
       }
       if (!alive) break;
       gt += T;
-      // ---- epilogue: this thread's columns of O for this item
-      if (DUP) {
-        // row sum of both halves; the barrier also ends every read of xch for this item
-        xl[half][qr] = l;
-        ptx::named_sync(2, nsync);
-        l += xl[half ^ 1][qr];
-      }
-      alive = __all_sync(0xffffffffu, ptx::mbar_wait(pv_done, (gt - 1) & 1, &abort_flag, p.status));
-      if (!alive) break;
+      // ---- epilogue: this thread's 64 columns of O for this item
+      xl[half][rt] = l;
+      ptx::named_sync(2, n_soft);
+      l += xl[half ^ 1][rt];
+      const int gl = gt - 1;
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(pv_done0 + 8 * (gl & 1), (gl >> 1) & 1, &abort_flag, p.status)))
+        break;
       ptx::tc_fence_after();
 #pragma unroll
       for (int cc = 0; cc < NCOL / 32; ++cc) {
@@ -426,82 +554,77 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 #pragma unroll
         for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(v[e]);
       }
-      const int bk = it.b * p.n_kv + it.kvh;
-      bf16* orow = p.out + ((size_t)(it.b * p.bs + t) * p.n_h + it.kvh * p.G + gq) * 128 + coff;
-      if (it.nchunks == 1) {
-        if (rvalid) {
-          const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-          for (int k = 0; k < NCOL / 8; ++k) {
-            uint4 w;
-            w.x = pack_bf16(s[8 * k + 0] * inv, s[8 * k + 1] * inv);
-            w.y = pack_bf16(s[8 * k + 2] * inv, s[8 * k + 3] * inv);
-            w.z = pack_bf16(s[8 * k + 4] * inv, s[8 * k + 5] * inv);
-            w.w = pack_bf16(s[8 * k + 6] * inv, s[8 * k + 7] * inv);
-            reinterpret_cast<uint4*>(orow)[k] = w;
-          }
-        }
-        continue;
-      }
-      // several chunks: publish this chunk's partial, the last one merges
-      const size_t prow_idx = ((size_t)bk * p.max_chunks + it.c) * p.R + qr;
-      if (rvalid) {
-        float4* a = reinterpret_cast<float4*>(p.part_acc + prow_idx * 128 + coff);
-#pragma unroll
-        for (int k = 0; k < NCOL / 4; ++k) a[k] = make_float4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
-        if (half == 0) p.part_ml[prow_idx] = make_float2(m_ref, l);
-      }
-      __threadfence();
-      ptx::named_sync(1, nsync);
-      if (threadIdx.x == 0) last_flag = (atomicAdd(p.counters + bk, 1) == it.nchunks - 1);
-      ptx::named_sync(1, nsync);
-      if (!last_flag) continue;
-      __threadfence();
-      if (rvalid) {
-        const size_t base = (size_t)bk * p.max_chunks * p.R + qr;
-        float M = -INFINITY;
-        for (int c = 0; c < it.nchunks; ++c) M = fmaxf(M, __ldcg(p.part_ml + base + (size_t)c * p.R).x);
-        float L = 0.f;
-        float acc[NCOL];
-#pragma unroll
-        for (int e = 0; e < NCOL; ++e) acc[e] = 0.f;
-        for (int c = 0; c < it.nchunks; ++c) {
-          const float2 ml = __ldcg(p.part_ml + base + (size_t)c * p.R);
-          if (ml.y == 0.f) continue;
-          const float w = ptx::ex2(ml.x - M);
-          L += w * ml.y;
-          const float4* a = reinterpret_cast<const float4*>(p.part_acc + (base + (size_t)c * p.R) * 128 + coff);
-#pragma unroll
-          for (int k = 0; k < NCOL / 4; ++k) {
-            const float4 x = __ldcg(a + k);
-            acc[4 * k] += w * x.x;
-            acc[4 * k + 1] += w * x.y;
-            acc[4 * k + 2] += w * x.z;
-            acc[4 * k + 3] += w * x.w;
-          }
-        }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
+      ptx::tc_fence_before();
+      if (!rvalid) continue;
+      if (it.w < 0) {
+        bf16* orow = p.out + ((size_t)(b * p.bs + t) * p.n_h + kvh * p.G + gq) * 128 + coff;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
         for (int k = 0; k < NCOL / 8; ++k) {
           uint4 w;
-          w.x = pack_bf16(acc[8 * k + 0] * inv, acc[8 * k + 1] * inv);
-          w.y = pack_bf16(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
-          w.z = pack_bf16(acc[8 * k + 4] * inv, acc[8 * k + 5] * inv);
-          w.w = pack_bf16(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
+          w.x = pack_bf16(s[8 * k + 0] * inv, s[8 * k + 1] * inv);
+          w.y = pack_bf16(s[8 * k + 2] * inv, s[8 * k + 3] * inv);
+          w.z = pack_bf16(s[8 * k + 4] * inv, s[8 * k + 5] * inv);
+          w.w = pack_bf16(s[8 * k + 6] * inv, s[8 * k + 7] * inv);
           reinterpret_cast<uint4*>(orow)[k] = w;
         }
+      } else {
+        const size_t prow = ((size_t)it.x * p.max_splits + it.w) * p.R + rt;
+        float4* a = reinterpret_cast<float4*>(p.part_acc + prow * 128 + coff);
+#pragma unroll
+        for (int k = 0; k < NCOL / 4; ++k) a[k] = make_float4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
+        if (half == 0) p.part_ml[prow] = make_float2(m_ref, l);
       }
     }
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == WARP_MMA) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
 }
 
-// ---- host side ---------------------------------------------------------------
+// ---------------------------------------------------------------------------
+// combine: one warp per (pair, query row)
+// ---------------------------------------------------------------------------
+__global__ void attn_combine_kernel(AttnTcParams p, const int* splits) {
+  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= p.batch * p.n_kv * p.R) return;
+  const int pr = wid / p.R, r = wid - pr * p.R;
+  const int n = splits[pr];
+  if (n == 1) return;  // written by the attention kernel
+  const int b = pr / p.n_kv, kvh = pr - b * p.n_kv;
+  const int gq = r / p.bs, t = r - gq * p.bs;
+  bf16* orow = p.out + ((size_t)(b * p.bs + t) * p.n_h + kvh * p.G + gq) * 128;
+  float o[4] = {0.f, 0.f, 0.f, 0.f};
+  if (n > 1) {
+    const size_t base = (size_t)pr * p.max_splits * p.R + r;
+    float M = -INFINITY;
+    for (int c = 0; c < n; ++c) M = fmaxf(M, p.part_ml[base + (size_t)c * p.R].x);
+    float L = 0.f;
+    for (int c = 0; c < n; ++c) {
+      const float2 ml = p.part_ml[base + (size_t)c * p.R];
+      if (ml.y == 0.f) continue;
+      const float w = ptx::ex2(ml.x - M);
+      L += w * ml.y;
+      const float4 x = reinterpret_cast<const float4*>(p.part_acc + (base + (size_t)c * p.R) * 128)[lane];
+      o[0] += w * x.x;
+      o[1] += w * x.y;
+      o[2] += w * x.z;
+      o[3] += w * x.w;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] *= inv;
+  }
+  // n == 0: a refused sequence, its rows are zero
+  uint2 w;
+  w.x = pack_bf16(o[0], o[1]);
+  w.y = pack_bf16(o[2], o[3]);
+  reinterpret_cast<uint2*>(orow)[lane] = w;
+}
 
 int sm_count() {
   static std::mutex mu;
@@ -518,12 +641,23 @@ int sm_count() {
   return count[dev];
 }
 
+template <bool NARROW>
+cudaError_t launch_attn(const AttnTcParams& p, int grid, cudaStream_t s) {
+  const size_t smem = Plan<NARROW>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NARROW>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  LaunchScope ls_(DFLASH_KERNEL_ATTENTION, s);
+  attn_tc_kernel<NARROW><<<grid, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 // bf16 row-major [rows][cols] matrix, box {64, box_rows}, 128-byte swizzle (gemm_tc.cu)
 bool encode_2d_bf16(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows);
 
-int attn_tc_chunk() { return CHUNK; }
+int attn_tc_chunk() { return TK * kItemMinTiles; }
 
 cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   if (a.batch <= 0) return cudaSuccess;
@@ -531,43 +665,63 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   AttnTcParams p;
   memset(&p, 0, sizeof(p));
   const int R = (a.n_h / a.n_kv) * a.bs;
-  const bool dup = R <= 64;
-  if (!encode_2d_bf16(&p.q, a.q, (long long)a.batch * a.n_h * a.bs, 128, dup ? 64 : 128) ||
+  const bool narrow = R <= 64;
+  if (!encode_2d_bf16(&p.q, a.q, (long long)a.batch * a.n_h * a.bs, 128, narrow ? 64 : 128) ||
       !encode_2d_bf16(&p.k, a.cache_k, (long long)a.batch * a.n_kv * a.capacity, 128, 128) ||
       !encode_2d_bf16(&p.v, a.cache_v, (long long)a.batch * a.n_kv * a.capacity, 128, 128))
     return cudaErrorInvalidValue;
+  const int pairs = a.batch * a.n_kv;
+  p.max_splits = a.n_chunks;  // ranges are cut into at most this many items
+  int4* items = (int4*)a.sched;
+  int* splits = (int*)(items + (size_t)pairs * p.max_splits);
+  int* ctr = splits + pairs;  // [0] item count, [1] next item
   p.lens = a.lens;
   p.out = (bf16*)a.out;
   p.part_acc = a.part_acc;
   p.part_ml = a.part_ml;
-  p.counters = a.counters;
+  p.items = items;
+  p.n_items = ctr;
+  p.next_item = ctr + 1;
   p.status = a.status;
   p.batch = a.batch;
   p.n_h = a.n_h;
   p.n_kv = a.n_kv;
   p.bs = a.bs;
   p.G = a.n_h / a.n_kv;
-  p.R = p.G * a.bs;
+  p.R = R;
   p.capacity = a.capacity;
   p.window = a.window;
   p.table_len = a.table_len;
-  p.max_chunks = a.n_chunks;
-  p.total_items = a.n_chunks * a.batch * a.n_kv;
   p.sl2 = a.scaling * 1.4426950408889634f;
-  cudaError_t e = cudaMemsetAsync(a.counters, 0, sizeof(int) * a.batch * a.n_kv, s);
+  const int n_sm = sm_count();
+  SchedParams sp;
+  sp.lens = a.lens;
+  sp.items = items;
+  sp.n_items = ctr;
+  sp.next_item = ctr + 1;
+  sp.splits = splits;
+  sp.batch = a.batch;
+  sp.n_kv = a.n_kv;
+  sp.bs = a.bs;
+  sp.window = a.window;
+  sp.capacity = a.capacity;
+  sp.table_len = a.table_len;
+  sp.max_splits = p.max_splits;
+  sp.n_sm = n_sm;
+  {
+    LaunchScope ls_(DFLASH_KERNEL_SCHEDULE, s);
+    attn_schedule_kernel<<<1, 1024, 0, s>>>(sp);
+  }
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  int grid = sm_count();
-  if (grid > p.total_items) grid = p.total_items;
-  if (dup) {
-    e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
-    if (e != cudaSuccess) return e;
-    LaunchScope ls_(DFLASH_KERNEL_ATTENTION, s);
-    attn_tc_kernel<true><<<grid, kThreads, SMEM, s>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
-    if (e != cudaSuccess) return e;
-    LaunchScope ls_(DFLASH_KERNEL_ATTENTION, s);
-    attn_tc_kernel<false><<<grid, kThreads, SMEM, s>>>(p);
+  const int max_items = pairs * p.max_splits;
+  const int grid = n_sm < max_items ? n_sm : max_items;
+  e = narrow ? launch_attn<true>(p, grid, s) : launch_attn<false>(p, grid, s);
+  if (e != cudaSuccess) return e;
+  const int warps = pairs * R;
+  {
+    LaunchScope ls_(DFLASH_KERNEL_COMBINE, s);
+    attn_combine_kernel<<<(warps + 7) / 8, 256, 0, s>>>(p, splits);
   }
   return cudaGetLastError();
 }

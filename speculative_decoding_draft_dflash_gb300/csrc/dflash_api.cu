@@ -98,7 +98,7 @@ Weights qkv_weights(const dflash_dims* d, const void* W_Q, const void* W_K, cons
 // Scratch of each call, carved in a fixed order (base == nullptr only sizes it).
 struct CtxScratch { float* Y; int splits; };
 struct InjectScratch { float* Y; int splits; };
-struct BlockScratch { float* Y; int splits; void* q; float* part_acc; float2* part_ml; int* counters; };
+struct BlockScratch { float* Y; int splits; void* q; float* part_acc; float2* part_ml; void* sched; };
 
 CtxScratch carve_ctx(Carver& cv, const dflash_dims* d, int M) {
   CtxScratch s;
@@ -127,7 +127,9 @@ BlockScratch carve_block(Carver& cv, const dflash_dims* d, int batch, int capaci
   const size_t part_rows = (size_t)batch * d->n_h * n_chunks * d->block_size;
   s.part_acc = cv.take<float>(part_rows * d->d_h);
   s.part_ml = cv.take<float2>(part_rows);
-  s.counters = cv.take<int>((size_t)batch * d->n_kv);
+  // work items {pair, k_begin, k_end, split}, split count per pair, two counters
+  const size_t pairs = (size_t)batch * d->n_kv;
+  s.sched = cv.take<char>(pairs * n_chunks * 16 + pairs * 4 + 64);
   return s;
 }
 
@@ -334,7 +336,7 @@ DFLASH_API dflash_status dflash_block_attn(const dflash_dims* d, const dflash_kv
   p.out = out;
   p.part_acc = s.part_acc;
   p.part_ml = s.part_ml;
-  p.counters = s.counters;
+  p.sched = s.sched;
   p.status = status;
   p.batch = c->batch;
   p.n_h = d->n_h;

@@ -151,7 +151,7 @@ struct AttnParams {
   void* out;              // [batch][bs][n_h * d_h]
   float* part_acc;        // partial accumulators, per chunk
   float2* part_ml;        // partial (max, sum), per chunk
-  int* counters;          // [batch][n_kv] chunk-completion counters
+  void* sched;            // tensor-core path: work list, split counts and counters
   unsigned* status;       // device status word
   int batch, n_h, n_kv, d_h, bs, capacity, window, chunk, n_chunks, table_len;
   float scaling;

@@ -24,7 +24,7 @@ DFLASH_F32, DFLASH_BF16 = 0, 1
 DEV_CAPACITY, DEV_ROPE, DEV_CROP, DEV_ROWS, DEV_TIMEOUT = 1, 2, 4, 8, 16
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE = range(6)
 KERNEL_NAMES = {1: "gemm", 2: "rmsnorm", 3: "head_epilogue", 4: "attention", 5: "combine",
-                6: "lens", 7: "crop", 8: "rope_table"}
+                6: "lens", 7: "crop", 8: "rope_table", 9: "schedule"}
 KERNEL_IDS = {v: k for k, v in KERNEL_NAMES.items()}
 
 
