@@ -600,15 +600,21 @@ __global__ void attn_combine_kernel(AttnTcParams p, const int* splits) {
   bf16* orow = p.out + ((size_t)(b * p.bs + t) * p.n_h + kvh * p.G + gq) * 128;
   float o[4] = {0.f, 0.f, 0.f, 0.f};
   if (n > 1) {
+    // row maximum and sum over the splits, lane-strided, then the weighted rows
     const size_t base = (size_t)pr * p.max_splits * p.R + r;
     float M = -INFINITY;
-    for (int c = 0; c < n; ++c) M = fmaxf(M, p.part_ml[base + (size_t)c * p.R].x);
+    for (int c = lane; c < n; c += 32) M = fmaxf(M, p.part_ml[base + (size_t)c * p.R].x);
+    M = warp_max(M);
     float L = 0.f;
+    for (int c = lane; c < n; c += 32) {
+      const float2 ml = p.part_ml[base + (size_t)c * p.R];
+      if (ml.y > 0.f) L += ptx::ex2(ml.x - M) * ml.y;
+    }
+    L = warp_sum(L);
+#pragma unroll 4
     for (int c = 0; c < n; ++c) {
       const float2 ml = p.part_ml[base + (size_t)c * p.R];
-      if (ml.y == 0.f) continue;
-      const float w = ptx::ex2(ml.x - M);
-      L += w * ml.y;
+      const float w = ml.y > 0.f ? ptx::ex2(ml.x - M) : 0.f;
       const float4 x = reinterpret_cast<const float4*>(p.part_acc + (base + (size_t)c * p.R) * 128)[lane];
       o[0] += w * x.x;
       o[1] += w * x.y;

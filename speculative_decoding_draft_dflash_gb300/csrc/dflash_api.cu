@@ -110,8 +110,10 @@ CtxScratch carve_ctx(Carver& cv, const dflash_dims* d, int M) {
 InjectScratch carve_inject(Carver& cv, const dflash_dims* d, int M) {
   InjectScratch s;
   const int N = 2 * d->n_kv * d->d_h;
-  s.splits = gemm_splits(d->dtype, M, kv_weights(d, nullptr, nullptr), d->d);
-  s.Y = cv.take<float>((size_t)s.splits * M * N);
+  const Weights W = kv_weights(d, nullptr, nullptr);
+  s.splits = gemm_splits(d->dtype, M, W, d->d);
+  const bool fused = d->dtype == DFLASH_BF16 && gemm_tc_heads_ok(M, W, d->d);
+  s.Y = fused ? nullptr : cv.take<float>((size_t)s.splits * M * N);
   return s;
 }
 
@@ -121,8 +123,10 @@ BlockScratch carve_block(Carver& cv, const dflash_dims* d, int batch, int capaci
   const int N = (d->n_h + 2 * d->n_kv) * d->d_h;
   int chunk, n_chunks;
   attn_chunks(d, capacity, window, &chunk, &n_chunks);
-  s.splits = gemm_splits(d->dtype, rows, qkv_weights(d, nullptr, nullptr, nullptr), d->d);
-  s.Y = cv.take<float>((size_t)s.splits * rows * N);
+  const Weights W = qkv_weights(d, nullptr, nullptr, nullptr);
+  s.splits = gemm_splits(d->dtype, rows, W, d->d);
+  const bool fused = d->dtype == DFLASH_BF16 && gemm_tc_heads_ok(rows, W, d->d);
+  s.Y = fused ? nullptr : cv.take<float>((size_t)s.splits * rows * N);
   s.q = cv.take<char>((size_t)batch * d->n_h * d->block_size * d->d_h * esize(d));
   const size_t part_rows = (size_t)batch * d->n_h * n_chunks * d->block_size;
   s.part_acc = cv.take<float>(part_rows * d->d_h);
@@ -131,6 +135,17 @@ BlockScratch carve_block(Carver& cv, const dflash_dims* d, int batch, int capaci
   const size_t pairs = (size_t)batch * d->n_kv;
   s.sched = cv.take<char>(pairs * n_chunks * 16 + pairs * 4 + 64);
   return s;
+}
+
+// Projection + per-head epilogue: fused into the tcgen05 GEMM when no split-K
+// is needed, else fp32 partials (ep.Y) and a separate epilogue kernel.
+cudaError_t project_heads(const dflash_dims* d, const Segments& A, int M, const Weights& W,
+                          const HeadEpilogue& ep, unsigned* status, cudaStream_t stream) {
+  if (d->dtype == DFLASH_BF16 && gemm_tc_heads_ok(M, W, d->d))
+    return gemm_tc_heads(A, M, W, ep, status, stream);
+  cudaError_t e = gemm(d->dtype, A, M, W, const_cast<float*>(ep.Y), ep.ldY, status, stream);
+  if (e != cudaSuccess) return e;
+  return d->dtype == DFLASH_F32 ? head_epilogue(d->dtype, ep, stream) : head_epilogue_bf16(ep, stream);
 }
 
 }  // namespace
@@ -239,7 +254,6 @@ DFLASH_API dflash_status dflash_kv_inject(const dflash_dims* d, const dflash_kv_
   const size_t layer_elems = (size_t)c->batch * d->n_kv * c->capacity * d->d_h;
   const size_t es = esize(d);
   const int32_t* lens = c->lens + (size_t)layer * c->batch;
-  cudaError_t e = gemm(d->dtype, A, M, kv_weights(d, W_K, W_V), s.Y, N, status, stream);
   HeadEpilogue ep;
   ep.Y = s.Y;
   ep.splits = splits;
@@ -262,7 +276,7 @@ DFLASH_API dflash_status dflash_kv_inject(const dflash_dims* d, const dflash_kv_
   ep.cache_v = (char*)c->v + (size_t)layer * layer_elems * es;
   ep.capacity = c->capacity;
   ep.status = status;
-  if (e == cudaSuccess) e = head_epilogue(d->dtype, ep, stream);
+  cudaError_t e = project_heads(d, A, M, kv_weights(d, W_K, W_V), ep, status, stream);
   if (e == cudaSuccess)
     e = lens_advance(c->lens + (size_t)layer * c->batch, cu_rows, c->batch, 0, M, c->capacity,
                      table_len, stream);
@@ -304,7 +318,6 @@ DFLASH_API dflash_status dflash_block_attn(const dflash_dims* d, const dflash_kv
   void* ck = (char*)c->k + (size_t)layer * layer_elems * es;
   void* cvv = (char*)c->v + (size_t)layer * layer_elems * es;
   int32_t* lens = c->lens + (size_t)layer * c->batch;
-  cudaError_t e = gemm(d->dtype, A, rows, qkv_weights(d, W_Q, W_K, W_V), s.Y, N, status, stream);
   HeadEpilogue ep;
   ep.Y = s.Y;
   ep.splits = splits;
@@ -327,7 +340,7 @@ DFLASH_API dflash_status dflash_block_attn(const dflash_dims* d, const dflash_kv
   ep.cache_v = cvv;
   ep.capacity = c->capacity;
   ep.status = status;
-  if (e == cudaSuccess) e = head_epilogue(d->dtype, ep, stream);
+  cudaError_t e = project_heads(d, A, rows, qkv_weights(d, W_Q, W_K, W_V), ep, status, stream);
   AttnParams p;
   p.q = s.q;
   p.cache_k = ck;

@@ -131,6 +131,16 @@ struct HeadEpilogue {
 };
 cudaError_t head_epilogue(int dtype, const HeadEpilogue& e, cudaStream_t s);
 
+// tcgen05 GEMM with the per-head epilogue fused (bf16, d_h = 128), for shapes
+// that fill the GPU without split-K (gemm_tc_heads_ok): the projection rows go
+// through norm / RoPE straight into Q and the cache.
+bool gemm_tc_heads_ok(int M, const Weights& W, int K);
+cudaError_t gemm_tc_heads(const Segments& A, int M, const Weights& W, const HeadEpilogue& ep,
+                          unsigned* status, cudaStream_t s);
+
+// Warp-per-(row, head) epilogue for bf16 with d_h = 128 (sums the split-K partials).
+cudaError_t head_epilogue_bf16(const HeadEpilogue& e, cudaStream_t s);
+
 // lens[b] += n_b where the append fitted (same checks as the epilogue)
 cudaError_t lens_advance(int32_t* lens, const int32_t* cu_rows, int batch, int bs, int M,
                          int capacity, int table_len, cudaStream_t s);

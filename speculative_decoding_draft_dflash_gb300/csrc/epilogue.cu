@@ -45,6 +45,65 @@ __global__ void rmsnorm_rows_kernel(const float* __restrict__ Y, int splits, int
   }
 }
 
+// Single pass: each thread keeps its float4 chunks of the row (summed over the
+// splits) in registers, one block reduction, then scale and store. N <= 8192.
+constexpr int kNormThreads = 256, kNormMaxChunks = 8;
+
+template <typename T>
+__device__ __forceinline__ void store4(T* dst, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float* dst, float4 v) {
+  *reinterpret_cast<float4*>(dst) = v;
+}
+template <>
+__device__ __forceinline__ void store4<bf16>(bf16* dst, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_vec_kernel(
+    const float* __restrict__ Y, int splits, int M, int N, const T* __restrict__ gamma, float eps,
+    T* __restrict__ out) {
+  __shared__ float red[32];
+  const int row = blockIdx.x;
+  const int n4 = N >> 2;
+  const size_t split_stride4 = (size_t)M * n4;
+  const float4* y4 = reinterpret_cast<const float4*>(Y) + (size_t)row * n4;
+  float4 v[kNormMaxChunks];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < kNormMaxChunks; ++k) {
+    const int c = threadIdx.x + k * kNormThreads;
+    v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < n4) {
+      for (int s = 0; s < splits; ++s) {
+        const float4 a = y4[s * split_stride4 + c];
+        v[k].x += a.x;
+        v[k].y += a.y;
+        v[k].z += a.z;
+        v[k].w += a.w;
+      }
+      ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+    }
+  }
+  ss = block_sum(ss, red);
+  const float r = 1.0f / sqrtf(ss / (float)N + eps);
+#pragma unroll
+  for (int k = 0; k < kNormMaxChunks; ++k) {
+    const int c = threadIdx.x + k * kNormThreads;
+    if (c < n4) {
+      const float4 g = make_float4(to_f(gamma[4 * c]), to_f(gamma[4 * c + 1]), to_f(gamma[4 * c + 2]),
+                                   to_f(gamma[4 * c + 3]));
+      store4<T>(out + (size_t)row * N + 4 * c,
+                make_float4(v[k].x * r * g.x, v[k].y * r * g.y, v[k].z * r * g.z, v[k].w * r * g.w));
+    }
+  }
+}
+
 // One CTA per (row, head); thread i handles the RoPE pair (i, i + d_h/2).
 template <typename T>
 __global__ void head_epilogue_kernel(HeadEpilogue e) {
@@ -117,6 +176,89 @@ __global__ void head_epilogue_kernel(HeadEpilogue e) {
   dst[i + half] = from_f<T>(x1);
 }
 
+// bf16, d_h = 128: one warp per (row, head); lane l holds dims 4l .. 4l+3, so the
+// RoPE partner (i + 64) of lanes 0-15 sits in lane l + 16.
+__global__ void __launch_bounds__(256) head_epilogue_bf16_kernel(HeadEpilogue e) {
+  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int heads = e.n_q + 2 * e.n_kv;
+  if (wid >= e.rows * heads) return;
+  const int row = wid / heads, head = wid - row * heads;
+  int b, t, n_b;
+  if (e.cu_rows) {
+    int lo = 0, hi = e.batch - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (e.cu_rows[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    t = row - e.cu_rows[b];
+    n_b = e.cu_rows[b + 1] - e.cu_rows[b];
+    if (n_b < 0 || e.cu_rows[b + 1] > e.rows || e.cu_rows[0] != 0 || t < 0 || t >= n_b) {
+      if (lane == 0) atomicOr(e.status, DFLASH_DEV_ROWS);
+      return;
+    }
+  } else {
+    b = row / e.bs;
+    t = row - b * e.bs;
+    n_b = e.bs;
+  }
+  const int start = e.lens[b];
+  if (start < 0 || start + n_b > e.capacity || start + n_b > e.table_len) {
+    if (lane == 0 && t == 0 && head == 0)
+      atomicOr(e.status, (start + n_b > e.capacity || start < 0) ? DFLASH_DEV_CAPACITY
+                                                                 : DFLASH_DEV_ROPE);
+    return;
+  }
+  const int pos = start + t;
+  const size_t split_stride4 = (size_t)e.rows * e.ldY / 4;
+  const float4* y4 = reinterpret_cast<const float4*>(e.Y + (size_t)row * e.ldY + (size_t)head * 128) + lane;
+  float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < e.splits; ++s) {
+    const float4 a = y4[s * split_stride4];
+    x.x += a.x;
+    x.y += a.y;
+    x.z += a.z;
+    x.w += a.w;
+  }
+  const int kind = head < e.n_q ? 0 : (head < e.n_q + e.n_kv ? 1 : 2);  // Q, K, V
+  if (kind < 2) {
+    const float ss = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
+    const float r = 1.0f / sqrtf(ss * (1.0f / 128.f) + e.eps);
+    const bf16* g = (const bf16*)(kind == 0 ? e.gamma_q : e.gamma_k) + 4 * lane;
+    x.x *= r * __bfloat162float(g[0]);
+    x.y *= r * __bfloat162float(g[1]);
+    x.z *= r * __bfloat162float(g[2]);
+    x.w *= r * __bfloat162float(g[3]);
+    // partner values: dims i + 64 for lanes 0-15, i - 64 for lanes 16-31
+    float4 o;
+    o.x = __shfl_xor_sync(0xffffffffu, x.x, 16);
+    o.y = __shfl_xor_sync(0xffffffffu, x.y, 16);
+    o.z = __shfl_xor_sync(0xffffffffu, x.z, 16);
+    o.w = __shfl_xor_sync(0xffffffffu, x.w, 16);
+    const float2* cs = e.rope + (size_t)pos * 64 + 4 * (lane & 15);
+    const float sg = lane < 16 ? -1.f : 1.f;  // rotate_half: [-x2; x1]
+    const float2 c0 = cs[0], c1 = cs[1], c2 = cs[2], c3 = cs[3];
+    x.x = x.x * c0.x + sg * o.x * c0.y;
+    x.y = x.y * c1.x + sg * o.y * c1.y;
+    x.z = x.z * c2.x + sg * o.z * c2.y;
+    x.w = x.w * c3.x + sg * o.w * c3.y;
+  }
+  bf16* dst;
+  if (kind == 0) {
+    dst = (bf16*)e.q_out + (((size_t)b * e.n_q + head) * e.bs + t) * 128;
+  } else {
+    const int kvh = head - e.n_q - (kind == 2 ? e.n_kv : 0);
+    bf16* base = (bf16*)(kind == 1 ? e.cache_k : e.cache_v);
+    dst = base + (((size_t)b * e.n_kv + kvh) * e.capacity + pos) * 128;
+  }
+  __nv_bfloat162 lo2 = __floats2bfloat162_rn(x.x, x.y), hi2 = __floats2bfloat162_rn(x.z, x.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&lo2);
+  u.y = *reinterpret_cast<uint32_t*>(&hi2);
+  reinterpret_cast<uint2*>(dst)[lane] = u;
+}
+
 __global__ void lens_advance_kernel(int32_t* lens, const int32_t* cu_rows, int batch, int bs,
                                     int M, int capacity, int table_len) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
@@ -162,6 +304,16 @@ __global__ void rope_table_kernel(double theta, int d_h, int max_pos, float2* ta
 cudaError_t rmsnorm_rows(int dtype, const float* Y, int splits, int M, int N, const void* gamma,
                          float eps, void* out, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
+  if (N % 4 == 0 && N <= 4 * kNormThreads * kNormMaxChunks) {
+    LaunchScope ls_(DFLASH_KERNEL_RMSNORM, s);
+    if (dtype == DFLASH_F32)
+      rmsnorm_rows_vec_kernel<float><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, (const float*)gamma,
+                                                               eps, (float*)out);
+    else
+      rmsnorm_rows_vec_kernel<bf16><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, (const bf16*)gamma,
+                                                              eps, (bf16*)out);
+    return cudaGetLastError();
+  }
   if (dtype == DFLASH_F32)
     {
       LaunchScope ls_(DFLASH_KERNEL_RMSNORM, s);
@@ -191,6 +343,17 @@ cudaError_t head_epilogue(int dtype, const HeadEpilogue& e, cudaStream_t s) {
       LaunchScope ls_(DFLASH_KERNEL_HEAD_EPILOGUE, s);
       head_epilogue_kernel<bf16><<<grid, threads, 0, s>>>(e);
     }
+  return cudaGetLastError();
+}
+
+cudaError_t head_epilogue_bf16(const HeadEpilogue& e, cudaStream_t s) {
+  if (e.rows <= 0) return cudaSuccess;
+  if (e.d_h != 128) return cudaErrorInvalidValue;
+  const long long warps = (long long)e.rows * (e.n_q + 2 * e.n_kv);
+  {
+    LaunchScope ls_(DFLASH_KERNEL_HEAD_EPILOGUE, s);
+    head_epilogue_bf16_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(e);
+  }
   return cudaGetLastError();
 }
 

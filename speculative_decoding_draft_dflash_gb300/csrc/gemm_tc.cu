@@ -1,17 +1,28 @@
-// Tensor-core projection GEMM for sm_103a: Y = X W^T with bf16 inputs and an
+// Tensor-core projection GEMMs for sm_103a: X W^T with bf16 inputs and an
 // fp32 accumulator in tensor memory.
 //
-// One CTA computes a 128 x BN tile of Y over its share of K (split-K across
-// gridDim.z; the epilogue kernels sum the splits):
+// One CTA computes a 128 x BN tile over its share of K (split-K across
+// gridDim.z):
 //   warp 0      TMA producer: 128 x 64 activation tile + BN x 64 weight tile
 //               per stage, 128-byte swizzle, completion on a "full" mbarrier;
 //   warp 1      allocates BN TMEM columns and issues tcgen05.mma (M=128,
 //               N=BN, K=16, four per stage) from one thread; tcgen05.commit
 //               frees each stage ("empty" mbarrier) and finally signals "done";
-//   warps 2-5   epilogue: tcgen05.ld of their 32 TMEM lanes, fp32 stores.
+//   warps 2-5   epilogue, one thread per tile row (tcgen05.ld of its lanes).
 // The activations arrive as up to eight K-segments (the k target layers'
 // hidden states of the context projection), each with its own tensor map;
 // the weights as up to three matrices stacked along N (W_Q | W_K | W_V).
+//
+// Two epilogues:
+//   fp32 store   the tile (a split-K partial) goes to Y; the context
+//                projection's RMSNorm kernel sums the splits;
+//   heads        (no split-K) whole 128-dim heads per tile (BN = 128 or 256).
+//                The thread owning a row applies the per-head RMSNorm (Q and K
+//                heads), rotates the pair (i, i + 64) at the row's absolute
+//                position and stores the bf16 row into the Q buffer or the
+//                row's cache slot (DFlash KV Injection Walkthrough, Steps
+//                4.1-4.3; DFlash source guide (II), parts 1-4). Shapes that need
+//                split-K use the fp32 store and a separate epilogue kernel.
 #include <mutex>
 
 #include "sm100_ptx.cuh"
@@ -28,8 +39,9 @@ struct TcGemmParams {
   int w_count;
   int w_off[4];       // prefix offsets of the stacked weights along N
   int M, ldY;
-  int kb_total, kb_per_split;
-  float* Y;
+  int kb_total, kb_per_split, splits;
+  float* Y;           // fp32 store: [split][M][ldY]
+  HeadEpilogue ep;    // heads: norm / RoPE / destination
   unsigned* status;
 };
 
@@ -53,7 +65,84 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsign
   }
 }
 
-template <int BN>
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Per-head epilogue of one 128-wide row x[0..127] of the projection of tile
+// row `row` (global), head `head` of the stacked [Q | K | V] layout.
+__device__ __forceinline__ void head_row(const HeadEpilogue& e, int row, int head, float (&x)[128]) {
+  int b, t, n_b;
+  if (e.cu_rows) {
+    int lo = 0, hi = e.batch - 1;
+    while (lo < hi) {  // last b with cu_rows[b] <= row
+      const int mid = (lo + hi + 1) >> 1;
+      if (e.cu_rows[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    t = row - e.cu_rows[b];
+    n_b = e.cu_rows[b + 1] - e.cu_rows[b];
+    if (n_b < 0 || e.cu_rows[b + 1] > e.rows || e.cu_rows[0] != 0 || t < 0 || t >= n_b) {
+      atomicOr(e.status, DFLASH_DEV_ROWS);
+      return;
+    }
+  } else {
+    b = row / e.bs;
+    t = row - b * e.bs;
+    n_b = e.bs;
+  }
+  const int start = e.lens[b];
+  if (start < 0 || start + n_b > e.capacity || start + n_b > e.table_len) {
+    if (t == 0 && head == 0)
+      atomicOr(e.status, (start + n_b > e.capacity || start < 0) ? DFLASH_DEV_CAPACITY
+                                                                 : DFLASH_DEV_ROPE);
+    return;
+  }
+  const int pos = start + t;
+  const int kind = head < e.n_q ? 0 : (head < e.n_q + e.n_kv ? 1 : 2);  // Q, K, V
+  if (kind < 2) {
+    float ss0 = 0.f, ss1 = 0.f, ss2 = 0.f, ss3 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 128; i += 4) {
+      ss0 = fmaf(x[i], x[i], ss0);
+      ss1 = fmaf(x[i + 1], x[i + 1], ss1);
+      ss2 = fmaf(x[i + 2], x[i + 2], ss2);
+      ss3 = fmaf(x[i + 3], x[i + 3], ss3);
+    }
+    const float r = 1.0f / sqrtf(((ss0 + ss1) + (ss2 + ss3)) * (1.0f / 128.f) + e.eps);
+    const bf16* g = (const bf16*)(kind == 0 ? e.gamma_q : e.gamma_k);
+    const float2* cs = e.rope + (size_t)pos * 64;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const float x0 = x[i] * r * __bfloat162float(g[i]);
+      const float x1 = x[i + 64] * r * __bfloat162float(g[i + 64]);
+      const float2 c = cs[i];
+      x[i] = x0 * c.x - x1 * c.y;  // rotate_half: [-x1, x0]
+      x[i + 64] = x1 * c.x + x0 * c.y;
+    }
+  }
+  bf16* dst;
+  if (kind == 0) {
+    dst = (bf16*)e.q_out + (((size_t)b * e.n_q + head) * e.bs + t) * 128;
+  } else {
+    const int kvh = head - e.n_q - (kind == 2 ? e.n_kv : 0);
+    bf16* base = (bf16*)(kind == 1 ? e.cache_k : e.cache_v);
+    dst = base + (((size_t)b * e.n_kv + kvh) * e.capacity + pos) * 128;
+  }
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    uint4 w;
+    w.x = pack_bf16(x[8 * k + 0], x[8 * k + 1]);
+    w.y = pack_bf16(x[8 * k + 2], x[8 * k + 3]);
+    w.z = pack_bf16(x[8 * k + 4], x[8 * k + 5]);
+    w.w = pack_bf16(x[8 * k + 6], x[8 * k + 7]);
+    d4[k] = w;
+  }
+}
+
+template <int BN, bool HEADS>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcGemmParams p) {
   using C = Cfg<BN>;
   constexpr int STAGES = C::STAGES;
@@ -139,12 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   } else {
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 are this warp's
     const int row = q * 32 + lane;
+    const bool in = (m0 + row) < p.M;
     // warp-uniform: tcgen05.ld below is a .sync.aligned instruction
     const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(done, 0, &abort_flag, p.status));
     ptx::tc_fence_after();
-    if (ok) {
+    if (ok && !HEADS) {
       float* y = p.Y + (size_t)blockIdx.z * p.M * p.ldY + (size_t)(m0 + row) * p.ldY + n0;
-      const bool in = (m0 + row) < p.M;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -157,6 +246,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                  __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
         }
+      }
+    }
+    if (ok && HEADS) {
+      // BN / 128 whole heads per tile, one after the other; each thread owns one row.
+      // Every lane joins the tcgen05.ld (warp-collective); only rows < M are stored.
+#pragma unroll 1
+      for (int hd = 0; hd < BN / 128; ++hd) {
+        float x[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hd * 128 + c * 32), r);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(r[j]);
+        }
+        if (in) head_row(p.ep, m0 + row, n0 / 128 + hd, x);
       }
     }
   }
@@ -193,11 +299,15 @@ struct Plan {
   int bn, kb_total, kb_per_split, splits;
 };
 
-Plan plan(int M, const Weights& W, int K) {
+// The widest of 256/128/64 that divides every stacked weight (heads: 256 or
+// 128, whole heads per tile). Split-K to about one wave on the GPU.
+Plan plan(int M, const Weights& W, int K, bool heads) {
   Plan pl;
   pl.bn = 256;
   for (int i = 0; i < W.count; ++i)
     while (W.n[i] % pl.bn) pl.bn >>= 1;
+  if (heads && pl.bn < 128) pl.bn = 0;  // heads need whole 128-dim heads per tile
+  if (pl.bn == 0) return pl;
   pl.kb_total = K / BK;
   const int tiles = ((M + BM - 1) / BM) * (W.total() / pl.bn);
   int splits = 148 / (tiles > 0 ? tiles : 1);
@@ -207,6 +317,17 @@ Plan plan(int M, const Weights& W, int K) {
   pl.kb_per_split = (pl.kb_total + splits - 1) / splits;
   pl.splits = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
   return pl;
+}
+
+template <int BN, bool HEADS>
+cudaError_t launch(const TcGemmParams& p, dim3 grid, cudaStream_t s) {
+  const size_t smem = Cfg<BN>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, HEADS>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  LaunchScope ls_(DFLASH_KERNEL_GEMM, s);
+  gemm_tc_kernel<BN, HEADS><<<grid, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -225,31 +346,17 @@ bool encode_2d_bf16(CUtensorMap* m, const void* base, long long rows, int cols, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-namespace {
+int gemm_tc_splits(int M, const Weights& W, int K) { return plan(M, W, K, false).splits; }
 
-template <int BN>
-cudaError_t launch(const TcGemmParams& p, dim3 grid, cudaStream_t s) {
-  const size_t smem = Cfg<BN>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  LaunchScope ls_(DFLASH_KERNEL_GEMM, s);
-  gemm_tc_kernel<BN><<<grid, kThreads, smem, s>>>(p);
-  return cudaGetLastError();
+bool gemm_tc_heads_ok(int M, const Weights& W, int K) {
+  const Plan pl = plan(M, W, K, true);
+  return pl.bn >= 128 && pl.splits == 1;
 }
 
-}  // namespace
+namespace {
 
-int gemm_tc_splits(int M, const Weights& W, int K) { return plan(M, W, K).splits; }
-
-cudaError_t gemm_tc(const Segments& A, int M, const Weights& W, float* Y, int ldY,
-                    unsigned* status, cudaStream_t s) {
-  const int N = W.total();
-  if (M <= 0 || N <= 0) return cudaSuccess;
-  const int K = A.n * A.kseg;
-  const Plan pl = plan(M, W, K);
-  if (pl.bn < 64 || A.kseg % BK) return cudaErrorInvalidValue;
-  TcGemmParams p;
+cudaError_t fill_common(TcGemmParams& p, const Segments& A, int M, const Weights& W, const Plan& pl,
+                        int K) {
   memset(&p, 0, sizeof(p));
   for (int i = 0; i < A.n; ++i)
     if (!encode_2d_bf16(&p.a[i], A.p[i], M, A.kseg, BM)) return cudaErrorInvalidValue;
@@ -264,17 +371,49 @@ cudaError_t gemm_tc(const Segments& A, int M, const Weights& W, float* Y, int ld
   p.w_count = W.count;
   p.kseg_blocks = A.kseg / BK;
   p.M = M;
-  p.ldY = ldY;
   p.kb_total = pl.kb_total;
   p.kb_per_split = pl.kb_per_split;
+  p.splits = pl.splits;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t gemm_tc(const Segments& A, int M, const Weights& W, float* Y, int ldY,
+                    unsigned* status, cudaStream_t s) {
+  const int N = W.total();
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  const int K = A.n * A.kseg;
+  const Plan pl = plan(M, W, K, false);
+  if (pl.bn < 64 || A.kseg % BK) return cudaErrorInvalidValue;
+  TcGemmParams p;
+  cudaError_t e = fill_common(p, A, M, W, pl, K);
+  if (e != cudaSuccess) return e;
+  p.ldY = ldY;
   p.Y = Y;
   p.status = status;
   dim3 grid((M + BM - 1) / BM, N / pl.bn, pl.splits);
   switch (pl.bn) {
-    case 256: return launch<256>(p, grid, s);
-    case 128: return launch<128>(p, grid, s);
-    default: return launch<64>(p, grid, s);
+    case 256: return launch<256, false>(p, grid, s);
+    case 128: return launch<128, false>(p, grid, s);
+    default: return launch<64, false>(p, grid, s);
   }
+}
+
+cudaError_t gemm_tc_heads(const Segments& A, int M, const Weights& W, const HeadEpilogue& ep,
+                          unsigned* status, cudaStream_t s) {
+  const int N = W.total();
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  const int K = A.n * A.kseg;
+  const Plan pl = plan(M, W, K, true);
+  if (pl.bn < 128 || pl.splits != 1 || ep.d_h != 128 || A.kseg % BK) return cudaErrorInvalidValue;
+  TcGemmParams p;
+  cudaError_t e = fill_common(p, A, M, W, pl, K);
+  if (e != cudaSuccess) return e;
+  p.ep = ep;
+  p.status = status;
+  dim3 grid((M + BM - 1) / BM, N / pl.bn, 1);
+  return pl.bn == 256 ? launch<256, true>(p, grid, s) : launch<128, true>(p, grid, s);
 }
 
 }  // namespace dflash
