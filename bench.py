@@ -31,6 +31,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+TRACED = ["attention", "gemm", "combine", "head_epilogue", "rmsnorm", "schedule"]
 METRIC = "draft blocks/sec per layer at B=32, ctx≤4K, block 16; attn HBM GB/s vs roofline"
 UNIT = "blocks/s/layer"
 WORKLOAD = "serve_b32"
@@ -39,11 +40,12 @@ WORKLOAD = "serve_b32"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch every call eagerly")
     return ap.parse_args()
 
 
@@ -272,30 +274,51 @@ def run_ours(args, w):
     def step():
         dev.run_round(x, crop=True, stream=stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    assert D.dflash_status_get(stream) == 0, "device status after warm-up"
-
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
 
+    # eager warm-up (first calls resolve symbols and encode tensor maps), then the
+    # step captured in a CUDA graph: the timed region is one replay of K captured steps
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                step()
+        return g
+
+    if args.no_graph:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        launches0 = D.dflash_launch_count()
+        run_timed = lambda: [step() for _ in range(args.steps)]  # noqa: E731
+    else:
+        g1 = capture(1)
+        for _ in range(args.warmup):
+            g1.replay()
+        torch.cuda.synchronize()
+        assert D.dflash_status_get(stream) == 0, "device status after warm-up"
+        launches0 = D.dflash_launch_count()
+        gK = capture(args.steps)
+        run_timed = gK.replay
+    launches = D.dflash_launch_count() - launches0 if not args.no_graph else None
+
     # ---- timed region: K steps, CUDA events on the launching stream ----
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches0 = D.dflash_launch_count()
-    D.dflash_trace_start(["attention", "gemm", "combine", "head_epilogue", "rmsnorm", "schedule"],
-                         64 * args.steps)
     with ClockSampler(dev_index) as clk:
         barrier()
         ev0.record(stream)
-        for _ in range(args.steps):
-            step()
+        run_timed()
         ev1.record(stream)
         barrier()
-    trace = D.dflash_trace_stop()
-    launches = D.dflash_launch_count() - launches0
+    if args.no_graph:
+        launches = D.dflash_launch_count() - launches0
     t_ms = ev0.elapsed_time(ev1)
     if world > 1:
         tt = torch.tensor([t_ms], device="cuda")
@@ -304,6 +327,27 @@ def run_ours(args, w):
     ms_per_step = t_ms / args.steps
     value = world * w.batch * w.n_layers / (ms_per_step * 1e-3)
     assert D.dflash_status_get(stream) == 0, "device status after the timed region"
+
+    # ---- per-kernel durations: the same K steps again, with CUDA event pairs that
+    # the library records around each launch on its own stream (captured as event
+    # nodes). Kept out of the timed region above: each event node costs microseconds.
+    D.dflash_trace_start(TRACED, 64 * args.steps)
+    if args.no_graph:
+        t_ev0 = torch.cuda.Event(enable_timing=True)
+        t_ev1 = torch.cuda.Event(enable_timing=True)
+        t_ev0.record(stream)
+        run_timed()
+        t_ev1.record(stream)
+    else:
+        gT = capture(args.steps)
+        t_ev0 = torch.cuda.Event(enable_timing=True)
+        t_ev1 = torch.cuda.Event(enable_timing=True)
+        t_ev0.record(stream)
+        gT.replay()
+        t_ev1.record(stream)
+    torch.cuda.synchronize()
+    trace = D.dflash_trace_stop()
+    t_traced = t_ev0.elapsed_time(t_ev1)
 
     # ---- per-kernel times from the trace (same timed region) ----
     per = {}
@@ -315,7 +359,7 @@ def run_ours(args, w):
     for i, ms in enumerate(gemm_times):
         per.setdefault(gemm_names[i % len(gemm_names)], []).append(ms)
     kernels = {k: {"launches": len(v), "avg_us": 1e3 * sum(v) / len(v),
-                   "share_of_step": sum(v) / t_ms} for k, v in per.items() if v}
+                   "share_of_step": sum(v) / t_traced} for k, v in per.items() if v}
     pk = peaks()
     starts = L0 + w.new_ctx
     attn_bytes = attention_bytes(w, starts)
@@ -360,7 +404,12 @@ def run_ours(args, w):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_of(w), "clocks": clk.summary(), "e2e": e2e,
             "gpu_launches": int(launches), "roofline": roofline, "roofline_other": others,
-            "kernels": kernels}
+            "kernels": kernels,
+            "timing": ("value: one replay of a CUDA graph of the K steps, no tracing; kernel "
+                       "durations (roofline.achieved, kernels): a second replay of the same K "
+                       "steps with CUDA event pairs around each launch (%.3f ms/step with "
+                       "the events)" % (t_traced / args.steps)) if not args.no_graph else
+                      "eager launches; kernel durations from a second traced pass"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, total, n, _ = oracle_sample_rate(w, budget_s=12.0)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count(),
@@ -396,13 +445,30 @@ def run_e2e(args, w, dev, x, stream, D):
             for dst, src in zip(out_h, dev.out):
                 dst.copy_(src, non_blocking=True)
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(2):
         step()
+    torch.cuda.synchronize()
+    if args.no_graph:
+        for _ in range(max(3, args.warmup)):
+            step()
+    else:
+        g1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1, stream=stream):
+            step()
+        for _ in range(max(3, args.warmup)):
+            g1.replay()
+        gK = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gK, stream=stream):
+            for _ in range(args.steps):
+                step()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for _ in range(args.steps):
-        step()
+    if args.no_graph:
+        for _ in range(args.steps):
+            step()
+    else:
+        gK.replay()
     ev1.record(stream)
     torch.cuda.synchronize()
     assert D.dflash_status_get(stream) == 0

@@ -242,9 +242,11 @@ const char* dflash_status_string(dflash_status s);
 /*
  * Starts recording a CUDA event pair around every launch whose kind bit
  * (1u << kind) is set in kernel_mask, on the launch's own stream, for at most
- * max_launches launches (later ones are not recorded). The events are created
- * on the first call and kept for the process. Not thread-safe with respect to
- * concurrent launches from several host threads.
+ * max_launches launches (later ones are not recorded). Inside a stream capture
+ * the pairs become timestamped event nodes of the graph, read after a replay.
+ * Each call creates fresh events (kept for the process, since a captured graph
+ * may still refer to them). Recording adds a few microseconds per event to
+ * the stream, so time a step without tracing when the total matters.
  */
 dflash_status dflash_trace_start(unsigned int kernel_mask, int max_launches);
 

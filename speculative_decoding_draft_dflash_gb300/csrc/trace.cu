@@ -14,7 +14,9 @@ struct TraceState {
   unsigned mask = 0;
   int max_launches = 0;
   int count = 0;
-  std::vector<cudaEvent_t> events;  // 2 per launch
+  int base = 0;                     // first event pair of the current session
+  std::vector<cudaEvent_t> events;  // 2 per launch; a session never reuses an earlier
+                                    // session's events (a captured graph may still hold them)
   std::vector<int> kinds;
 };
 
@@ -32,15 +34,23 @@ LaunchScope::LaunchScope(int kind, cudaStream_t s) : kind_(kind), stream_(s), sl
   if (!t.active || !(t.mask & (1u << kind))) return;
   std::lock_guard<std::mutex> lock(t.mu);
   if (!t.active || t.count >= t.max_launches) return;
+  // External: inside a stream capture this becomes a timestamped event node
+  if (cudaEventRecordWithFlags(t.events[2 * (t.base + t.count)], s, cudaEventRecordExternal) !=
+      cudaSuccess) {
+    cudaGetLastError();  // tracing must not turn into a launch error
+    return;
+  }
   slot_ = t.count++;
   t.kinds[slot_] = kind;
-  cudaEventRecord(t.events[2 * slot_], s);
 }
 
 LaunchScope::~LaunchScope() {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (slot_ < 0) return;
-  cudaEventRecord(state().events[2 * slot_ + 1], stream_);
+  TraceState& t = state();
+  if (cudaEventRecordWithFlags(t.events[2 * (t.base + slot_) + 1], stream_, cudaEventRecordExternal) !=
+      cudaSuccess)
+    cudaGetLastError();
 }
 
 }  // namespace dflash
@@ -51,12 +61,13 @@ DFLASH_API dflash_status dflash_trace_start(unsigned int kernel_mask, int max_la
   if (max_launches < 0) return DFLASH_ERR_INVALID_ARG;
   TraceState& t = state();
   std::lock_guard<std::mutex> lock(t.mu);
-  while ((int)t.events.size() < 2 * max_launches) {
+  t.base = (int)t.events.size() / 2;
+  while ((int)t.events.size() < 2 * (t.base + max_launches)) {
     cudaEvent_t e;
     if (cudaEventCreate(&e) != cudaSuccess) return DFLASH_ERR_CUDA;
     t.events.push_back(e);
   }
-  if ((int)t.kinds.size() < max_launches) t.kinds.resize(max_launches);
+  t.kinds.assign(max_launches, 0);
   t.mask = kernel_mask;
   t.max_launches = max_launches;
   t.count = 0;
@@ -70,9 +81,10 @@ DFLASH_API dflash_status dflash_trace_stop(int* kinds, float* ms, int capacity, 
   t.active = false;
   if (count) *count = t.count;
   for (int i = 0; i < t.count && i < capacity; ++i) {
-    if (cudaEventSynchronize(t.events[2 * i + 1]) != cudaSuccess) return DFLASH_ERR_CUDA;
+    const int ev = 2 * (t.base + i);
+    if (cudaEventSynchronize(t.events[ev + 1]) != cudaSuccess) return DFLASH_ERR_CUDA;
     float v = 0.f;
-    if (cudaEventElapsedTime(&v, t.events[2 * i], t.events[2 * i + 1]) != cudaSuccess)
+    if (cudaEventElapsedTime(&v, t.events[ev], t.events[ev + 1]) != cudaSuccess)
       return DFLASH_ERR_CUDA;
     if (kinds) kinds[i] = t.kinds[i];
     if (ms) ms[i] = v;
