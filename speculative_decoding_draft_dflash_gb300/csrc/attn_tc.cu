@@ -20,7 +20,8 @@
 //              and S columns 64(w/4)..+63: two threads per row, exchanging the
 //              tile maximum and the row sum through shared memory. P (bf16) is
 //              stored into TMEM and read from there by the PV MMA.
-//   8          TMA: the Q tile of each item (double-buffered) and K tiles;
+//   8          TMA: the Q tile of each item (double-buffered) and K tiles
+//              (three stages for R <= 64);
 //   9          MMA: S_j = Q K_j^T (two TMEM S buffers), O += P_j V_j (P from
 //              TMEM, V read MN-major from shared memory);
 //   10         TMA: V tiles (released later than K, so on their own thread).
@@ -48,11 +49,13 @@ constexpr int kRing = 4;                   // item ring slots
 
 // Shared-memory plan. NARROW (R <= 64): query rows 64-127 of an A tile are
 // padding, so the two Q buffers interleave (each only needs its rows 0-63 to
-// be its own) and V gets a third stage. WIDE (R > 64): plain double buffer.
+// be its own) and K gets a third stage: a K tile must land before its S MMA,
+// which runs two tiles ahead of the PV MMA, so K loads need the longer lead.
+// WIDE (R > 64): plain double buffers.
 template <bool NARROW>
 struct Plan {
-  static constexpr int K_STAGES = 2;
-  static constexpr int V_STAGES = NARROW ? 3 : 2;
+  static constexpr int K_STAGES = NARROW ? 3 : 2;
+  static constexpr int V_STAGES = 2;
   static constexpr uint32_t Q_BYTES = NARROW ? 40960 : 2 * TILE;
   static constexpr uint32_t OFF_K = Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + K_STAGES * TILE;
@@ -226,30 +229,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const int n_soft = 64 * nq;                     // softmax threads
   const bool soft = warp < kSoftmaxWarps && (warp & 3) < nq;
   const uint32_t sbase = ptx::smem_u32(smem);
-  // barriers (8 bytes each)
+  // barriers (8 bytes each): q 2+2, k 3+3, v 3+3, s 2+2, p 1, pv 2, items 4+4, MMA exit 1
   const uint32_t q_full0 = ptx::smem_u32(bars + 0), q_empty0 = ptx::smem_u32(bars + 2);
-  const uint32_t k_full0 = ptx::smem_u32(bars + 4), k_empty0 = ptx::smem_u32(bars + 6);
-  const uint32_t v_full0 = ptx::smem_u32(bars + 8), v_empty0 = ptx::smem_u32(bars + 11);
-  const uint32_t s_full0 = ptx::smem_u32(bars + 14), s_free0 = ptx::smem_u32(bars + 16);
-  const uint32_t p_full = ptx::smem_u32(bars + 18), pv_done0 = ptx::smem_u32(bars + 19);
-  const uint32_t it_full0 = ptx::smem_u32(bars + 21), it_empty0 = ptx::smem_u32(bars + 25);
+  const uint32_t k_full0 = ptx::smem_u32(bars + 4), k_empty0 = ptx::smem_u32(bars + 7);
+  const uint32_t v_full0 = ptx::smem_u32(bars + 10), v_empty0 = ptx::smem_u32(bars + 13);
+  const uint32_t s_full0 = ptx::smem_u32(bars + 16), s_free0 = ptx::smem_u32(bars + 18);
+  const uint32_t p_full = ptx::smem_u32(bars + 20), pv_done0 = ptx::smem_u32(bars + 21);
+  const uint32_t it_full0 = ptx::smem_u32(bars + 23), it_empty0 = ptx::smem_u32(bars + 27);
+  const uint32_t mma_fin = ptx::smem_u32(bars + 31);
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(q_full0 + 8 * i, 1);
       ptx::mbar_init(q_empty0 + 8 * i, 1);
-      ptx::mbar_init(k_full0 + 8 * i, 1);
-      ptx::mbar_init(k_empty0 + 8 * i, 1);
       ptx::mbar_init(s_full0 + 8 * i, 1);
       ptx::mbar_init(s_free0 + 8 * i, n_soft);
       ptx::mbar_init(pv_done0 + 8 * i, 1);
+    }
+    for (int i = 0; i < PL::K_STAGES; ++i) {
+      ptx::mbar_init(k_full0 + 8 * i, 1);
+      ptx::mbar_init(k_empty0 + 8 * i, 1);
     }
     for (int i = 0; i < PL::V_STAGES; ++i) {
       ptx::mbar_init(v_full0 + 8 * i, 1);
       ptx::mbar_init(v_empty0 + 8 * i, 1);
     }
     ptx::mbar_init(p_full, n_soft);
+    ptx::mbar_init(mma_fin, 1);
     for (int i = 0; i < kRing; ++i) {
       ptx::mbar_init(it_full0 + 8 * i, 1);
       ptx::mbar_init(it_empty0 + 8 * i, 2 + n_soft);
@@ -299,8 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const int kvrow = (b * p.n_kv + kvh) * p.capacity;
         const int ntiles = (it.z - it.y + TK - 1) / TK;
         for (int j = 0; j < ntiles; ++j) {
-          const int s = gk & 1, u = gk >> 1;
-          if (gk >= 2 && !ptx::mbar_wait(k_empty0 + 8 * s, (u - 1) & 1, &abort_flag, p.status)) {
+          const int s = gk % PL::K_STAGES, u = gk / PL::K_STAGES;
+          if (gk >= PL::K_STAGES &&
+              !ptx::mbar_wait(k_empty0 + 8 * s, (u - 1) & 1, &abort_flag, p.status)) {
             stop = true;
             break;
           }
@@ -315,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       // nothing of ours may still be landing in shared memory when the CTA exits
       for (int i = nq_loads > 2 ? nq_loads - 2 : 0; i < nq_loads; ++i)
         drain(q_full0 + 8 * (i & 1), (i >> 1) & 1, p.status);
-      for (int g = gk > 2 ? gk - 2 : 0; g < gk; ++g) drain(k_full0 + 8 * (g & 1), (g >> 1) & 1, p.status);
+      for (int g = gk > PL::K_STAGES ? gk - PL::K_STAGES : 0; g < gk; ++g)
+        drain(k_full0 + 8 * (g % PL::K_STAGES), (g / PL::K_STAGES) & 1, p.status);
     }
   } else if (warp == WARP_V) {
     // ---------------------------------------------------- V loads
@@ -355,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, TK);
       constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, 128) | (1u << 16);  // V MN-major
       int gt = 0;
-      bool stop = false;
+      bool stop = false, issued = false;
       for (int n = 0; !stop; ++n) {
         const int slot = n % kRing;
         if (!ptx::mbar_wait(it_full0 + 8 * slot, (n / kRing) & 1, &abort_flag, p.status)) break;
@@ -368,18 +377,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const uint32_t qa = sbase + PL::q_base(qb);
         auto issue_s = [&](int j) -> bool {
           const int g = base + j, s = g & 1, u = g >> 1;
+          const int ks = g % PL::K_STAGES, ku = g / PL::K_STAGES;
           if (g >= 2 && !ptx::mbar_wait(s_free0 + 8 * s, (u - 1) & 1, &abort_flag, p.status))
             return false;
-          if (!ptx::mbar_wait(k_full0 + 8 * s, u & 1, &abort_flag, p.status)) return false;
+          if (!ptx::mbar_wait(k_full0 + 8 * ks, ku & 1, &abort_flag, p.status)) return false;
           ptx::tc_fence_after();
-          const uint32_t ka = sbase + PL::OFF_K + s * TILE;
+          const uint32_t ka = sbase + PL::OFF_K + ks * TILE;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
             ptx::mma_bf16(tmem + TM_S + s * TK, ptx::smem_desc_sw128(qa + off),
                           ptx::smem_desc_sw128(ka + off), idesc_s, kk > 0 ? 1u : 0u);
           }
-          ptx::mma_commit(k_empty0 + 8 * s);
+          issued = true;
+          ptx::mma_commit(k_empty0 + 8 * ks);
           ptx::mma_commit(s_full0 + 8 * s);
           if (j == T - 1) ptx::mma_commit(q_empty0 + 8 * qb);
           return true;
@@ -408,8 +419,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         }
         gt = base + T;
       }
-      // every MMA has finished before TMEM is released
-      for (int g = gt > 2 ? gt - 2 : 0; g < gt; ++g) drain(pv_done0 + 8 * (g & 1), (g >> 1) & 1, p.status);
+      // every MMA issued by this thread (also those of an item cut short by an abort)
+      // has finished before TMEM is released
+      if (issued) {
+        ptx::mma_commit(mma_fin);
+        drain(mma_fin, 0, p.status);
+      }
     }
   } else if (soft) {
     // ---------------------------------------------------- softmax
@@ -714,21 +729,20 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   sp.table_len = a.table_len;
   sp.max_splits = p.max_splits;
   sp.n_sm = n_sm;
+  cudaError_t e;
   {
     LaunchScope ls_(DFLASH_KERNEL_SCHEDULE, s);
     attn_schedule_kernel<<<1, 1024, 0, s>>>(sp);
+    e = cudaGetLastError();
   }
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int max_items = pairs * p.max_splits;
   const int grid = n_sm < max_items ? n_sm : max_items;
   e = narrow ? launch_attn<true>(p, grid, s) : launch_attn<false>(p, grid, s);
   if (e != cudaSuccess) return e;
   const int warps = pairs * R;
-  {
-    LaunchScope ls_(DFLASH_KERNEL_COMBINE, s);
-    attn_combine_kernel<<<(warps + 7) / 8, 256, 0, s>>>(p, splits);
-  }
+  LaunchScope ls_(DFLASH_KERNEL_COMBINE, s);
+  attn_combine_kernel<<<(warps + 7) / 8, 256, 0, s>>>(p, (const int*)splits);
   return cudaGetLastError();
 }
 

@@ -27,6 +27,15 @@ TraceState& state() {
 
 std::atomic<unsigned long long> g_launches{0};
 
+// Inside a stream capture an event must be recorded as an external node to carry a
+// timestamp; outside a capture a plain record does that.
+cudaError_t record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return cudaErrorUnknown;
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal)
+                                             : cudaEventRecord(e, s);
+}
+
 }  // namespace
 
 LaunchScope::LaunchScope(int kind, cudaStream_t s) : kind_(kind), stream_(s), slot_(-1) {
@@ -34,9 +43,7 @@ LaunchScope::LaunchScope(int kind, cudaStream_t s) : kind_(kind), stream_(s), sl
   if (!t.active || !(t.mask & (1u << kind))) return;
   std::lock_guard<std::mutex> lock(t.mu);
   if (!t.active || t.count >= t.max_launches) return;
-  // External: inside a stream capture this becomes a timestamped event node
-  if (cudaEventRecordWithFlags(t.events[2 * (t.base + t.count)], s, cudaEventRecordExternal) !=
-      cudaSuccess) {
+  if (record(t.events[2 * (t.base + t.count)], s) != cudaSuccess) {
     cudaGetLastError();  // tracing must not turn into a launch error
     return;
   }
@@ -48,9 +55,7 @@ LaunchScope::~LaunchScope() {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (slot_ < 0) return;
   TraceState& t = state();
-  if (cudaEventRecordWithFlags(t.events[2 * (t.base + slot_) + 1], stream_, cudaEventRecordExternal) !=
-      cudaSuccess)
-    cudaGetLastError();
+  if (record(t.events[2 * (t.base + slot_) + 1], stream_) != cudaSuccess) cudaGetLastError();
 }
 
 }  // namespace dflash
