@@ -615,8 +615,16 @@ __global__ void attn_combine_kernel(AttnTcParams p, const int* splits) {
   bf16* orow = p.out + ((size_t)(b * p.bs + t) * p.n_h + kvh * p.G + gq) * 128;
   float o[4] = {0.f, 0.f, 0.f, 0.f};
   if (n > 1) {
-    // row maximum and sum over the splits, lane-strided, then the weighted rows
+    // row maximum and sum over the splits, lane-strided, then the weighted rows; the
+    // rows of the first kPre splits are requested before the (max, sum) pairs are read
+    constexpr int kPre = 4;
     const size_t base = (size_t)pr * p.max_splits * p.R + r;
+    const float4* acc = reinterpret_cast<const float4*>(p.part_acc + base * 128) + lane;
+    const size_t acc_stride4 = (size_t)p.R * 32;  // one split, in float4
+    float4 pre[kPre];
+#pragma unroll
+    for (int c = 0; c < kPre; ++c)
+      pre[c] = c < n ? acc[c * acc_stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
     float M = -INFINITY;
     for (int c = lane; c < n; c += 32) M = fmaxf(M, p.part_ml[base + (size_t)c * p.R].x);
     M = warp_max(M);
@@ -626,16 +634,19 @@ __global__ void attn_combine_kernel(AttnTcParams p, const int* splits) {
       if (ml.y > 0.f) L += ptx::ex2(ml.x - M) * ml.y;
     }
     L = warp_sum(L);
-#pragma unroll 4
-    for (int c = 0; c < n; ++c) {
+    auto add = [&](int c, const float4& x) {
       const float2 ml = p.part_ml[base + (size_t)c * p.R];
       const float w = ml.y > 0.f ? ptx::ex2(ml.x - M) : 0.f;
-      const float4 x = reinterpret_cast<const float4*>(p.part_acc + (base + (size_t)c * p.R) * 128)[lane];
       o[0] += w * x.x;
       o[1] += w * x.y;
       o[2] += w * x.z;
       o[3] += w * x.w;
-    }
+    };
+#pragma unroll
+    for (int c = 0; c < kPre; ++c)
+      if (c < n) add(c, pre[c]);
+#pragma unroll 4
+    for (int c = kPre; c < n; ++c) add(c, acc[c * acc_stride4]);
     const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[e] *= inv;

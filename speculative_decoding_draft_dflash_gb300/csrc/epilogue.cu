@@ -64,7 +64,45 @@ __device__ __forceinline__ void store4<bf16>(bf16* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = u;
 }
 
+// Sum of the split-K partials of one row chunk: all loads of two splits are issued
+// before any of them is used, so a row costs one memory round trip per two splits.
+template <int CH>
+__device__ __forceinline__ void sum_splits(const float4* __restrict__ y4, size_t split_stride4,
+                                           int splits, int n4, float4 (&v)[CH]) {
+#pragma unroll
+  for (int k = 0; k < CH; ++k) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < splits; s += 2) {
+    float4 a[CH], b[CH];
+    const bool two = s + 1 < splits;
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+      const int c = threadIdx.x + k * kNormThreads;
+      a[k] = c < n4 ? y4[s * split_stride4 + c] : make_float4(0.f, 0.f, 0.f, 0.f);
+      b[k] = (two && c < n4) ? y4[(s + 1) * split_stride4 + c] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+      v[k].x += a[k].x + b[k].x;
+      v[k].y += a[k].y + b[k].y;
+      v[k].z += a[k].z + b[k].z;
+      v[k].w += a[k].w + b[k].w;
+    }
+  }
+}
+
 template <typename T>
+__device__ __forceinline__ float4 load_gamma4(const T* g) {
+  return make_float4(to_f(g[0]), to_f(g[1]), to_f(g[2]), to_f(g[3]));
+}
+template <>
+__device__ __forceinline__ float4 load_gamma4<bf16>(const bf16* g) {
+  const uint2 u = *reinterpret_cast<const uint2*>(g);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <typename T, int CH>
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_vec_kernel(
     const float* __restrict__ Y, int splits, int M, int N, const T* __restrict__ gamma, float eps,
     T* __restrict__ out) {
@@ -73,34 +111,26 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_vec_kernel(
   const int n4 = N >> 2;
   const size_t split_stride4 = (size_t)M * n4;
   const float4* y4 = reinterpret_cast<const float4*>(Y) + (size_t)row * n4;
-  float4 v[kNormMaxChunks];
+  float4 g[CH];
+#pragma unroll
+  for (int k = 0; k < CH; ++k) {
+    const int c = threadIdx.x + k * kNormThreads;
+    g[k] = c < n4 ? load_gamma4(gamma + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float4 v[CH];
+  sum_splits(y4, split_stride4, splits, n4, v);
   float ss = 0.f;
 #pragma unroll
-  for (int k = 0; k < kNormMaxChunks; ++k) {
-    const int c = threadIdx.x + k * kNormThreads;
-    v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (c < n4) {
-      for (int s = 0; s < splits; ++s) {
-        const float4 a = y4[s * split_stride4 + c];
-        v[k].x += a.x;
-        v[k].y += a.y;
-        v[k].z += a.z;
-        v[k].w += a.w;
-      }
-      ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
-    }
-  }
+  for (int k = 0; k < CH; ++k)
+    ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
   ss = block_sum(ss, red);
   const float r = 1.0f / sqrtf(ss / (float)N + eps);
 #pragma unroll
-  for (int k = 0; k < kNormMaxChunks; ++k) {
+  for (int k = 0; k < CH; ++k) {
     const int c = threadIdx.x + k * kNormThreads;
-    if (c < n4) {
-      const float4 g = make_float4(to_f(gamma[4 * c]), to_f(gamma[4 * c + 1]), to_f(gamma[4 * c + 2]),
-                                   to_f(gamma[4 * c + 3]));
-      store4<T>(out + (size_t)row * N + 4 * c,
-                make_float4(v[k].x * r * g.x, v[k].y * r * g.y, v[k].z * r * g.z, v[k].w * r * g.w));
-    }
+    if (c < n4)
+      store4<T>(out + (size_t)row * N + 4 * c, make_float4(v[k].x * r * g[k].x, v[k].y * r * g[k].y,
+                                                           v[k].z * r * g[k].z, v[k].w * r * g[k].w));
   }
 }
 
@@ -177,24 +207,47 @@ __global__ void head_epilogue_kernel(HeadEpilogue e) {
 }
 
 // bf16, d_h = 128: one warp per (row, head); lane l holds dims 4l .. 4l+3, so the
-// RoPE partner (i + 64) of lanes 0-15 sits in lane l + 16.
+// RoPE partner (i + 64) of lanes 0-15 sits in lane l + 16. The loads that do not
+// depend on the row's sequence (split partials, gamma) are issued first; the
+// sequence is found with one ballot over cu_rows, so the dependent chain is
+// cu_rows -> lens -> RoPE row.
 __global__ void __launch_bounds__(256) head_epilogue_bf16_kernel(HeadEpilogue e) {
   const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int heads = e.n_q + 2 * e.n_kv;
   if (wid >= e.rows * heads) return;
   const int row = wid / heads, head = wid - row * heads;
+  const int kind = head < e.n_q ? 0 : (head < e.n_q + e.n_kv ? 1 : 2);  // Q, K, V
+  // split-K partials of this (row, head): two splits per round trip
+  const size_t split_stride4 = (size_t)e.rows * e.ldY / 4;
+  const float4* y4 = reinterpret_cast<const float4*>(e.Y + (size_t)row * e.ldY + (size_t)head * 128) + lane;
+  float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < e.splits; s += 2) {
+    const float4 a = y4[s * split_stride4];
+    const float4 c = s + 1 < e.splits ? y4[(s + 1) * split_stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    x.x += a.x + c.x;
+    x.y += a.y + c.y;
+    x.z += a.z + c.z;
+    x.w += a.w + c.w;
+  }
+  float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
+  if (kind < 2) {  // gamma has no alignment guarantee beyond its element size
+    const bf16* gp = (const bf16*)(kind == 0 ? e.gamma_q : e.gamma_k) + 4 * lane;
+    g = make_float4(__bfloat162float(gp[0]), __bfloat162float(gp[1]), __bfloat162float(gp[2]),
+                    __bfloat162float(gp[3]));
+  }
   int b, t, n_b;
   if (e.cu_rows) {
-    int lo = 0, hi = e.batch - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (e.cu_rows[mid] <= row) lo = mid; else hi = mid - 1;
+    // b = number of sequences 1..batch-1 that start at or before this row
+    b = 0;
+    for (int base = 1; base < e.batch; base += 32) {
+      const int j = base + lane;
+      b += __popc(__ballot_sync(0xffffffffu, j < e.batch && e.cu_rows[j] <= row));
     }
-    b = lo;
-    t = row - e.cu_rows[b];
-    n_b = e.cu_rows[b + 1] - e.cu_rows[b];
-    if (n_b < 0 || e.cu_rows[b + 1] > e.rows || e.cu_rows[0] != 0 || t < 0 || t >= n_b) {
+    const int r0 = e.cu_rows[b], r1 = e.cu_rows[b + 1];
+    t = row - r0;
+    n_b = r1 - r0;
+    if (n_b < 0 || r1 > e.rows || e.cu_rows[0] != 0 || t < 0 || t >= n_b) {
       if (lane == 0) atomicOr(e.status, DFLASH_DEV_ROWS);
       return;
     }
@@ -211,34 +264,22 @@ __global__ void __launch_bounds__(256) head_epilogue_bf16_kernel(HeadEpilogue e)
     return;
   }
   const int pos = start + t;
-  const size_t split_stride4 = (size_t)e.rows * e.ldY / 4;
-  const float4* y4 = reinterpret_cast<const float4*>(e.Y + (size_t)row * e.ldY + (size_t)head * 128) + lane;
-  float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < e.splits; ++s) {
-    const float4 a = y4[s * split_stride4];
-    x.x += a.x;
-    x.y += a.y;
-    x.z += a.z;
-    x.w += a.w;
-  }
-  const int kind = head < e.n_q ? 0 : (head < e.n_q + e.n_kv ? 1 : 2);  // Q, K, V
   if (kind < 2) {
+    const float2* cs = e.rope + (size_t)pos * 64 + 4 * (lane & 15);  // (cos, sin), dims 4l.. mod 64
+    const float2 c0 = cs[0], c1 = cs[1], c2 = cs[2], c3 = cs[3];
     const float ss = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
     const float r = 1.0f / sqrtf(ss * (1.0f / 128.f) + e.eps);
-    const bf16* g = (const bf16*)(kind == 0 ? e.gamma_q : e.gamma_k) + 4 * lane;
-    x.x *= r * __bfloat162float(g[0]);
-    x.y *= r * __bfloat162float(g[1]);
-    x.z *= r * __bfloat162float(g[2]);
-    x.w *= r * __bfloat162float(g[3]);
+    x.x *= r * g.x;
+    x.y *= r * g.y;
+    x.z *= r * g.z;
+    x.w *= r * g.w;
     // partner values: dims i + 64 for lanes 0-15, i - 64 for lanes 16-31
     float4 o;
     o.x = __shfl_xor_sync(0xffffffffu, x.x, 16);
     o.y = __shfl_xor_sync(0xffffffffu, x.y, 16);
     o.z = __shfl_xor_sync(0xffffffffu, x.z, 16);
     o.w = __shfl_xor_sync(0xffffffffu, x.w, 16);
-    const float2* cs = e.rope + (size_t)pos * 64 + 4 * (lane & 15);
     const float sg = lane < 16 ? -1.f : 1.f;  // rotate_half: [-x2; x1]
-    const float2 c0 = cs[0], c1 = cs[1], c2 = cs[2], c3 = cs[3];
     x.x = x.x * c0.x + sg * o.x * c0.y;
     x.y = x.y * c1.x + sg * o.y * c1.y;
     x.z = x.z * c2.x + sg * o.z * c2.y;
@@ -299,19 +340,34 @@ __global__ void rope_table_kernel(double theta, int d_h, int max_pos, float2* ta
   }
 }
 
+// smallest per-thread chunk count (1, 2, 4 or 8 float4) that covers the row
+template <typename T>
+void launch_norm(int need, int M, cudaStream_t s, const float* Y, int splits, int N, const T* gamma,
+                 float eps, T* out) {
+  if (need <= 1)
+    rmsnorm_rows_vec_kernel<T, 1><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, gamma, eps, out);
+  else if (need <= 2)
+    rmsnorm_rows_vec_kernel<T, 2><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, gamma, eps, out);
+  else if (need <= 4)
+    rmsnorm_rows_vec_kernel<T, 4><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, gamma, eps, out);
+  else
+    rmsnorm_rows_vec_kernel<T, 8><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, gamma, eps, out);
+}
+
 }  // namespace
 
 cudaError_t rmsnorm_rows(int dtype, const float* Y, int splits, int M, int N, const void* gamma,
                          float eps, void* out, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  if (N % 4 == 0 && N <= 4 * kNormThreads * kNormMaxChunks) {
+  // the vector kernel loads gamma 4 elements at a time (8-byte aligned for bf16)
+  if (N % 4 == 0 && N <= 4 * kNormThreads * kNormMaxChunks &&
+      (dtype == DFLASH_F32 || ((uintptr_t)gamma & 7) == 0)) {
+    const int need = (N / 4 + kNormThreads - 1) / kNormThreads;
     LaunchScope ls_(DFLASH_KERNEL_RMSNORM, s);
     if (dtype == DFLASH_F32)
-      rmsnorm_rows_vec_kernel<float><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, (const float*)gamma,
-                                                               eps, (float*)out);
+      launch_norm<float>(need, M, s, Y, splits, N, (const float*)gamma, eps, (float*)out);
     else
-      rmsnorm_rows_vec_kernel<bf16><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, (const bf16*)gamma,
-                                                              eps, (bf16*)out);
+      launch_norm<bf16>(need, M, s, Y, splits, N, (const bf16*)gamma, eps, (bf16*)out);
     return cudaGetLastError();
   }
   if (dtype == DFLASH_F32)
