@@ -126,18 +126,26 @@ class ClockSampler:
 # algorithmic bytes and flops (per launch) for the roofline
 # ---------------------------------------------------------------------------
 
-def attention_bytes(w, starts):
-    """K/V rows read + Q read + output written, per layer launch (bf16)."""
+def attention_bytes(w, starts, window=0):
+    """K/V rows read + Q read + output written, per layer launch (bf16).
+
+    Keys read per sequence: [max(0, start - W + 1), start + bs) with a sliding
+    window W, else [0, start + bs).
+    """
     e = 2
-    ends = starts + w.bs
     rows = 0
-    for s, t in zip(starts, ends):
-        lo = 0
-        rows += t - lo
+    for s in starts:
+        lo = max(0, int(s) - window + 1) if window > 0 else 0
+        rows += int(s) + w.bs - lo
     kv = rows * w.n_kv * w.d_h * 2 * e
     q = w.batch * w.n_h * w.bs * w.d_h * e
     out = w.batch * w.bs * w.n_h * w.d_h * e
     return int(kv + q + out)
+
+
+def mean_attention_bytes(w, starts):
+    """Average over the draft layers (their windows differ in hybrid workloads)."""
+    return int(sum(attention_bytes(w, starts, win) for win in w.windows) / len(w.windows))
 
 
 def measured_traffic(kernel):
@@ -231,13 +239,26 @@ def _json_default(o):
     raise TypeError(f"not JSON serialisable: {type(o)}")
 
 
+def step_bytes(w, starts):
+    """Bytes one draft round touches at least once: KV cache rows read + weights."""
+    e = 4 if w.dtype == "f32" else 2
+    weights = (w.k * w.d * w.d + w.n_layers * w.d * (w.n_h + 2 * w.n_kv) * w.d_h) * e
+    cache = sum(attention_bytes(w, starts, win) for win in w.windows)
+    return weights + cache
+
+
 def config_of(w):
-    return {"workload": w.name, "batch": w.batch, "context": f"U[{w.prefill_lo},{w.prefill_hi}]",
-            "new_context_rows": w.new_ctx, "block_size": w.bs, "draft_layers": w.n_layers,
-            "d": w.d, "n_h": w.n_h, "n_kv": w.n_kv, "d_h": w.d_h, "k_target_layers": w.k,
-            "windows": list(w.windows),
-            "l2": "inputs larger than L2: every step reads the whole KV cache (~0.6 GB) and "
-                  "~0.3 GB of weights, well over the 129 MB L2"}
+    from speculative_decoding_draft_dflash_gb300 import synth
+    starts = synth.prefill_lens(w) + w.new_ctx
+    cfg = {"workload": w.name, "batch": w.batch, "context": f"U[{w.prefill_lo},{w.prefill_hi}]",
+           "new_context_rows": w.new_ctx, "block_size": w.bs, "draft_layers": w.n_layers,
+           "d": w.d, "n_h": w.n_h, "n_kv": w.n_kv, "d_h": w.d_h, "k_target_layers": w.k,
+           "windows": list(w.windows)}
+    mb = step_bytes(w, starts) / 1e6
+    cfg["l2"] = (f"inputs larger than L2: every step reads the KV cache rows and the weights, "
+                 f"{mb:.0f} MB in all, over the 129 MB L2" if mb > 129 else
+                 f"step working set {mb:.0f} MB fits in the 129 MB L2: rates are L2-assisted")
+    return cfg
 
 
 # ---------------------------------------------------------------------------
@@ -331,70 +352,24 @@ def run_ours(args, w):
     # ---- per-kernel durations: the same K steps again, with CUDA event pairs that
     # the library records around each launch on its own stream (captured as event
     # nodes). Kept out of the timed region above: each event node costs microseconds.
-    D.dflash_trace_start(TRACED, 64 * args.steps)
-    if args.no_graph:
-        t_ev0 = torch.cuda.Event(enable_timing=True)
-        t_ev1 = torch.cuda.Event(enable_timing=True)
-        t_ev0.record(stream)
-        run_timed()
-        t_ev1.record(stream)
-    else:
-        gT = capture(args.steps)
-        t_ev0 = torch.cuda.Event(enable_timing=True)
-        t_ev1 = torch.cuda.Event(enable_timing=True)
-        t_ev0.record(stream)
-        gT.replay()
-        t_ev1.record(stream)
-    torch.cuda.synchronize()
-    trace = D.dflash_trace_stop()
-    t_traced = t_ev0.elapsed_time(t_ev1)
-
-    # ---- per-kernel times from the trace (same timed region) ----
-    per = {}
-    for name, ms in trace:
-        per.setdefault(name, []).append(ms)
-    # the gemm kinds in launch order within a step: fc, then per layer (kv, qkv)
-    gemm_names = ["gemm_fc"] + [n for _ in range(w.n_layers) for n in ("gemm_kv", "gemm_qkv")]
-    gemm_times = per.pop("gemm", [])
-    for i, ms in enumerate(gemm_times):
-        per.setdefault(gemm_names[i % len(gemm_names)], []).append(ms)
-    kernels = {k: {"launches": len(v), "avg_us": 1e3 * sum(v) / len(v),
-                   "share_of_step": sum(v) / t_traced} for k, v in per.items() if v}
+    # a layer's projections: one grouped launch (context K/V + block Q/K/V) when
+    # dflash_draft_layer groups them, else a K/V and a Q/K/V launch
+    gemm_names = [["gemm_fc"] + ["gemm_layer"] * w.n_layers,
+                  ["gemm_fc"] + [n for _ in range(w.n_layers) for n in ("gemm_kv", "gemm_qkv")]]
+    kernels, t_traced = traced_kernels(args, D, stream, capture, run_timed, gemm_names)
     pk = peaks()
     starts = L0 + w.new_ctx
-    attn_bytes = attention_bytes(w, starts)
+    attn_bytes = mean_attention_bytes(w, starts)
     M = w.batch * w.new_ctx
     costs = {"gemm_fc": gemm_cost(M, w.k * w.d, w.d),
              "gemm_kv": gemm_cost(M, w.d, 2 * w.n_kv * w.d_h),
              "gemm_qkv": gemm_cost(w.batch * w.bs, w.d, (w.n_h + 2 * w.n_kv) * w.d_h)}
-    ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-
-    def roofline_for(name):
-        k = kernels[name]
-        dur = k["avg_us"] * 1e-6
-        if name == "attention":
-            ach = attn_bytes / dur / 1e9
-            return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
-                    "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": measured_traffic(name),
-                    "algorithmic_bytes_per_launch": attn_bytes,
-                    "frac_of_nominal_8TBs": ach / 8000.0, "peak_source": pk["source"]}
-        if name in costs:
-            fl, by = costs[name]
-            if fl / by > ridge:
-                ach = fl / dur / 1e12
-                return {"kernel": name, "bound": "tensor", "achieved": ach,
-                        "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                        "frac": ach / pk["bf16_tflops_sustained"], "traffic": measured_traffic(name),
-                        "algorithmic_flops_per_launch": fl, "peak_source": pk["source"] + " sustained"}
-            ach = by / dur / 1e9
-            return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
-                    "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": measured_traffic(name),
-                    "algorithmic_bytes_per_launch": by, "peak_source": pk["source"]}
-        return None
-
+    costs["gemm_layer"] = tuple(a + b for a, b in zip(costs["gemm_kv"], costs["gemm_qkv"]))
+    rf = lambda name: roofline_for(name, kernels, costs, attn_bytes, pk)  # noqa: E731
     dominant = max(kernels, key=lambda k: kernels[k]["share_of_step"] * (k in costs or k == "attention"))
-    roofline = roofline_for(dominant)
-    others = {k: roofline_for(k) for k in kernels if k != dominant and (k in costs or k == "attention")}
+    roofline = rf(dominant)
+    others = {k: rf(k) for k in kernels if k != dominant and (k in costs or k == "attention")}
+    prefill = run_prefill_gemms(args, w, dev, stream, D, pk) if w.prefill_inject else None
 
     # ---- end to end: host inputs in, host results out, through the same calls ----
     e2e = run_e2e(args, w, dev, x, stream, D)
@@ -410,6 +385,8 @@ def run_ours(args, w):
                        "steps with CUDA event pairs around each launch (%.3f ms/step with "
                        "the events)" % (t_traced / args.steps)) if not args.no_graph else
                       "eager launches; kernel durations from a second traced pass"}
+    if prefill is not None:
+        line["prefill_gemms"] = prefill
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, total, n, _ = oracle_sample_rate(w, budget_s=12.0)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count(),
@@ -420,6 +397,114 @@ def run_ours(args, w):
         print(json.dumps(line, default=_json_default), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def traced_kernels(args, D, stream, capture, run_timed, gemm_names):
+    """Per-kernel durations from one more pass of the K steps with CUDA event pairs."""
+    import torch
+    D.dflash_trace_start(TRACED, 64 * args.steps)
+    t_ev0 = torch.cuda.Event(enable_timing=True)
+    t_ev1 = torch.cuda.Event(enable_timing=True)
+    if args.no_graph:
+        t_ev0.record(stream)
+        run_timed()
+        t_ev1.record(stream)
+    else:
+        gT = capture(args.steps)
+        t_ev0.record(stream)
+        gT.replay()
+        t_ev1.record(stream)
+    torch.cuda.synchronize()
+    trace = D.dflash_trace_stop()
+    t_traced = t_ev0.elapsed_time(t_ev1)
+    per = {}
+    for name, ms in trace:
+        per.setdefault(name, []).append(ms)
+    # gemm launches in their order within a step; gemm_names is one list of names per
+    # step, or several candidates told apart by the number of launches per step
+    gemm_times = per.pop("gemm", [])
+    if gemm_names and isinstance(gemm_names[0], (list, tuple)):
+        per_step = len(gemm_times) // max(1, args.steps)
+        gemm_names = next((g for g in gemm_names if len(g) == per_step), gemm_names[0])
+    for i, ms in enumerate(gemm_times):
+        per.setdefault(gemm_names[i % len(gemm_names)], []).append(ms)
+    kernels = {k: {"launches": len(v), "avg_us": 1e3 * sum(v) / len(v),
+                   "share_of_step": sum(v) / t_traced} for k, v in per.items() if v}
+    return kernels, t_traced
+
+
+def roofline_for(name, kernels, costs, attn_bytes, pk):
+    k = kernels[name]
+    dur = k["avg_us"] * 1e-6
+    if name == "attention":
+        ach = attn_bytes / dur / 1e9
+        return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": measured_traffic(name),
+                "algorithmic_bytes_per_launch": attn_bytes,
+                "frac_of_nominal_8TBs": ach / 8000.0, "peak_source": pk["source"]}
+    if name in costs:
+        fl, by = costs[name]
+        ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+        if fl / by > ridge:
+            ach = fl / dur / 1e12
+            return {"kernel": name, "bound": "tensor", "achieved": ach,
+                    "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                    "frac": ach / pk["bf16_tflops_sustained"], "frac_of_burst": ach / pk["bf16_tflops"],
+                    "traffic": measured_traffic(name), "algorithmic_flops_per_launch": fl,
+                    "peak_source": pk["source"] + " sustained"}
+        ach = by / dur / 1e9
+        return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": measured_traffic(name),
+                "algorithmic_bytes_per_launch": by, "peak_source": pk["source"]}
+    return None
+
+
+def run_prefill_gemms(args, w, dev, stream, D, pk):
+    """The prefill of a workload whose cache is filled by projection + inject: crop every
+    layer to 0, then project and inject the sum(L0) prefill rows again (the same rows land
+    in the same slots), so the fc and K/V GEMMs run at M = sum(L0). Returns their rooflines."""
+    import torch
+    from speculative_decoding_draft_dflash_gb300 import synth
+    counts = dev.L0
+    M = int(counts.sum())
+    hid = [torch.from_numpy(np.ascontiguousarray(h)).to(device="cuda", dtype=dev.dt)
+           for h in synth.hidden_states(w, 0, counts)]
+    cu = torch.from_numpy(synth.cu_rows(counts).astype(np.int32)).cuda()
+    zero = torch.zeros(w.batch, dtype=torch.int32, device="cuda")
+    C = torch.empty((M, w.d), dtype=dev.dt, device="cuda")
+
+    def pstep():
+        D.dflash_cache_crop(dev.cache, zero, stream)
+        D.dflash_ctx_project(dev.dims, hid, M, dev.W_fc, dev.g_h, C, dev.ws, stream)
+        for l in range(w.n_layers):
+            D.dflash_kv_inject(dev.dims, dev.cache, l, C, cu, M, dev.W_K[l], dev.W_V[l], dev.g_k[l],
+                               dev.rope, dev.table_len, dev.ws, stream)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                pstep()
+        return g
+
+    steps = max(10, min(args.steps, 50))
+    pstep()
+    torch.cuda.synchronize()
+    g1 = capture(1)
+    for _ in range(3):
+        g1.replay()
+    torch.cuda.synchronize()
+    assert D.dflash_status_get(stream) == 0, "device status after the prefill warm-up"
+    pargs = argparse.Namespace(**{**vars(args), "steps": steps})
+    kernels, _ = traced_kernels(pargs, D, stream, capture, lambda: [pstep() for _ in range(steps)],
+                                ["gemm_fc"] + ["gemm_kv"] * w.n_layers)
+    assert D.dflash_status_get(stream) == 0, "device status after the prefill pass"
+    costs = {"gemm_fc": gemm_cost(M, w.k * w.d, w.d), "gemm_kv": gemm_cost(M, w.d, 2 * w.n_kv * w.d_h)}
+    out = {"M": M, "steps": steps}
+    for name in ("gemm_fc", "gemm_kv"):
+        if name in kernels:
+            out[name] = {**roofline_for(name, kernels, costs, 0, pk), "avg_us": kernels[name]["avg_us"]}
+    return out
 
 
 def run_e2e(args, w, dev, x, stream, D):

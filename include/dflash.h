@@ -205,6 +205,27 @@ dflash_status dflash_block_attn(const dflash_dims* dims, const dflash_kv_cache* 
                                 void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * One draft layer in a single call: dflash_kv_inject of the context rows C
+ * followed by dflash_block_attn of the block H, with the same arguments and the
+ * same results, lengths and device errors as those two calls in that order (the
+ * block of sequence b starts after the rows the inject appended for it). This is
+ * the layer's single forward over concat[context; block] of the source guide
+ * (part 2: K/V from the concatenation, Q from the block only; walkthrough Step
+ * 4.2). With bf16 and shapes whose two projections fill the GPU without split-K,
+ * both projections (context K/V and block Q/K/V, with their norm / RoPE / store
+ * epilogues) and the attention work list run in one launch, followed by the
+ * attention and its combine; otherwise it issues the two calls.
+ *   arguments      as dflash_kv_inject (C, cu_rows, M) and dflash_block_attn
+ *   workspace      dflash_workspace_bytes(dims, batch, capacity, max(M, ...))
+ */
+dflash_status dflash_draft_layer(const dflash_dims* dims, const dflash_kv_cache* cache, int layer,
+                                 const void* C, const int32_t* cu_rows, int M, const void* H,
+                                 const void* W_Q, const void* W_K, const void* W_V,
+                                 const void* gamma_q, const void* gamma_k, const float* rope_table,
+                                 int table_len, int sliding_window, float scaling, void* out,
+                                 void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * crop(start) on every layer: lens[l][b] = new_lens[b] for all l. No cache
  * data moves. (DFlash source guide (II), part 4; DFlash KV Injection
  * Walkthrough, Step 7.) A target that is negative or above a layer's current

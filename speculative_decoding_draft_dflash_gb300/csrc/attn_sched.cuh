@@ -1,0 +1,149 @@
+// Work list of the tensor-core block attention, computed by one CTA.
+//
+// For every sequence b the block occupies positions start .. start + bs - 1,
+// start = lens[b] plus the rows a KV inject issued in the same call appended
+// (DFlash KV Injection Walkthrough, Step 7: the cache grows by the new context
+// rows, then the block follows them). The keys a query of the block sees are
+// [lo, start + bs): the whole prefix, or the last W positions under a sliding
+// window of W (the window reading of the hybrid layers). Each (sequence, KV
+// head) pair's key range is cut into items of about equal tile counts; the
+// items are listed largest first, which the attention CTAs then take in order
+// from an atomic counter.
+//
+// The same pass records, per sequence, the block start (read by the attention
+// for the window test) and the cache length after the call, which the combine
+// kernel writes back once the attention has finished with the old lengths.
+#pragma once
+
+#include "dflash_internal.cuh"
+
+namespace dflash {
+namespace sched {
+
+constexpr int kTileKeys = 128;     // keys per attention tile
+constexpr int kItemMinTiles = 4;   // smallest item worth a pipeline ramp
+constexpr int kMaxClass = 64;      // item sizes in tiles are bucketed up to this
+
+struct Params {
+  const int32_t* lens;      // [batch] lengths before the call
+  const int32_t* pre_rows;  // cu_rows [batch + 1] of rows injected in the same call, or null
+  int pre_M;                // row count of that inject
+  int4* items;              // {pair, k_begin, k_end, split (-1 = whole range)}
+  int* n_items;
+  int* next_item;
+  int* splits;              // [pair]: items of the pair (0 = refused sequence)
+  int32_t* qstart;          // [batch]: first position of the block
+  int32_t* lens_new;        // [batch]: length after the call
+  int batch, n_kv, bs, window, capacity, table_len, max_splits, n_sm;
+};
+
+// Rows the inject of the same call appended for sequence b: all of its rows when they
+// fit the cache and the RoPE table (the condition under which the inject advances the
+// length), else none.
+__device__ __forceinline__ int injected_rows(const int32_t* cu_rows, int M, int b, int start,
+                                             int capacity, int table_len) {
+  if (!cu_rows) return 0;
+  const int r0 = cu_rows[b], r1 = cu_rows[b + 1];
+  const int n = r1 - r0;
+  if (n < 0 || r1 > M || cu_rows[0] != 0) return 0;
+  if (start < 0 || start + n > capacity || start + n > table_len) return 0;
+  return n;
+}
+
+struct Range {
+  int start, end, lo;
+  bool ok;  // the block fits the cache and the RoPE table
+};
+
+__device__ __forceinline__ Range seq_range(const Params& p, int b) {
+  Range r;
+  const int l = p.lens[b];
+  r.start = l + injected_rows(p.pre_rows, p.pre_M, b, l, p.capacity, p.table_len);
+  r.end = r.start + p.bs;
+  r.lo = p.window > 0 ? max(0, r.start - p.window + 1) : 0;
+  r.ok = r.start >= 0 && r.end <= p.capacity && r.end <= p.table_len;
+  return r;
+}
+
+__device__ __forceinline__ int cta_sum(int v, int* tmp) {
+  v = __reduce_add_sync(0xffffffffu, v);
+  if ((threadIdx.x & 31) == 0) tmp[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int t = 0;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += tmp[i];
+  __syncthreads();
+  return t;
+}
+
+// Run by every thread of one CTA (blockDim.x a multiple of 32, at least kMaxClass + 1).
+inline __device__ void build(const Params& p) {
+  __shared__ int tmp[32];
+  __shared__ int s_class_base[kMaxClass + 1];
+  __shared__ int s_class_cnt[kMaxClass + 1];
+  const int pairs = p.batch * p.n_kv;
+  // total tiles -> item size: about three items per SM, at least kItemMinTiles tiles,
+  // and never more than max_splits items per range
+  int mine = 0;
+  for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
+    const Range r = seq_range(p, b);
+    if (r.ok) mine += p.n_kv * ((r.end - r.lo + kTileKeys - 1) / kTileKeys);
+    p.qstart[b] = r.start;
+    p.lens_new[b] = r.ok ? r.end : r.start;
+  }
+  const int total_tiles = cta_sum(mine, tmp);
+  int item_tiles = (total_tiles + 3 * p.n_sm - 1) / (3 * p.n_sm);
+  if (item_tiles < kItemMinTiles) item_tiles = kItemMinTiles;
+  if (threadIdx.x <= kMaxClass) s_class_cnt[threadIdx.x] = 0;
+  if (threadIdx.x == 0) *p.next_item = 0;
+  __syncthreads();
+  // A range of t tiles becomes n = ceil(t / item_tiles) items of floor / ceil(t / n) tiles;
+  // count the items of each size
+  for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x) {
+    const Range r = seq_range(p, pr / p.n_kv);
+    int n = 0;
+    if (r.ok) {
+      const int t = (r.end - r.lo + kTileKeys - 1) / kTileKeys;
+      n = (t + item_tiles - 1) / item_tiles;
+      if (n > p.max_splits) n = p.max_splits;
+      const int small = t / n, big_cnt = t - small * n;  // big_cnt items of small + 1 tiles
+      if (big_cnt) atomicAdd(&s_class_cnt[min(small + 1, kMaxClass)], big_cnt);
+      if (n - big_cnt) atomicAdd(&s_class_cnt[min(small, kMaxClass)], n - big_cnt);
+    }
+    p.splits[pr] = n;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int c = kMaxClass; c >= 0; --c) {  // largest items first
+      s_class_base[c] = acc;
+      acc += s_class_cnt[c];
+    }
+    *p.n_items = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x <= kMaxClass) s_class_cnt[threadIdx.x] = 0;
+  __syncthreads();
+  for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x) {
+    const int n = p.splits[pr];
+    if (n == 0) continue;
+    const Range r = seq_range(p, pr / p.n_kv);
+    const int t = (r.end - r.lo + kTileKeys - 1) / kTileKeys;
+    const int small = t / n, big_cnt = t - small * n;
+    int k = r.lo;
+    for (int s = 0; s < n; ++s) {
+      const int tiles = small + (s < big_cnt ? 1 : 0);
+      const int c = min(tiles, kMaxClass);
+      const int slot = s_class_base[c] + atomicAdd(&s_class_cnt[c], 1);
+      const int k1 = min(r.end, k + tiles * kTileKeys);
+      p.items[slot] = make_int4(pr, k, k1, n == 1 ? -1 : s);
+      k = k1;
+    }
+  }
+}
+
+}  // namespace sched
+
+// Work-list buffers and parameters of an attention call (attn_tc.cu).
+sched::Params attn_sched_params(const AttnParams& a);
+
+}  // namespace dflash

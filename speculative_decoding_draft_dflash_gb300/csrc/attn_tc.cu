@@ -31,6 +31,7 @@
 
 #include <mutex>
 
+#include "attn_sched.cuh"
 #include "sm100_ptx.cuh"
 
 namespace dflash {
@@ -44,7 +45,6 @@ constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
 constexpr int WARP_KQ = 8, WARP_MMA = 9, WARP_V = 10;
 constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 384;  // TMEM columns: S[2], O, P[2] (64 each)
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kItemMinTiles = 4;
 constexpr int kRing = 4;                   // item ring slots
 
 // Shared-memory plan. NARROW (R <= 64): query rows 64-127 of an A tile are
@@ -68,7 +68,9 @@ struct AttnTcParams {
   CUtensorMap q;   // [B*n_h*bs][128] bf16, box rows 64 (NARROW) or 128
   CUtensorMap k;   // [B*n_kv*capacity][128] bf16 (this layer)
   CUtensorMap v;
-  const int32_t* lens;
+  const int32_t* qstart;  // [batch]: first position of each block (window test)
+  int32_t* lens;          // [batch]: receives lens_new once the attention is done
+  const int32_t* lens_new;
   bf16* out;
   float* part_acc;       // [pair][max_splits][R][128]
   float2* part_ml;       // [pair][max_splits][R]
@@ -106,107 +108,12 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, ui
       : "memory");
 }
 
-struct Range {
-  int start, end, lo;
-  bool ok;
-};
-
-__device__ __forceinline__ Range seq_range(const int32_t* lens, int b, int bs, int window,
-                                           int capacity, int table_len) {
-  Range r;
-  r.start = lens[b];
-  r.end = r.start + bs;
-  r.lo = window > 0 ? max(0, r.start - window + 1) : 0;
-  r.ok = r.start >= 0 && r.end <= capacity && r.end <= table_len;
-  return r;
-}
-
 // ---------------------------------------------------------------------------
-// scheduler: one CTA
+// work list: one CTA (attn_sched.cuh), unless the projection launch built it
 // ---------------------------------------------------------------------------
-struct SchedParams {
-  const int32_t* lens;
-  int4* items;
-  int* n_items;
-  int* next_item;
-  int* splits;      // [pair]: items of the pair (0 = refused sequence)
-  int batch, n_kv, bs, window, capacity, table_len, max_splits, n_sm;
-};
+static_assert(TK == sched::kTileKeys, "attention tile and work-list tile differ");
 
-constexpr int kMaxClass = 64;  // item sizes in tiles are bucketed up to this
-
-__device__ int block_sum_1024(int v, int* tmp) {
-  v = __reduce_add_sync(0xffffffffu, v);
-  if ((threadIdx.x & 31) == 0) tmp[threadIdx.x >> 5] = v;
-  __syncthreads();
-  int t = 0;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += tmp[i];
-  __syncthreads();
-  return t;
-}
-
-__global__ void __launch_bounds__(1024) attn_schedule_kernel(SchedParams p) {
-  __shared__ int tmp[32];
-  __shared__ int s_class_base[kMaxClass + 1];
-  __shared__ int s_class_cnt[kMaxClass + 1];
-  const int pairs = p.batch * p.n_kv;
-  // total tiles -> item size: about three items per SM, at least kItemMinTiles tiles,
-  // and never more than max_splits items per range
-  int mine = 0;
-  for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
-    const Range r = seq_range(p.lens, b, p.bs, p.window, p.capacity, p.table_len);
-    if (r.ok) mine += p.n_kv * ((r.end - r.lo + TK - 1) / TK);
-  }
-  const int total_tiles = block_sum_1024(mine, tmp);
-  int item_tiles = (total_tiles + 3 * p.n_sm - 1) / (3 * p.n_sm);
-  if (item_tiles < kItemMinTiles) item_tiles = kItemMinTiles;
-  if (threadIdx.x <= kMaxClass) s_class_cnt[threadIdx.x] = 0;
-  if (threadIdx.x == 0) *p.next_item = 0;
-  __syncthreads();
-  // A range of t tiles becomes n = ceil(t / item_tiles) items of floor / ceil(t / n) tiles;
-  // count the items of each size
-  for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x) {
-    const Range r = seq_range(p.lens, pr / p.n_kv, p.bs, p.window, p.capacity, p.table_len);
-    int n = 0;
-    if (r.ok) {
-      const int t = (r.end - r.lo + TK - 1) / TK;
-      n = (t + item_tiles - 1) / item_tiles;
-      if (n > p.max_splits) n = p.max_splits;
-      const int small = t / n, big_cnt = t - small * n;  // big_cnt items of small + 1 tiles
-      if (big_cnt) atomicAdd(&s_class_cnt[min(small + 1, kMaxClass)], big_cnt);
-      if (n - big_cnt) atomicAdd(&s_class_cnt[min(small, kMaxClass)], n - big_cnt);
-    }
-    p.splits[pr] = n;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int c = kMaxClass; c >= 0; --c) {  // largest items first
-      s_class_base[c] = acc;
-      acc += s_class_cnt[c];
-    }
-    *p.n_items = acc;
-  }
-  __syncthreads();
-  if (threadIdx.x <= kMaxClass) s_class_cnt[threadIdx.x] = 0;
-  __syncthreads();
-  for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x) {
-    const int n = p.splits[pr];
-    if (n == 0) continue;
-    const Range r = seq_range(p.lens, pr / p.n_kv, p.bs, p.window, p.capacity, p.table_len);
-    const int t = (r.end - r.lo + TK - 1) / TK;
-    const int small = t / n, big_cnt = t - small * n;
-    int k = r.lo;
-    for (int s = 0; s < n; ++s) {
-      const int tiles = small + (s < big_cnt ? 1 : 0);
-      const int c = min(tiles, kMaxClass);
-      const int slot = s_class_base[c] + atomicAdd(&s_class_cnt[c], 1);
-      const int k1 = min(r.end, k + tiles * TK);
-      p.items[slot] = make_int4(pr, k, k1, n == 1 ? -1 : s);
-      k = k1;
-    }
-  }
-}
+__global__ void __launch_bounds__(1024) attn_schedule_kernel(sched::Params p) { sched::build(p); }
 
 // ---------------------------------------------------------------------------
 // attention
@@ -445,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       if (it.x < 0) break;
       const int b = it.x / p.n_kv, kvh = it.x - b * p.n_kv;
       const int T = (it.z - it.y + TK - 1) / TK;
-      const int qpos = p.lens[b] + t;
+      const int qpos = p.qstart[b] + t;
       float m_ref = -INFINITY, l = 0.f;
       bool alive = true;
       for (int j = 0; j < T && alive; ++j) {
@@ -604,6 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 // combine: one warp per (pair, query row)
 // ---------------------------------------------------------------------------
 __global__ void attn_combine_kernel(AttnTcParams p, const int* splits) {
+  // the attention has read the old lengths: publish the lengths after the call
+  if (blockIdx.x == 0 && p.lens)
+    for (int b = threadIdx.x; b < p.batch; b += blockDim.x) p.lens[b] = p.lens_new[b];
   const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (wid >= p.batch * p.n_kv * p.R) return;
@@ -689,7 +599,32 @@ cudaError_t launch_attn(const AttnTcParams& p, int grid, cudaStream_t s) {
 // bf16 row-major [rows][cols] matrix, box {64, box_rows}, 128-byte swizzle (gemm_tc.cu)
 bool encode_2d_bf16(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows);
 
-int attn_tc_chunk() { return TK * kItemMinTiles; }
+int attn_tc_chunk() { return TK * sched::kItemMinTiles; }
+
+// Work-list buffers inside AttnParams::sched: items [pairs][n_chunks] int4, splits
+// [pairs], 16 counters, qstart [batch], lens_new [batch].
+sched::Params attn_sched_params(const AttnParams& a) {
+  const int pairs = a.batch * a.n_kv;
+  sched::Params sp;
+  sp.lens = a.lens;
+  sp.pre_rows = a.pre_rows;
+  sp.pre_M = a.pre_M;
+  sp.items = (int4*)a.sched;
+  sp.splits = (int*)(sp.items + (size_t)pairs * a.n_chunks);
+  sp.n_items = sp.splits + pairs;
+  sp.next_item = sp.n_items + 1;
+  sp.qstart = sp.n_items + 16;
+  sp.lens_new = sp.qstart + a.batch;
+  sp.batch = a.batch;
+  sp.n_kv = a.n_kv;
+  sp.bs = a.bs;
+  sp.window = a.window;
+  sp.capacity = a.capacity;
+  sp.table_len = a.table_len;
+  sp.max_splits = a.n_chunks;  // ranges are cut into at most this many items
+  sp.n_sm = sm_count();
+  return sp;
+}
 
 cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   if (a.batch <= 0) return cudaSuccess;
@@ -703,17 +638,17 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
       !encode_2d_bf16(&p.v, a.cache_v, (long long)a.batch * a.n_kv * a.capacity, 128, 128))
     return cudaErrorInvalidValue;
   const int pairs = a.batch * a.n_kv;
-  p.max_splits = a.n_chunks;  // ranges are cut into at most this many items
-  int4* items = (int4*)a.sched;
-  int* splits = (int*)(items + (size_t)pairs * p.max_splits);
-  int* ctr = splits + pairs;  // [0] item count, [1] next item
-  p.lens = a.lens;
+  const sched::Params sp = attn_sched_params(a);
+  p.max_splits = sp.max_splits;
+  p.qstart = sp.qstart;
+  p.lens = a.lens_out;
+  p.lens_new = sp.lens_new;
   p.out = (bf16*)a.out;
   p.part_acc = a.part_acc;
   p.part_ml = a.part_ml;
-  p.items = items;
-  p.n_items = ctr;
-  p.next_item = ctr + 1;
+  p.items = sp.items;
+  p.n_items = sp.n_items;
+  p.next_item = sp.next_item;
   p.status = a.status;
   p.batch = a.batch;
   p.n_h = a.n_h;
@@ -725,35 +660,20 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   p.window = a.window;
   p.table_len = a.table_len;
   p.sl2 = a.scaling * 1.4426950408889634f;
-  const int n_sm = sm_count();
-  SchedParams sp;
-  sp.lens = a.lens;
-  sp.items = items;
-  sp.n_items = ctr;
-  sp.next_item = ctr + 1;
-  sp.splits = splits;
-  sp.batch = a.batch;
-  sp.n_kv = a.n_kv;
-  sp.bs = a.bs;
-  sp.window = a.window;
-  sp.capacity = a.capacity;
-  sp.table_len = a.table_len;
-  sp.max_splits = p.max_splits;
-  sp.n_sm = n_sm;
-  cudaError_t e;
-  {
+  cudaError_t e = cudaSuccess;
+  if (!a.sched_ready) {
     LaunchScope ls_(DFLASH_KERNEL_SCHEDULE, s);
     attn_schedule_kernel<<<1, 1024, 0, s>>>(sp);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;
   const int max_items = pairs * p.max_splits;
-  const int grid = n_sm < max_items ? n_sm : max_items;
+  const int grid = sp.n_sm < max_items ? sp.n_sm : max_items;
   e = narrow ? launch_attn<true>(p, grid, s) : launch_attn<false>(p, grid, s);
   if (e != cudaSuccess) return e;
   const int warps = pairs * R;
   LaunchScope ls_(DFLASH_KERNEL_COMBINE, s);
-  attn_combine_kernel<<<(warps + 7) / 8, 256, 0, s>>>(p, (const int*)splits);
+  attn_combine_kernel<<<(warps + 7) / 8, 256, 0, s>>>(p, (const int*)sp.splits);
   return cudaGetLastError();
 }
 

@@ -5,7 +5,7 @@
 // entry point allocates, frees or synchronises (dflash_status_get excepted).
 #include <mutex>
 
-#include "dflash_internal.cuh"
+#include "attn_sched.cuh"
 
 namespace dflash {
 
@@ -131,9 +131,10 @@ BlockScratch carve_block(Carver& cv, const dflash_dims* d, int batch, int capaci
   const size_t part_rows = (size_t)batch * d->n_h * n_chunks * d->block_size;
   s.part_acc = cv.take<float>(part_rows * d->d_h);
   s.part_ml = cv.take<float2>(part_rows);
-  // work items {pair, k_begin, k_end, split}, split count per pair, two counters
+  // work items {pair, k_begin, k_end, split}, split count per pair, counters, and per
+  // sequence the block start and the length after the call
   const size_t pairs = (size_t)batch * d->n_kv;
-  s.sched = cv.take<char>(pairs * n_chunks * 16 + pairs * 4 + 64);
+  s.sched = cv.take<char>(pairs * n_chunks * 16 + pairs * 4 + 64 + (size_t)batch * 8);
   return s;
 }
 
@@ -225,40 +226,22 @@ DFLASH_API dflash_status dflash_ctx_project(const dflash_dims* d, const void* co
   return cuda_status(e);
 }
 
-DFLASH_API dflash_status dflash_kv_inject(const dflash_dims* d, const dflash_kv_cache* c, int layer,
-                                          const void* C, const int32_t* cu_rows, int M,
-                                          const void* W_K, const void* W_V, const void* gamma_k,
-                                          const float* rope, int table_len, void* workspace,
-                                          size_t ws_bytes, cudaStream_t stream) {
-  dflash_status st = check_dims(d);
-  if (st != DFLASH_OK) return st;
-  st = check_cache(c, layer);
-  if (st != DFLASH_OK) return st;
-  if (M < 0 || table_len < 0) return DFLASH_ERR_INVALID_ARG;
-  if (M == 0) return DFLASH_OK;
-  if (!C || !cu_rows || !W_K || !W_V || !gamma_k || !rope || !workspace) return DFLASH_ERR_INVALID_ARG;
-  if (!aligned16(C) || !aligned16(W_K) || !aligned16(W_V) || ((uintptr_t)workspace & 255) ||
-      ((uintptr_t)rope & 7))
-    return DFLASH_ERR_INVALID_ARG;
-  Carver cv(workspace, ws_bytes);
-  InjectScratch s = carve_inject(cv, d, M);
-  if (!cv.ok) return DFLASH_ERR_WORKSPACE;
-  unsigned* status = status_word();
-  if (!status) return DFLASH_ERR_CUDA;
-  const int N = 2 * d->n_kv * d->d_h;
-  const int splits = s.splits;
-  Segments A;
-  A.n = 1;
-  A.kseg = d->d;
-  A.p[0] = C;
-  const size_t layer_elems = (size_t)c->batch * d->n_kv * c->capacity * d->d_h;
-  const size_t es = esize(d);
-  const int32_t* lens = c->lens + (size_t)layer * c->batch;
+namespace {
+
+size_t layer_elems(const dflash_dims* d, const dflash_kv_cache* c) {
+  return (size_t)c->batch * d->n_kv * c->capacity * d->d_h;
+}
+
+// Per-head epilogue of an inject: context rows (grouped by cu_rows) -> K-norm, RoPE at
+// lens[b] + t, cache rows; V rows unchanged.
+HeadEpilogue inject_epilogue(const dflash_dims* d, const dflash_kv_cache* c, int layer,
+                             const int32_t* cu_rows, int M, const void* gamma_k, const float* rope,
+                             int table_len, float* Y, int splits, unsigned* status) {
   HeadEpilogue ep;
-  ep.Y = s.Y;
+  ep.Y = Y;
   ep.splits = splits;
   ep.rows = M;
-  ep.ldY = N;
+  ep.ldY = 2 * d->n_kv * d->d_h;
   ep.n_q = 0;
   ep.n_kv = d->n_kv;
   ep.d_h = d->d_h;
@@ -270,59 +253,25 @@ DFLASH_API dflash_status dflash_kv_inject(const dflash_dims* d, const dflash_kv_
   ep.cu_rows = cu_rows;
   ep.batch = c->batch;
   ep.bs = 0;
-  ep.lens = lens;
+  ep.lens = c->lens + (size_t)layer * c->batch;
   ep.q_out = nullptr;
-  ep.cache_k = (char*)c->k + (size_t)layer * layer_elems * es;
-  ep.cache_v = (char*)c->v + (size_t)layer * layer_elems * es;
+  ep.cache_k = (char*)c->k + (size_t)layer * layer_elems(d, c) * esize(d);
+  ep.cache_v = (char*)c->v + (size_t)layer * layer_elems(d, c) * esize(d);
   ep.capacity = c->capacity;
   ep.status = status;
-  cudaError_t e = project_heads(d, A, M, kv_weights(d, W_K, W_V), ep, status, stream);
-  if (e == cudaSuccess)
-    e = lens_advance(c->lens + (size_t)layer * c->batch, cu_rows, c->batch, 0, M, c->capacity,
-                     table_len, stream);
-  return cuda_status(e);
+  return ep;
 }
 
-DFLASH_API dflash_status dflash_block_attn(const dflash_dims* d, const dflash_kv_cache* c,
-                                           int layer, const void* H, const void* W_Q,
-                                           const void* W_K, const void* W_V, const void* gamma_q,
-                                           const void* gamma_k, const float* rope, int table_len,
-                                           int window, float scaling, void* out, void* workspace,
-                                           size_t ws_bytes, cudaStream_t stream) {
-  dflash_status st = check_dims(d);
-  if (st != DFLASH_OK) return st;
-  st = check_cache(c, layer);
-  if (st != DFLASH_OK) return st;
-  if (table_len < 0 || window < 0) return DFLASH_ERR_INVALID_ARG;
-  if (window > 0 && window < d->block_size) return DFLASH_ERR_INVALID_ARG;
-  if (!H || !W_Q || !W_K || !W_V || !gamma_q || !gamma_k || !rope || !out || !workspace)
-    return DFLASH_ERR_INVALID_ARG;
-  if (!aligned16(H) || !aligned16(W_Q) || !aligned16(W_K) || !aligned16(W_V) || !aligned16(out) ||
-      ((uintptr_t)workspace & 255) || ((uintptr_t)rope & 7))
-    return DFLASH_ERR_INVALID_ARG;
-  Carver cv(workspace, ws_bytes);
-  BlockScratch s = carve_block(cv, d, c->batch, c->capacity, window);
-  if (!cv.ok) return DFLASH_ERR_WORKSPACE;
-  unsigned* status = status_word();
-  if (!status) return DFLASH_ERR_CUDA;
-  const int rows = c->batch * d->block_size;
-  const int nq = d->n_h * d->d_h, nkv = d->n_kv * d->d_h;
-  const int N = nq + 2 * nkv;
-  const int splits = s.splits;
-  Segments A;
-  A.n = 1;
-  A.kseg = d->d;
-  A.p[0] = H;
-  const size_t layer_elems = (size_t)c->batch * d->n_kv * c->capacity * d->d_h;
-  const size_t es = esize(d);
-  void* ck = (char*)c->k + (size_t)layer * layer_elems * es;
-  void* cvv = (char*)c->v + (size_t)layer * layer_elems * es;
-  int32_t* lens = c->lens + (size_t)layer * c->batch;
+// Per-head epilogue of a block: Q and K norms, RoPE at the block positions, Q to q_out,
+// K/V to the block's cache rows.
+HeadEpilogue block_epilogue(const dflash_dims* d, const dflash_kv_cache* c, int layer,
+                            const void* gamma_q, const void* gamma_k, const float* rope,
+                            int table_len, void* q_out, float* Y, int splits, unsigned* status) {
   HeadEpilogue ep;
-  ep.Y = s.Y;
+  ep.Y = Y;
   ep.splits = splits;
-  ep.rows = rows;
-  ep.ldY = N;
+  ep.rows = c->batch * d->block_size;
+  ep.ldY = (d->n_h + 2 * d->n_kv) * d->d_h;
   ep.n_q = d->n_h;
   ep.n_kv = d->n_kv;
   ep.d_h = d->d_h;
@@ -334,18 +283,23 @@ DFLASH_API dflash_status dflash_block_attn(const dflash_dims* d, const dflash_kv
   ep.cu_rows = nullptr;
   ep.batch = c->batch;
   ep.bs = d->block_size;
-  ep.lens = lens;
-  ep.q_out = s.q;
-  ep.cache_k = ck;
-  ep.cache_v = cvv;
+  ep.lens = c->lens + (size_t)layer * c->batch;
+  ep.q_out = q_out;
+  ep.cache_k = (char*)c->k + (size_t)layer * layer_elems(d, c) * esize(d);
+  ep.cache_v = (char*)c->v + (size_t)layer * layer_elems(d, c) * esize(d);
   ep.capacity = c->capacity;
   ep.status = status;
-  cudaError_t e = project_heads(d, A, rows, qkv_weights(d, W_Q, W_K, W_V), ep, status, stream);
+  return ep;
+}
+
+AttnParams block_attention(const dflash_dims* d, const dflash_kv_cache* c, int layer,
+                           const BlockScratch& s, int window, float scaling, int table_len,
+                           void* out, unsigned* status) {
   AttnParams p;
   p.q = s.q;
-  p.cache_k = ck;
-  p.cache_v = cvv;
-  p.lens = lens;
+  p.cache_k = (char*)c->k + (size_t)layer * layer_elems(d, c) * esize(d);
+  p.cache_v = (char*)c->v + (size_t)layer * layer_elems(d, c) * esize(d);
+  p.lens = c->lens + (size_t)layer * c->batch;
   p.out = out;
   p.part_acc = s.part_acc;
   p.part_ml = s.part_ml;
@@ -361,10 +315,154 @@ DFLASH_API dflash_status dflash_block_attn(const dflash_dims* d, const dflash_kv
   attn_chunks(d, c->capacity, window, &p.chunk, &p.n_chunks);
   p.table_len = table_len;
   p.scaling = scaling > 0.f ? scaling : 1.0f / sqrtf((float)d->d_h);
+  p.pre_rows = nullptr;
+  p.pre_M = 0;
+  p.lens_out = nullptr;
+  p.sched_ready = false;
+  return p;
+}
+
+dflash_status check_inject(const dflash_dims* d, const dflash_kv_cache* c, int layer, const void* C,
+                           const int32_t* cu_rows, int M, const void* W_K, const void* W_V,
+                           const void* gamma_k, const float* rope, int table_len,
+                           const void* workspace) {
+  dflash_status st = check_dims(d);
+  if (st != DFLASH_OK) return st;
+  st = check_cache(c, layer);
+  if (st != DFLASH_OK) return st;
+  if (M < 0 || table_len < 0) return DFLASH_ERR_INVALID_ARG;
+  if (M == 0) return DFLASH_OK;
+  if (!C || !cu_rows || !W_K || !W_V || !gamma_k || !rope || !workspace) return DFLASH_ERR_INVALID_ARG;
+  if (!aligned16(C) || !aligned16(W_K) || !aligned16(W_V) || ((uintptr_t)workspace & 255) ||
+      ((uintptr_t)rope & 7))
+    return DFLASH_ERR_INVALID_ARG;
+  return DFLASH_OK;
+}
+
+dflash_status check_block(const dflash_dims* d, const dflash_kv_cache* c, int layer, const void* H,
+                          const void* W_Q, const void* W_K, const void* W_V, const void* gamma_q,
+                          const void* gamma_k, const float* rope, int table_len, int window,
+                          const void* out, const void* workspace) {
+  dflash_status st = check_dims(d);
+  if (st != DFLASH_OK) return st;
+  st = check_cache(c, layer);
+  if (st != DFLASH_OK) return st;
+  if (table_len < 0 || window < 0) return DFLASH_ERR_INVALID_ARG;
+  if (window > 0 && window < d->block_size) return DFLASH_ERR_INVALID_ARG;
+  if (!H || !W_Q || !W_K || !W_V || !gamma_q || !gamma_k || !rope || !out || !workspace)
+    return DFLASH_ERR_INVALID_ARG;
+  if (!aligned16(H) || !aligned16(W_Q) || !aligned16(W_K) || !aligned16(W_V) || !aligned16(out) ||
+      ((uintptr_t)workspace & 255) || ((uintptr_t)rope & 7))
+    return DFLASH_ERR_INVALID_ARG;
+  return DFLASH_OK;
+}
+
+Segments one_segment(const dflash_dims* d, const void* X) {
+  Segments A;
+  A.n = 1;
+  A.kseg = d->d;
+  A.p[0] = X;
+  return A;
+}
+
+}  // namespace
+
+DFLASH_API dflash_status dflash_kv_inject(const dflash_dims* d, const dflash_kv_cache* c, int layer,
+                                          const void* C, const int32_t* cu_rows, int M,
+                                          const void* W_K, const void* W_V, const void* gamma_k,
+                                          const float* rope, int table_len, void* workspace,
+                                          size_t ws_bytes, cudaStream_t stream) {
+  dflash_status st = check_inject(d, c, layer, C, cu_rows, M, W_K, W_V, gamma_k, rope, table_len,
+                                  workspace);
+  if (st != DFLASH_OK || M == 0) return st;
+  Carver cv(workspace, ws_bytes);
+  InjectScratch s = carve_inject(cv, d, M);
+  if (!cv.ok) return DFLASH_ERR_WORKSPACE;
+  unsigned* status = status_word();
+  if (!status) return DFLASH_ERR_CUDA;
+  const HeadEpilogue ep = inject_epilogue(d, c, layer, cu_rows, M, gamma_k, rope, table_len, s.Y,
+                                          s.splits, status);
+  cudaError_t e = project_heads(d, one_segment(d, C), M, kv_weights(d, W_K, W_V), ep, status, stream);
+  if (e == cudaSuccess)
+    e = lens_advance(c->lens + (size_t)layer * c->batch, cu_rows, c->batch, 0, M, c->capacity,
+                     table_len, stream);
+  return cuda_status(e);
+}
+
+DFLASH_API dflash_status dflash_block_attn(const dflash_dims* d, const dflash_kv_cache* c,
+                                           int layer, const void* H, const void* W_Q,
+                                           const void* W_K, const void* W_V, const void* gamma_q,
+                                           const void* gamma_k, const float* rope, int table_len,
+                                           int window, float scaling, void* out, void* workspace,
+                                           size_t ws_bytes, cudaStream_t stream) {
+  dflash_status st = check_block(d, c, layer, H, W_Q, W_K, W_V, gamma_q, gamma_k, rope, table_len,
+                                 window, out, workspace);
+  if (st != DFLASH_OK) return st;
+  Carver cv(workspace, ws_bytes);
+  BlockScratch s = carve_block(cv, d, c->batch, c->capacity, window);
+  if (!cv.ok) return DFLASH_ERR_WORKSPACE;
+  unsigned* status = status_word();
+  if (!status) return DFLASH_ERR_CUDA;
+  const int rows = c->batch * d->block_size;
+  const HeadEpilogue ep = block_epilogue(d, c, layer, gamma_q, gamma_k, rope, table_len, s.q, s.Y,
+                                         s.splits, status);
+  cudaError_t e = project_heads(d, one_segment(d, H), rows, qkv_weights(d, W_Q, W_K, W_V), ep,
+                                status, stream);
+  AttnParams p = block_attention(d, c, layer, s, window, scaling, table_len, out, status);
+  // the tensor-core attention's combine kernel publishes the new lengths itself
+  const bool tc_attn = d->dtype != DFLASH_F32;
+  p.lens_out = tc_attn ? c->lens + (size_t)layer * c->batch : nullptr;
   if (e == cudaSuccess)
     e = attention(d->dtype, p, stream);
+  if (e == cudaSuccess && !tc_attn)
+    e = lens_advance(c->lens + (size_t)layer * c->batch, nullptr, c->batch, d->block_size, rows,
+                     c->capacity, table_len, stream);
+  return cuda_status(e);
+}
+
+DFLASH_API dflash_status dflash_draft_layer(const dflash_dims* d, const dflash_kv_cache* c,
+                                            int layer, const void* C, const int32_t* cu_rows, int M,
+                                            const void* H, const void* W_Q, const void* W_K,
+                                            const void* W_V, const void* gamma_q,
+                                            const void* gamma_k, const float* rope, int table_len,
+                                            int window, float scaling, void* out, void* workspace,
+                                            size_t ws_bytes, cudaStream_t stream) {
+  dflash_status st = check_inject(d, c, layer, C, cu_rows, M, W_K, W_V, gamma_k, rope, table_len,
+                                  workspace);
+  if (st != DFLASH_OK) return st;
+  st = check_block(d, c, layer, H, W_Q, W_K, W_V, gamma_q, gamma_k, rope, table_len, window, out,
+                   workspace);
+  if (st != DFLASH_OK) return st;
+  const int rows = c->batch * d->block_size;
+  const Weights Wkv = kv_weights(d, W_K, W_V), Wqkv = qkv_weights(d, W_Q, W_K, W_V);
+  if (d->dtype != DFLASH_BF16 || M == 0 || !gemm_tc_layer_ok(M, Wkv, rows, Wqkv, d->d)) {
+    // the same work as two calls
+    st = dflash_kv_inject(d, c, layer, C, cu_rows, M, W_K, W_V, gamma_k, rope, table_len,
+                          workspace, ws_bytes, stream);
+    if (st != DFLASH_OK) return st;
+    return dflash_block_attn(d, c, layer, H, W_Q, W_K, W_V, gamma_q, gamma_k, rope, table_len,
+                             window, scaling, out, workspace, ws_bytes, stream);
+  }
+  Carver cv(workspace, ws_bytes);
+  BlockScratch s = carve_block(cv, d, c->batch, c->capacity, window);
+  if (!cv.ok) return DFLASH_ERR_WORKSPACE;
+  unsigned* status = status_word();
+  if (!status) return DFLASH_ERR_CUDA;
+  const HeadEpilogue ep_kv = inject_epilogue(d, c, layer, cu_rows, M, gamma_k, rope, table_len,
+                                             nullptr, 1, status);
+  HeadEpilogue ep_qkv = block_epilogue(d, c, layer, gamma_q, gamma_k, rope, table_len, s.q,
+                                       nullptr, 1, status);
+  ep_qkv.pre_rows = cu_rows;  // the block follows the rows injected here
+  ep_qkv.pre_M = M;
+  AttnParams p = block_attention(d, c, layer, s, window, scaling, table_len, out, status);
+  p.pre_rows = cu_rows;
+  p.pre_M = M;
+  p.lens_out = c->lens + (size_t)layer * c->batch;
+  p.sched_ready = true;
+  const sched::Params sp = attn_sched_params(p);
+  cudaError_t e = gemm_tc_layer(C, M, Wkv, ep_kv, H, rows, Wqkv, ep_qkv, d->d, &sp, status, stream);
   if (e == cudaSuccess)
-    e = lens_advance(lens, nullptr, c->batch, d->block_size, rows, c->capacity, table_len, stream);
+    e = attention(d->dtype, p, stream);
   return cuda_status(e);
 }
 

@@ -128,6 +128,10 @@ struct HeadEpilogue {
   void* cache_v;
   int capacity;
   unsigned* status;
+  // block rows only: rows of an inject in the same call precede the block, so a
+  // sequence's block starts after the rows that inject appended (cu_rows, row count)
+  const int32_t* pre_rows = nullptr;
+  int pre_M = 0;
 };
 cudaError_t head_epilogue(int dtype, const HeadEpilogue& e, cudaStream_t s);
 
@@ -137,6 +141,15 @@ cudaError_t head_epilogue(int dtype, const HeadEpilogue& e, cudaStream_t s);
 bool gemm_tc_heads_ok(int M, const Weights& W, int K);
 cudaError_t gemm_tc_heads(const Segments& A, int M, const Weights& W, const HeadEpilogue& ep,
                           unsigned* status, cudaStream_t s);
+
+// Both projections of one draft layer in a single tcgen05 launch (bf16, d_h = 128):
+// the inject's context K/V and the block's Q/K/V, fused epilogues, plus optionally
+// the attention work list (sched::Params, attn_sched.cuh) from one extra CTA.
+namespace sched { struct Params; }
+bool gemm_tc_layer_ok(int Mc, const Weights& Wkv, int Mb, const Weights& Wqkv, int K);
+cudaError_t gemm_tc_layer(const void* C, int Mc, const Weights& Wkv, const HeadEpilogue& ep_kv,
+                          const void* H, int Mb, const Weights& Wqkv, const HeadEpilogue& ep_qkv,
+                          int K, const sched::Params* sp, unsigned* status, cudaStream_t s);
 
 // Warp-per-(row, head) epilogue for bf16 with d_h = 128 (sums the split-K partials).
 cudaError_t head_epilogue_bf16(const HeadEpilogue& e, cudaStream_t s);
@@ -161,8 +174,13 @@ struct AttnParams {
   void* out;              // [batch][bs][n_h * d_h]
   float* part_acc;        // partial accumulators, per chunk
   float2* part_ml;        // partial (max, sum), per chunk
-  void* sched;            // tensor-core path: work list, split counts and counters
+  void* sched;            // tensor-core path: work list, split counts, counters, lengths
   unsigned* status;       // device status word
+  // tensor-core path only:
+  const int32_t* pre_rows;  // cu_rows of rows injected in the same call (the block follows
+  int pre_M;                // them), or null
+  int32_t* lens_out;        // receives the lengths after the call (block appended), or null
+  bool sched_ready;         // the work list was built by the projection launch
   int batch, n_h, n_kv, d_h, bs, capacity, window, chunk, n_chunks, table_len;
   float scaling;
 };

@@ -8,7 +8,7 @@
 //  - lens_advance / crop_lens: the cache's update() length bump and
 //    crop(start) (source guide part 4; walkthrough Step 7).
 //  - rope_table: cos/sin of p * theta^(-2i/d_h) in double precision.
-#include "dflash_internal.cuh"
+#include "attn_sched.cuh"
 
 namespace dflash {
 namespace {
@@ -160,7 +160,8 @@ __global__ void head_epilogue_kernel(HeadEpilogue e) {
     t = row - b * e.bs;
     n_b = e.bs;
   }
-  const int start = e.lens[b];
+  int start = e.lens[b];
+  start += sched::injected_rows(e.pre_rows, e.pre_M, b, start, e.capacity, e.table_len);
   const int pos = start + t;
   if (start < 0 || start + n_b > e.capacity || start + n_b > e.table_len) {
     if (threadIdx.x == 0 && t == 0 && head == 0)
@@ -256,7 +257,8 @@ __global__ void __launch_bounds__(256) head_epilogue_bf16_kernel(HeadEpilogue e)
     t = row - b * e.bs;
     n_b = e.bs;
   }
-  const int start = e.lens[b];
+  int start = e.lens[b];
+  start += sched::injected_rows(e.pre_rows, e.pre_M, b, start, e.capacity, e.table_len);
   if (start < 0 || start + n_b > e.capacity || start + n_b > e.table_len) {
     if (lane == 0 && t == 0 && head == 0)
       atomicOr(e.status, (start + n_b > e.capacity || start < 0) ? DFLASH_DEV_CAPACITY

@@ -23,8 +23,10 @@
 //                row's cache slot (DFlash KV Injection Walkthrough, Steps
 //                4.1-4.3; DFlash source guide (II), parts 1-4). Shapes that need
 //                split-K use the fp32 store and a separate epilogue kernel.
+#include <cstdlib>
 #include <mutex>
 
+#include "attn_sched.cuh"
 #include "sm100_ptx.cuh"
 
 namespace dflash {
@@ -43,6 +45,18 @@ struct TcGemmParams {
   float* Y;           // fp32 store: [split][M][ldY]
   HeadEpilogue ep;    // heads: norm / RoPE / destination
   unsigned* status;
+  // Grouped launch (heads epilogue, no split-K): grid columns [0, ny0) compute the
+  // problem above, columns [ny0, ny0 + ny1) a second one with one activation segment
+  // (same K), and with sched_cta one more column whose first CTA builds the
+  // attention work list while the tiles run.
+  int ny0, ny1, sched_cta;
+  CUtensorMap a1;
+  CUtensorMap b1[3];
+  int w1_count;
+  int w1_off[4];
+  int M1;
+  HeadEpilogue ep1;
+  sched::Params sp;
 };
 
 template <int BN>
@@ -92,7 +106,8 @@ __device__ __forceinline__ void head_row(const HeadEpilogue& e, int row, int hea
     t = row - b * e.bs;
     n_b = e.bs;
   }
-  const int start = e.lens[b];
+  int start = e.lens[b];
+  start += sched::injected_rows(e.pre_rows, e.pre_M, b, start, e.capacity, e.table_len);
   if (start < 0 || start + n_b > e.capacity || start + n_b > e.table_len) {
     if (t == 0 && head == 0)
       atomicOr(e.status, (start + n_b > e.capacity || start < 0) ? DFLASH_DEV_CAPACITY
@@ -152,8 +167,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
+  // problem of this CTA (grouped launches); whole CTAs branch, before any barrier
+  const int col = (int)blockIdx.y;
+  if (p.sched_cta && col == p.ny0 + p.ny1) {
+    if (blockIdx.x == 0 && blockIdx.z == 0) sched::build(p.sp);
+    return;
+  }
+  const bool second = p.ny1 > 0 && col >= p.ny0;
+  const CUtensorMap* amap = second ? &p.a1 : p.a;
+  const CUtensorMap* bmap = second ? p.b1 : p.b;
+  const int* w_off = second ? p.w1_off : p.w_off;
+  const int w_count = second ? p.w1_count : p.w_count;
+  const int M = second ? p.M1 : p.M;
+  const int kseg_blocks = second ? p.kb_total : p.kseg_blocks;
+  const HeadEpilogue& ep = second ? p.ep1 : p.ep;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+  const int m0 = blockIdx.x * BM, n0 = (second ? col - p.ny0 : col) * BN;
+  if (m0 >= M) return;  // grid.x covers the taller problem
   const int kb0 = blockIdx.z * p.kb_per_split;
   const int nkb = min(p.kb_total, kb0 + p.kb_per_split) - kb0;
   const uint32_t full0 = ptx::smem_u32(bars);
@@ -170,8 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < 8; ++i) ptx::prefetch_tmap(&p.a[i]);
-    for (int i = 0; i < p.w_count; ++i) ptx::prefetch_tmap(&p.b[i]);
+    for (int i = 0; i < (second ? 1 : 8); ++i) ptx::prefetch_tmap(&amap[i]);
+    for (int i = 0; i < w_count; ++i) ptx::prefetch_tmap(&bmap[i]);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), BN);
@@ -183,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   const uint32_t tmem = tmem_slot;
 
   int wi = 0;
-  while (wi + 1 < p.w_count && n0 >= p.w_off[wi + 1]) ++wi;
-  const int nb = n0 - p.w_off[wi];
+  while (wi + 1 < w_count && n0 >= w_off[wi + 1]) ++wi;
+  const int nb = n0 - w_off[wi];
 
   if (warp == 0) {
     if (lane == 0) {
@@ -194,12 +224,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const uint32_t ph = (i / STAGES) & 1;
         if (i >= STAGES && !ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, &abort_flag, p.status)) break;
         const int kb = kb0 + i;
-        const int seg = kb / p.kseg_blocks;
-        const int kx = (kb - seg * p.kseg_blocks) * BK;
+        const int seg = kb / kseg_blocks;
+        const int kx = (kb - seg * kseg_blocks) * BK;
         const uint32_t sa = ptx::smem_u32(smem + (size_t)s * C::STAGE);
         ptx::mbar_arrive_expect_tx(full0 + 8 * s, C::STAGE);
-        ptx::tma_load_2d(sa, &p.a[seg], full0 + 8 * s, kx, m0);
-        ptx::tma_load_2d(sa + C::A_BYTES, &p.b[wi], full0 + 8 * s, kb * BK, nb);
+        ptx::tma_load_2d(sa, &amap[seg], full0 + 8 * s, kx, m0);
+        ptx::tma_load_2d(sa + C::A_BYTES, &bmap[wi], full0 + 8 * s, kb * BK, nb);
         ++issued;
       }
       // no copy of ours may still be landing when the CTA exits
@@ -228,12 +258,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   } else {
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 are this warp's
     const int row = q * 32 + lane;
-    const bool in = (m0 + row) < p.M;
+    const bool in = (m0 + row) < M;
     // warp-uniform: tcgen05.ld below is a .sync.aligned instruction
     const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(done, 0, &abort_flag, p.status));
     ptx::tc_fence_after();
     if (ok && !HEADS) {
-      float* y = p.Y + (size_t)blockIdx.z * p.M * p.ldY + (size_t)(m0 + row) * p.ldY + n0;
+      float* y = p.Y + (size_t)blockIdx.z * M * p.ldY + (size_t)(m0 + row) * p.ldY + n0;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -262,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(r[j]);
         }
-        if (in) head_row(p.ep, m0 + row, n0 / 128 + hd, x);
+        if (in) head_row(ep, m0 + row, n0 / 128 + hd, x);
       }
     }
   }
@@ -414,6 +444,69 @@ cudaError_t gemm_tc_heads(const Segments& A, int M, const Weights& W, const Head
   p.status = status;
   dim3 grid((M + BM - 1) / BM, N / pl.bn, 1);
   return pl.bn == 256 ? launch<256, true>(p, grid, s) : launch<128, true>(p, grid, s);
+}
+
+// Both projections of a draft layer in one launch: the context rows' K/V (inject) and
+// the block's Q/K/V, each with the fused per-head epilogue, plus (sp != null) the
+// attention work list from an extra CTA. Worth it when the two tile sets together fill
+// a good part of the GPU without split-K; gemm_tc_layer_ok decides.
+namespace {
+int layer_bn(int Mc, const Weights& Wkv, int Mb, const Weights& Wqkv, int K) {
+  if (Mc <= 0 || Mb <= 0 || K % BK) return 0;
+  const Plan a = plan(Mc, Wkv, K, true), b = plan(Mb, Wqkv, K, true);
+  const int bn = a.bn < b.bn ? a.bn : b.bn;
+  if (bn < 128) return 0;
+  // DFLASH_FUSED_LAYER=0 never groups, =1 groups whenever the shapes allow (the two are
+  // the same arithmetic); otherwise group when the tiles fill a good part of the GPU
+  const char* env = getenv("DFLASH_FUSED_LAYER");
+  if (env && env[0] == '0') return 0;
+  if (env && env[0] == '1') return bn;
+  const int tiles = ((Mc + BM - 1) / BM) * (Wkv.total() / bn) + ((Mb + BM - 1) / BM) * (Wqkv.total() / bn);
+  return tiles >= 64 ? bn : 0;
+}
+}  // namespace
+
+bool gemm_tc_layer_ok(int Mc, const Weights& Wkv, int Mb, const Weights& Wqkv, int K) {
+  return layer_bn(Mc, Wkv, Mb, Wqkv, K) != 0;
+}
+
+cudaError_t gemm_tc_layer(const void* C, int Mc, const Weights& Wkv, const HeadEpilogue& ep_kv,
+                          const void* H, int Mb, const Weights& Wqkv, const HeadEpilogue& ep_qkv,
+                          int K, const sched::Params* sp, unsigned* status, cudaStream_t s) {
+  const int bn = layer_bn(Mc, Wkv, Mb, Wqkv, K);
+  if (!bn || ep_kv.d_h != 128 || ep_qkv.d_h != 128) return cudaErrorInvalidValue;
+  Plan pl;
+  pl.bn = bn;
+  pl.kb_total = K / BK;
+  pl.kb_per_split = pl.kb_total;
+  pl.splits = 1;
+  Segments A;
+  A.n = 1;
+  A.kseg = K;
+  A.p[0] = C;
+  TcGemmParams p;
+  cudaError_t e = fill_common(p, A, Mc, Wkv, pl, K);
+  if (e != cudaSuccess) return e;
+  p.ep = ep_kv;
+  p.status = status;
+  if (!encode_2d_bf16(&p.a1, H, Mb, K, BM)) return cudaErrorInvalidValue;
+  int off = 0;
+  for (int i = 0; i < Wqkv.count; ++i) {
+    if (!encode_2d_bf16(&p.b1[i], Wqkv.p[i], Wqkv.n[i], K, bn)) return cudaErrorInvalidValue;
+    p.w1_off[i] = off;
+    off += Wqkv.n[i];
+  }
+  p.w1_off[Wqkv.count] = off;
+  p.w1_count = Wqkv.count;
+  p.M1 = Mb;
+  p.ep1 = ep_qkv;
+  p.ny0 = Wkv.total() / bn;
+  p.ny1 = Wqkv.total() / bn;
+  p.sched_cta = sp != nullptr;
+  if (sp) p.sp = *sp;
+  const int mt0 = (Mc + BM - 1) / BM, mt1 = (Mb + BM - 1) / BM;
+  dim3 grid(mt0 > mt1 ? mt0 : mt1, p.ny0 + p.ny1 + (sp ? 1 : 0), 1);
+  return bn == 256 ? launch<256, true>(p, grid, s) : launch<128, true>(p, grid, s);
 }
 
 }  // namespace dflash

@@ -58,6 +58,8 @@ def _load():
         "dflash_kv_inject": (c_int, [P, P, c_int, P, P, c_int, P, P, P, P, c_int, P, c_size_t, P]),
         "dflash_block_attn": (c_int, [P, P, c_int, P, P, P, P, P, P, P, c_int, c_int, c_float, P, P,
                                       c_size_t, P]),
+        "dflash_draft_layer": (c_int, [P, P, c_int, P, P, c_int, P, P, P, P, P, P, P, c_int, c_int,
+                                       c_float, P, P, c_size_t, P]),
         "dflash_cache_crop": (c_int, [P, P, P]),
         "dflash_status_get": (c_int, [POINTER(c_uint), P]),
         "dflash_status_string": (ctypes.c_char_p, [c_int]),
@@ -192,6 +194,18 @@ def dflash_block_attn(dims, cache, layer, H, W_Q, W_K, W_V, gamma_q, gamma_k, ro
                                   float(scaling), _ptr(out), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)),
            "dflash_block_attn")
+
+
+def dflash_draft_layer(dims, cache, layer, C, cu_rows, M, H, W_Q, W_K, W_V, gamma_q, gamma_k,
+                       rope_table, table_len, sliding_window, scaling, out, workspace, stream=None):
+    """dflash_kv_inject of C's rows followed by dflash_block_attn of H, as one call."""
+    desc = cache.desc if isinstance(cache, KVCache) else cache
+    _check(_lib.dflash_draft_layer(ctypes.byref(dims), ctypes.byref(desc), int(layer), _ptr(C),
+                                   _ptr(cu_rows), int(M), _ptr(H), _ptr(W_Q), _ptr(W_K), _ptr(W_V),
+                                   _ptr(gamma_q), _ptr(gamma_k), _ptr(rope_table), int(table_len),
+                                   int(sliding_window), float(scaling), _ptr(out), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "dflash_draft_layer")
 
 
 def dflash_cache_crop(cache, new_lens, stream=None):

@@ -25,3 +25,15 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(params=["calls", "layer"])
+def layer_mode(request, monkeypatch):
+    """How a draft layer is issued: two calls (kv_inject, block_attn), or one
+    dflash_draft_layer call with its single grouped projection launch forced on
+    wherever the shapes allow it. Returns the run_round fused_layer flag."""
+    if request.param == "layer":
+        monkeypatch.setenv("DFLASH_FUSED_LAYER", "1")
+        return True
+    monkeypatch.delenv("DFLASH_FUSED_LAYER", raising=False)
+    return False

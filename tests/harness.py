@@ -101,7 +101,7 @@ def oracle_rounds(w: synth.Workload, seqs, rounds=None):
 # device run
 # ---------------------------------------------------------------------------
 
-def device_rounds(w: synth.Workload, seqs, rounds=None, dev=None):
+def device_rounds(w: synth.Workload, seqs, rounds=None, dev=None, fused_layer=True):
     """Runs the same schedule on the device for all sequences; returns host copies for ``seqs``."""
     import torch
     from speculative_decoding_draft_dflash_gb300 import dflash as D
@@ -116,7 +116,7 @@ def device_rounds(w: synth.Workload, seqs, rounds=None, dev=None):
     for rnd in range(1, rounds + 1):
         x = dev.round_inputs(rnd, lens)
         res = {"C": {}, "out": [], "rows": [], "lens_block": [], "before": {}}
-        C = dev.run_round(x, crop=False)
+        C = dev.run_round(x, crop=False, fused_layer=fused_layer)
         torch.cuda.synchronize()
         lens_block = dev.cache.lens.cpu().numpy().copy()
         Ch = C.float().cpu().numpy()

@@ -19,7 +19,7 @@ def _tiny():
         prefill_lo=10, prefill_hi=60, rounds=1, seed=9)
 
 
-def test_capacity_overflow_skips_sequence_and_flags():
+def test_capacity_overflow_skips_sequence_and_flags(layer_mode):
     from speculative_decoding_draft_dflash_gb300 import dflash as D
     w = _tiny()
     L0 = synth.prefill_lens(w)
@@ -27,7 +27,7 @@ def test_capacity_overflow_skips_sequence_and_flags():
     dev = _dev(w, capacity=cap)
     assert D.dflash_status_get() == 0
     x = dev.round_inputs(1, L0)
-    dev.run_round(x, crop=False)
+    dev.run_round(x, crop=False, fused_layer=layer_mode)
     st = D.dflash_status_get()
     assert st & D.DEV_CAPACITY
     lens = dev.cache.lens.cpu().numpy()[0]
@@ -60,14 +60,14 @@ def test_crop_beyond_length_refused():
     assert dev.cache.lens.cpu().numpy()[0].tolist() == [L0[0], 0, 0]
 
 
-def test_rope_table_too_short_flags():
+def test_rope_table_too_short_flags(layer_mode):
     from speculative_decoding_draft_dflash_gb300 import dflash as D
     w = _tiny()
     dev = _dev(w)
     L0 = synth.prefill_lens(w)
     x = dev.round_inputs(1, L0)
     dev.table_len = int(L0.min()) + 8     # positions beyond the table for every sequence
-    dev.run_round(x, crop=False)
+    dev.run_round(x, crop=False, fused_layer=layer_mode)
     assert D.dflash_status_get() & D.DEV_ROPE
     assert dev.cache.lens.cpu().numpy()[0].tolist() == L0.tolist()
 

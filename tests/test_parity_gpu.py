@@ -38,8 +38,8 @@ SMALL = {
 }
 
 
-def _run(w, seqs):
-    dev_res, dev = harness.device_rounds(w, seqs)
+def _run(w, seqs, fused_layer=True):
+    dev_res, dev = harness.device_rounds(w, seqs, fused_layer=fused_layer)
     ora_res = harness.oracle_rounds(w, seqs)
     return harness.compare(w, dev_res, ora_res, seqs)
 
@@ -51,9 +51,9 @@ def test_walkthrough_f32():
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
-def test_small_workloads(name):
+def test_small_workloads(name, layer_mode):
     w = SMALL[name]
-    _run(w, list(range(w.batch)))
+    _run(w, list(range(w.batch)), fused_layer=layer_mode)
 
 
 def _sample(w, n, seed=11):
