@@ -508,50 +508,88 @@ def run_prefill_gemms(args, w, dev, stream, D, pk):
 
 
 def run_e2e(args, w, dev, x, stream, D):
-    """The same steps with inputs copied from pinned host memory and outputs read back each step."""
+    """The same steps through the same calls, with every step's inputs copied in from pinned
+    host memory and its outputs copied back. Two buffer slots: step i+1's inputs upload and
+    step i-1's outputs download on copy streams while step i computes (a step's compute
+    waits for its upload; a slot is refilled only once the step that used it is done and
+    its outputs are out)."""
     import torch
+    from speculative_decoding_draft_dflash_gb300.runner import RoundInputs
+
+    def clone(xx):
+        return RoundInputs(xx.rnd, xx.counts, [t.clone() for t in xx.hidden], xx.cu_rows.clone(),
+                           [t.clone() for t in xx.H], xx.crop_to.clone(), xx.M)
+
+    slots = [x, clone(x)]
+    outs = [dev.out, [torch.empty_like(o) for o in dev.out]]
     hid_h = [t.cpu().pin_memory() for t in x.hidden]
     H_h = [t.cpu().pin_memory() for t in x.H]
     cu_h = x.cu_rows.cpu().pin_memory()
     crop_h = x.crop_to.cpu().pin_memory()
-    out_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in dev.out]
+    out_h = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in dev.out] for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in hid_h + H_h + [cu_h, crop_h])
-    d2h = sum(t.numel() * t.element_size() for t in out_h)
+    d2h = sum(t.numel() * t.element_size() for t in out_h[0])
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    Ev = lambda: torch.cuda.Event()  # noqa: E731
 
-    def step():
-        with torch.cuda.stream(stream):
-            for dst, src in zip(x.hidden, hid_h):
-                dst.copy_(src, non_blocking=True)
-            for dst, src in zip(x.H, H_h):
-                dst.copy_(src, non_blocking=True)
-            x.cu_rows.copy_(cu_h, non_blocking=True)
-            x.crop_to.copy_(crop_h, non_blocking=True)
-            dev.run_round(x, crop=True, stream=stream)
-            for dst, src in zip(out_h, dev.out):
-                dst.copy_(src, non_blocking=True)
+    def steps(n):
+        """n pipelined steps; every cross-stream dependency is an event of this sequence."""
+        fork = Ev()
+        fork.record(stream)
+        s_in.wait_event(fork)
+        s_out.wait_event(fork)
+        ev_in, ev_done, ev_out = [None, None], [None, None], [None, None]
+        for i in range(n):
+            k = i % 2
+            xi, oi = slots[k], outs[k]
+            with torch.cuda.stream(s_in):
+                if ev_done[k] is not None:
+                    s_in.wait_event(ev_done[k])       # step i-2 is done with slot k
+                for dst, src in zip(xi.hidden, hid_h):
+                    dst.copy_(src, non_blocking=True)
+                for dst, src in zip(xi.H, H_h):
+                    dst.copy_(src, non_blocking=True)
+                xi.cu_rows.copy_(cu_h, non_blocking=True)
+                xi.crop_to.copy_(crop_h, non_blocking=True)
+                ev_in[k] = Ev()
+                ev_in[k].record(s_in)
+            stream.wait_event(ev_in[k])
+            if ev_out[k] is not None:
+                stream.wait_event(ev_out[k])          # step i-2's outputs are copied out
+            dev.run_round(xi, crop=True, stream=stream, out=oi)
+            ev_done[k] = Ev()
+            ev_done[k].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[k])
+                for dst, src in zip(out_h[k], oi):
+                    dst.copy_(src, non_blocking=True)
+                ev_out[k] = Ev()
+                ev_out[k].record(s_out)
+        for e in ev_out + ev_in:                       # join the copy streams
+            if e is not None:
+                stream.wait_event(e)
 
-    for _ in range(2):
-        step()
+    with torch.cuda.stream(stream):
+        steps(2)
     torch.cuda.synchronize()
     if args.no_graph:
-        for _ in range(max(3, args.warmup)):
-            step()
+        with torch.cuda.stream(stream):
+            steps(max(3, args.warmup))
     else:
         g1 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g1, stream=stream):
-            step()
+            steps(2)
         for _ in range(max(3, args.warmup)):
             g1.replay()
         gK = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gK, stream=stream):
-            for _ in range(args.steps):
-                step()
+            steps(args.steps)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     if args.no_graph:
-        for _ in range(args.steps):
-            step()
+        with torch.cuda.stream(stream):
+            steps(args.steps)
     else:
         gK.replay()
     ev1.record(stream)
@@ -560,7 +598,9 @@ def run_e2e(args, w, dev, x, stream, D):
     ms = ev0.elapsed_time(ev1) / args.steps
     world = int(os.environ.get("WORLD_SIZE", "1"))
     return {"value": world * w.batch * w.n_layers / (ms * 1e-3), "unit": UNIT,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms,
+            "overlap": "two buffer slots: step i+1's inputs upload and step i-1's outputs "
+                       "download on copy streams while step i computes"}
 
 
 def main():

@@ -112,20 +112,22 @@ class DeviceWorkload:
         return RoundInputs(rnd, counts, hid, cu, H, crop, int(counts.sum()))
 
     # -- one round --------------------------------------------------------------
-    def run_round(self, x: RoundInputs, crop=True, stream=None, fused_layer=True):
+    def run_round(self, x: RoundInputs, crop=True, stream=None, fused_layer=True, out=None):
         """ctx_project -> for each layer (kv_inject, block_attn) -> crop. Results stay on device.
 
         ``fused_layer``: issue each layer's inject + block attention as one
         dflash_draft_layer call (same results) instead of two calls.
+        ``out``: per-layer output buffers (default: this workload's own).
         """
         w = self.w
+        out = self.out if out is None else out
         C = self.C[:x.M]
         D.dflash_ctx_project(self.dims, x.hidden, x.M, self.W_fc, self.g_h, C, self.ws, stream)
         for l in range(w.n_layers):
             if fused_layer:
                 D.dflash_draft_layer(self.dims, self.cache, l, C, x.cu_rows, x.M, x.H[l],
                                      self.W_Q[l], self.W_K[l], self.W_V[l], self.g_q[l], self.g_k[l],
-                                     self.rope, self.table_len, w.windows[l], 0.0, self.out[l],
+                                     self.rope, self.table_len, w.windows[l], 0.0, out[l],
                                      self.ws, stream)
                 continue
             D.dflash_kv_inject(self.dims, self.cache, l, C, x.cu_rows, x.M, self.W_K[l],
@@ -133,7 +135,7 @@ class DeviceWorkload:
                                stream)
             D.dflash_block_attn(self.dims, self.cache, l, x.H[l], self.W_Q[l], self.W_K[l],
                                 self.W_V[l], self.g_q[l], self.g_k[l], self.rope, self.table_len,
-                                w.windows[l], 0.0, self.out[l], self.ws, stream)
+                                w.windows[l], 0.0, out[l], self.ws, stream)
         if crop:
             D.dflash_cache_crop(self.cache, x.crop_to, stream)
         return C
