@@ -265,6 +265,22 @@ def config_of(w):
 # our arm
 # ---------------------------------------------------------------------------
 
+def max_over_ranks(x, world, device="cuda"):
+    """The largest of every rank's value (the slowest replica sets the job's time)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, w, ms_per_step):
+    """Blocks per second per layer over all replicas: each rank drafts its own batch."""
+    return world * w.batch * w.n_layers / (ms_per_step * 1e-3)
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -340,13 +356,9 @@ def run_ours(args, w):
         barrier()
     if args.no_graph:
         launches = D.dflash_launch_count() - launches0
-    t_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        tt = torch.tensor([t_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_ms = float(tt.item())
+    t_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
     ms_per_step = t_ms / args.steps
-    value = world * w.batch * w.n_layers / (ms_per_step * 1e-3)
+    value = whole_job_rate(world, w, ms_per_step)
     assert D.dflash_status_get(stream) == 0, "device status after the timed region"
 
     # ---- per-kernel durations: the same K steps again, with CUDA event pairs that
@@ -584,6 +596,10 @@ def run_e2e(args, w, dev, x, stream, D):
         gK = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gK, stream=stream):
             steps(args.steps)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
@@ -595,9 +611,8 @@ def run_e2e(args, w, dev, x, stream, D):
     ev1.record(stream)
     torch.cuda.synchronize()
     assert D.dflash_status_get(stream) == 0
-    ms = ev0.elapsed_time(ev1) / args.steps
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    return {"value": world * w.batch * w.n_layers / (ms * 1e-3), "unit": UNIT,
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world) / args.steps
+    return {"value": whole_job_rate(world, w, ms), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms,
             "overlap": "two buffer slots: step i+1's inputs upload and step i-1's outputs "
                        "download on copy streams while step i computes"}
