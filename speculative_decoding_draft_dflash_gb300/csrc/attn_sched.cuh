@@ -32,6 +32,8 @@ struct Params {
   int* n_items;
   int* next_item;
   int* splits;              // [pair]: items of the pair (0 = refused sequence)
+  int* merge_list;          // pairs whose rows the combine writes (split or refused),
+  int* n_merge;             //   and their count
   int32_t* qstart;          // [batch]: first position of the block
   int32_t* lens_new;        // [batch]: length after the call
   int batch, n_kv, bs, window, capacity, table_len, max_splits, n_sm;
@@ -75,14 +77,31 @@ __device__ __forceinline__ int cta_sum(int v, int* tmp) {
   return t;
 }
 
+// Three sums at once (tmp: 3 x 32 ints); every thread gets the totals in v.
+__device__ __forceinline__ void cta_sum3(int (&v)[3], int* tmp) {
+  const int w = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
+  for (int i = 0; i < 3; ++i) {
+    const int x = __reduce_add_sync(0xffffffffu, v[i]);
+    if ((threadIdx.x & 31) == 0) tmp[i * 32 + w] = x;
+  }
+  __syncthreads();
+  for (int i = 0; i < 3; ++i) {
+    int t = 0;
+    for (int j = 0; j < nw; ++j) t += tmp[i * 32 + j];
+    v[i] = t;
+  }
+  __syncthreads();
+}
+
 // Run by every thread of one CTA (blockDim.x a multiple of 32, at least kMaxClass + 1).
 inline __device__ void build(const Params& p) {
-  __shared__ int tmp[32];
+  __shared__ int tmp[96];
   __shared__ int s_class_base[kMaxClass + 1];
   __shared__ int s_class_cnt[kMaxClass + 1];
+  __shared__ int s_merge;
   const int pairs = p.batch * p.n_kv;
-  // total tiles -> item size: about three items per SM, at least kItemMinTiles tiles,
-  // and never more than max_splits items per range
+  // total tiles, then the item size (below); at least kItemMinTiles tiles per item and
+  // never more than max_splits items per range
   int mine = 0;
   for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
     const Range r = seq_range(p, b);
@@ -91,10 +110,35 @@ inline __device__ void build(const Params& p) {
     p.lens_new[b] = r.ok ? r.end : r.start;
   }
   const int total_tiles = cta_sum(mine, tmp);
-  int item_tiles = (total_tiles + 3 * p.n_sm - 1) / (3 * p.n_sm);
-  if (item_tiles < kItemMinTiles) item_tiles = kItemMinTiles;
+  // Item size: about F items per SM for F = 2, 3 or 4. Items are taken greedily, largest
+  // first, so the finish is even when the item count fills whole waves of n_sm CTAs; with
+  // equal sequences (one long context, equal windows) a count just past a wave leaves most
+  // SMs idle at the end. Take the smallest F whose count fills its last wave within 5% of
+  // the best of the three.
+  int cand[3], cnt[3] = {0, 0, 0};
+  for (int f = 0; f < 3; ++f)
+    cand[f] = max(kItemMinTiles, (total_tiles + (f + 2) * p.n_sm - 1) / ((f + 2) * p.n_sm));
+  for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
+    const Range r = seq_range(p, b);
+    if (!r.ok) continue;
+    const int t = (r.end - r.lo + kTileKeys - 1) / kTileKeys;
+    for (int f = 0; f < 3; ++f) cnt[f] += p.n_kv * min(p.max_splits, (t + cand[f] - 1) / cand[f]);
+  }
+  cta_sum3(cnt, tmp);
+  float fill[3], best = 0.f;
+  for (int f = 0; f < 3; ++f) {
+    const int waves = (cnt[f] + p.n_sm - 1) / p.n_sm;
+    fill[f] = waves > 0 ? (float)cnt[f] / (float)(waves * p.n_sm) : 1.f;
+    best = fmaxf(best, fill[f]);
+  }
+  int item_tiles = cand[2];
+  for (int f = 2; f >= 0; --f)
+    if (fill[f] >= best - 0.05f) item_tiles = cand[f];
   if (threadIdx.x <= kMaxClass) s_class_cnt[threadIdx.x] = 0;
-  if (threadIdx.x == 0) *p.next_item = 0;
+  if (threadIdx.x == 0) {
+    *p.next_item = 0;
+    s_merge = 0;
+  }
   __syncthreads();
   // A range of t tiles becomes n = ceil(t / item_tiles) items of floor / ceil(t / n) tiles;
   // count the items of each size
@@ -110,6 +154,7 @@ inline __device__ void build(const Params& p) {
       if (n - big_cnt) atomicAdd(&s_class_cnt[min(small, kMaxClass)], n - big_cnt);
     }
     p.splits[pr] = n;
+    if (n != 1) p.merge_list[atomicAdd(&s_merge, 1)] = pr;  // any order: pairs are independent
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -119,6 +164,7 @@ inline __device__ void build(const Params& p) {
       acc += s_class_cnt[c];
     }
     *p.n_items = acc;
+    *p.n_merge = s_merge;
   }
   __syncthreads();
   if (threadIdx.x <= kMaxClass) s_class_cnt[threadIdx.x] = 0;

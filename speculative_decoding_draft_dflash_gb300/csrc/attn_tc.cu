@@ -510,16 +510,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 // ---------------------------------------------------------------------------
 // combine: one warp per (pair, query row)
 // ---------------------------------------------------------------------------
-__global__ void attn_combine_kernel(AttnTcParams p, const int* splits) {
-  // the attention has read the old lengths: publish the lengths after the call
-  if (blockIdx.x == 0 && p.lens)
-    for (int b = threadIdx.x; b < p.batch; b += blockDim.x) p.lens[b] = p.lens_new[b];
-  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (wid >= p.batch * p.n_kv * p.R) return;
-  const int pr = wid / p.R, r = wid - pr * p.R;
+// One query row of a marked pair: log-sum-exp merge of its split partials, or zeros
+// for a refused sequence.
+__device__ __forceinline__ void combine_row(const AttnTcParams& p, const int* splits, int pr,
+                                            int r, int lane) {
   const int n = splits[pr];
-  if (n == 1) return;  // written by the attention kernel
   const int b = pr / p.n_kv, kvh = pr - b * p.n_kv;
   const int gq = r / p.bs, t = r - gq * p.bs;
   bf16* orow = p.out + ((size_t)(b * p.bs + t) * p.n_h + kvh * p.G + gq) * 128;
@@ -568,6 +563,21 @@ __global__ void attn_combine_kernel(AttnTcParams p, const int* splits) {
   reinterpret_cast<uint2*>(orow)[lane] = w;
 }
 
+// Persistent grid; each warp takes (pair, query row) units of the pairs the work list
+// marked (split across items, or refused). Rows of whole-range items were written by
+// the attention kernel.
+__global__ void attn_combine_kernel(AttnTcParams p, const int* splits, const int* merge_list,
+                                    const int* n_merge) {
+  // the attention has read the old lengths: publish the lengths after the call
+  if (blockIdx.x == 0 && p.lens)
+    for (int b = threadIdx.x; b < p.batch; b += blockDim.x) p.lens[b] = p.lens_new[b];
+  const int lane = threadIdx.x & 31;
+  const int units = *n_merge * p.R;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int u = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units; u += warps)
+    combine_row(p, splits, merge_list[u / p.R], u % p.R, lane);
+}
+
 int sm_count() {
   static std::mutex mu;
   static int count[128] = {};
@@ -602,7 +612,7 @@ bool encode_2d_bf16(CUtensorMap* m, const void* base, long long rows, int cols, 
 int attn_tc_chunk() { return TK * sched::kItemMinTiles; }
 
 // Work-list buffers inside AttnParams::sched: items [pairs][n_chunks] int4, splits
-// [pairs], 16 counters, qstart [batch], lens_new [batch].
+// [pairs], 16 counters, qstart [batch], lens_new [batch], merge_list [pairs].
 sched::Params attn_sched_params(const AttnParams& a) {
   const int pairs = a.batch * a.n_kv;
   sched::Params sp;
@@ -613,8 +623,10 @@ sched::Params attn_sched_params(const AttnParams& a) {
   sp.splits = (int*)(sp.items + (size_t)pairs * a.n_chunks);
   sp.n_items = sp.splits + pairs;
   sp.next_item = sp.n_items + 1;
+  sp.n_merge = sp.n_items + 2;
   sp.qstart = sp.n_items + 16;
   sp.lens_new = sp.qstart + a.batch;
+  sp.merge_list = sp.lens_new + a.batch;
   sp.batch = a.batch;
   sp.n_kv = a.n_kv;
   sp.bs = a.bs;
@@ -671,9 +683,12 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   const int grid = sp.n_sm < max_items ? sp.n_sm : max_items;
   e = narrow ? launch_attn<true>(p, grid, s) : launch_attn<false>(p, grid, s);
   if (e != cudaSuccess) return e;
-  const int warps = pairs * R;
+  // marked rows are at most pairs * R; a few waves of warps cover them
+  const int rows = pairs * R;
+  int cgrid = (rows + 7) / 8;
+  if (cgrid > 4 * sp.n_sm) cgrid = 4 * sp.n_sm;
   LaunchScope ls_(DFLASH_KERNEL_COMBINE, s);
-  attn_combine_kernel<<<(warps + 7) / 8, 256, 0, s>>>(p, (const int*)sp.splits);
+  attn_combine_kernel<<<cgrid, 256, 0, s>>>(p, (const int*)sp.splits, sp.merge_list, sp.n_merge);
   return cudaGetLastError();
 }
 
