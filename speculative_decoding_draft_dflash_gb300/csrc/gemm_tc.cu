@@ -8,7 +8,9 @@
 //   warp 1      allocates BN TMEM columns and issues tcgen05.mma (M=128,
 //               N=BN, K=16, four per stage) from one thread; tcgen05.commit
 //               frees each stage ("empty" mbarrier) and finally signals "done";
-//   warps 2-5   epilogue, one thread per tile row (tcgen05.ld of its lanes).
+//   warps 2-5   epilogue: one thread per tile row moves the accumulator from TMEM
+//               (tcgen05.ld of its lanes) into a staging tile in shared memory; then
+//               all six warps store from there with coalesced accesses.
 // The activations arrive as up to eight K-segments (the k target layers'
 // hidden states of the context projection), each with its own tensor map;
 // the weights as up to three matrices stacked along N (W_Q | W_K | W_V).
@@ -17,7 +19,7 @@
 //   fp32 store   the tile (a split-K partial) goes to Y; the context
 //                projection's RMSNorm kernel sums the splits;
 //   heads        (no split-K) whole 128-dim heads per tile (BN = 128 or 256).
-//                The thread owning a row applies the per-head RMSNorm (Q and K
+//                A warp per (row, head) applies the per-head RMSNorm (Q and K
 //                heads), rotates the pair (i, i + 64) at the row's absolute
 //                position and stores the bf16 row into the Q buffer or the
 //                row's cache slot (DFlash KV Injection Walkthrough, Steps
@@ -32,7 +34,10 @@
 namespace dflash {
 namespace {
 
-constexpr int BM = 128, BK = 64, kThreads = 192;
+constexpr int BM = 128, BK = 64;
+// warps 0-5: TMA, MMA, 4 x TMEM -> shared memory; all six store in the epilogue's second
+// phase (more warps there measured no faster)
+constexpr int gemm_threads(bool) { return 192; }
 
 struct TcGemmParams {
   CUtensorMap a[8];   // activation segments [M][kseg], box {64, 128}
@@ -66,6 +71,10 @@ struct Cfg {
   static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
   static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + 256;
+  // epilogue staging tile over the stages: BM rows of BN fp32, padded, then row slots
+  static constexpr int LD = BN + 4;
+  static constexpr uint32_t STG_BYTES = BM * LD * 4;
+  static_assert(STG_BYTES + BM * 16 + BM * 8 <= STAGES * STAGE, "staging tile exceeds the stages");
 };
 
 // Waits without honouring the abort flag (used to drain in-flight work before exit).
@@ -84,86 +93,91 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Per-head epilogue of one 128-wide row x[0..127] of the projection of tile
-// row `row` (global), head `head` of the stacked [Q | K | V] layout.
-__device__ __forceinline__ void head_row(const HeadEpilogue& e, int row, int head, float (&x)[128]) {
-  int b, t, n_b;
+// Sequence, index and position of projection row `row`, or pos = -1 when the row is
+// not written (malformed cu_rows, or the sequence's rows do not fit the cache or the RoPE
+// table). Status bits as the per-head epilogue kernels set them; `first_tile` marks the
+// tile holding head 0, so each refused sequence is flagged once.
+struct RowSlot {
+  int b, t, pos;
+};
+__device__ __forceinline__ RowSlot row_slot(const HeadEpilogue& e, int row, bool first_tile) {
+  RowSlot rs{0, 0, -1};
+  int n_b;
   if (e.cu_rows) {
     int lo = 0, hi = e.batch - 1;
     while (lo < hi) {  // last b with cu_rows[b] <= row
       const int mid = (lo + hi + 1) >> 1;
       if (e.cu_rows[mid] <= row) lo = mid; else hi = mid - 1;
     }
-    b = lo;
-    t = row - e.cu_rows[b];
-    n_b = e.cu_rows[b + 1] - e.cu_rows[b];
-    if (n_b < 0 || e.cu_rows[b + 1] > e.rows || e.cu_rows[0] != 0 || t < 0 || t >= n_b) {
+    rs.b = lo;
+    rs.t = row - e.cu_rows[lo];
+    n_b = e.cu_rows[lo + 1] - e.cu_rows[lo];
+    if (n_b < 0 || e.cu_rows[lo + 1] > e.rows || e.cu_rows[0] != 0 || rs.t < 0 || rs.t >= n_b) {
       atomicOr(e.status, DFLASH_DEV_ROWS);
-      return;
+      return rs;
     }
   } else {
-    b = row / e.bs;
-    t = row - b * e.bs;
+    rs.b = row / e.bs;
+    rs.t = row - rs.b * e.bs;
     n_b = e.bs;
   }
-  int start = e.lens[b];
-  start += sched::injected_rows(e.pre_rows, e.pre_M, b, start, e.capacity, e.table_len);
+  int start = e.lens[rs.b];
+  start += sched::injected_rows(e.pre_rows, e.pre_M, rs.b, start, e.capacity, e.table_len);
   if (start < 0 || start + n_b > e.capacity || start + n_b > e.table_len) {
-    if (t == 0 && head == 0)
+    if (rs.t == 0 && first_tile)
       atomicOr(e.status, (start + n_b > e.capacity || start < 0) ? DFLASH_DEV_CAPACITY
                                                                  : DFLASH_DEV_ROPE);
-    return;
+    return rs;
   }
-  const int pos = start + t;
-  const int kind = head < e.n_q ? 0 : (head < e.n_q + e.n_kv ? 1 : 2);  // Q, K, V
-  if (kind < 2) {
-    float ss0 = 0.f, ss1 = 0.f, ss2 = 0.f, ss3 = 0.f;
-#pragma unroll
-    for (int i = 0; i < 128; i += 4) {
-      ss0 = fmaf(x[i], x[i], ss0);
-      ss1 = fmaf(x[i + 1], x[i + 1], ss1);
-      ss2 = fmaf(x[i + 2], x[i + 2], ss2);
-      ss3 = fmaf(x[i + 3], x[i + 3], ss3);
-    }
-    const float r = 1.0f / sqrtf(((ss0 + ss1) + (ss2 + ss3)) * (1.0f / 128.f) + e.eps);
-    const bf16* g = (const bf16*)(kind == 0 ? e.gamma_q : e.gamma_k);
-    const float2* cs = e.rope + (size_t)pos * 64;
-#pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      const float x0 = x[i] * r * __bfloat162float(g[i]);
-      const float x1 = x[i + 64] * r * __bfloat162float(g[i + 64]);
-      const float2 c = cs[i];
-      x[i] = x0 * c.x - x1 * c.y;  // rotate_half: [-x1, x0]
-      x[i + 64] = x1 * c.x + x0 * c.y;
-    }
-  }
-  bf16* dst;
-  if (kind == 0) {
-    dst = (bf16*)e.q_out + (((size_t)b * e.n_q + head) * e.bs + t) * 128;
-  } else {
-    const int kvh = head - e.n_q - (kind == 2 ? e.n_kv : 0);
-    bf16* base = (bf16*)(kind == 1 ? e.cache_k : e.cache_v);
-    dst = base + (((size_t)b * e.n_kv + kvh) * e.capacity + pos) * 128;
-  }
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    uint4 w;
-    w.x = pack_bf16(x[8 * k + 0], x[8 * k + 1]);
-    w.y = pack_bf16(x[8 * k + 2], x[8 * k + 3]);
-    w.z = pack_bf16(x[8 * k + 4], x[8 * k + 5]);
-    w.w = pack_bf16(x[8 * k + 6], x[8 * k + 7]);
-    d4[k] = w;
-  }
+  rs.pos = start + rs.t;
+  return rs;
+}
+
+// The epilogue parameters of a CTA's problem, copied into registers field by field: each
+// read stays a constant-bank access (a reference chosen at run time between the two
+// parameter structs would turn every later field read into a generic memory load).
+__device__ __forceinline__ HeadEpilogue pick_epilogue(const TcGemmParams& p, bool second) {
+  HeadEpilogue e;
+#define DFLASH_PICK(f) e.f = second ? p.ep1.f : p.ep.f
+  DFLASH_PICK(Y);
+  DFLASH_PICK(splits);
+  DFLASH_PICK(rows);
+  DFLASH_PICK(ldY);
+  DFLASH_PICK(n_q);
+  DFLASH_PICK(n_kv);
+  DFLASH_PICK(d_h);
+  DFLASH_PICK(eps);
+  DFLASH_PICK(gamma_q);
+  DFLASH_PICK(gamma_k);
+  DFLASH_PICK(rope);
+  DFLASH_PICK(table_len);
+  DFLASH_PICK(cu_rows);
+  DFLASH_PICK(batch);
+  DFLASH_PICK(bs);
+  DFLASH_PICK(lens);
+  DFLASH_PICK(q_out);
+  DFLASH_PICK(cache_k);
+  DFLASH_PICK(cache_v);
+  DFLASH_PICK(capacity);
+  DFLASH_PICK(status);
+  DFLASH_PICK(pre_rows);
+  DFLASH_PICK(pre_M);
+#undef DFLASH_PICK
+  return e;
 }
 
 template <int BN, bool HEADS>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcGemmParams p) {
+__global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const __grid_constant__ TcGemmParams p) {
+  constexpr int kThreads = gemm_threads(HEADS);
   using C = Cfg<BN>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + (size_t)STAGES * C::STAGE);
+  constexpr int NH = BN >= 128 ? BN / 128 : 1;                // heads per tile (heads epilogue)
+  float* stg = reinterpret_cast<float*>(smem);                // epilogue only
+  int4* slots = reinterpret_cast<int4*>(smem + C::STG_BYTES);  // epilogue only
+  float* rnorm = reinterpret_cast<float*>(slots + BM);         // epilogue only: [BM][NH]
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -176,11 +190,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   const bool second = p.ny1 > 0 && col >= p.ny0;
   const CUtensorMap* amap = second ? &p.a1 : p.a;
   const CUtensorMap* bmap = second ? p.b1 : p.b;
-  const int* w_off = second ? p.w1_off : p.w_off;
+  int w_off[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w_off[i] = second ? p.w1_off[i] : p.w_off[i];
   const int w_count = second ? p.w1_count : p.w_count;
   const int M = second ? p.M1 : p.M;
   const int kseg_blocks = second ? p.kb_total : p.kseg_blocks;
-  const HeadEpilogue& ep = second ? p.ep1 : p.ep;
+  const HeadEpilogue ep = pick_epilogue(p, second);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * BM, n0 = (second ? col - p.ny0 : col) * BN;
   if (m0 >= M) return;  // grid.x covers the taller problem
@@ -256,43 +272,143 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       drain_wait(done, 0, p.status);  // every MMA has finished before TMEM can be freed
     }
   } else {
+    // phase 1: TMEM -> a staging tile in the pipeline's shared memory (free once every
+    // MMA is done), one row per thread; rows padded by 4 floats so the float4 stores of a
+    // warp spread over all banks. The row's destination is resolved here too.
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 are this warp's
     const int row = q * 32 + lane;
-    const bool in = (m0 + row) < M;
     // warp-uniform: tcgen05.ld below is a .sync.aligned instruction
     const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(done, 0, &abort_flag, p.status));
     ptx::tc_fence_after();
-    if (ok && !HEADS) {
-      float* y = p.Y + (size_t)blockIdx.z * M * p.ldY + (size_t)(m0 + row) * p.ldY + n0;
+    if (ok) {
+      float* srow = stg + row * C::LD;
+      float ss[NH] = {};  // per-head sum of squares of this row (heads: RMSNorm)
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
         ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
         ptx::tmem_ld_wait();
-        if (in) {
-          float4* dst = reinterpret_cast<float4*>(y + c * 32);
+        float4* d = reinterpret_cast<float4*>(srow + c * 32);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        for (int j = 0; j < 8; ++j)
+          d[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                             __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        if (HEADS) {
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            a0 = fmaf(__uint_as_float(r[j]), __uint_as_float(r[j]), a0);
+            a1 = fmaf(__uint_as_float(r[j + 1]), __uint_as_float(r[j + 1]), a1);
+            a2 = fmaf(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 2]), a2);
+            a3 = fmaf(__uint_as_float(r[j + 3]), __uint_as_float(r[j + 3]), a3);
+          }
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+            if (c / 4 == h) ss[h] += (a0 + a1) + (a2 + a3);
         }
       }
+      if (HEADS) {
+        RowSlot rs{0, 0, -1};
+        if (m0 + row < M) rs = row_slot(ep, m0 + row, n0 == 0);
+        slots[row] = make_int4(rs.b, rs.t, rs.pos, 0);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) rnorm[row * NH + h] = 1.0f / sqrtf(ss[h] * (1.0f / 128.f) + ep.eps);
+      }
     }
-    if (ok && HEADS) {
-      // BN / 128 whole heads per tile, one after the other; each thread owns one row.
-      // Every lane joins the tcgen05.ld (warp-collective); only rows < M are stored.
-#pragma unroll 1
-      for (int hd = 0; hd < BN / 128; ++hd) {
-        float x[128];
+  }
+  // phase 2, all warps: coalesced stores from the staging tile
+  ptx::named_sync(1, kThreads);
+  if (!abort_flag) {
+    if (!HEADS) {
+      // fp32 partial rows: one warp per row, lanes along the row
+      float* ybase = p.Y + (size_t)blockIdx.z * M * p.ldY + n0;
+      for (int r = warp; r < BM && m0 + r < M; r += kThreads / 32) {
+        const float4* src = reinterpret_cast<const float4*>(stg + r * C::LD);
+        float4* dst = reinterpret_cast<float4*>(ybase + (size_t)(m0 + r) * p.ldY);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hd * 128 + c * 32), r);
-          ptx::tmem_ld_wait();
+        for (int j = lane; j < BN / 4; j += 32) dst[j] = src[j];
+      }
+    } else {
+      // one warp per (row, head): lane l holds dims 4l .. 4l+3 and reads its RoPE partner
+      // dims (i +- 64, lane l ^ 16) from the staging tile as well; the norm scale came with
+      // the row. Rows go in batches of RB per warp, all loads of a batch issued first.
+      constexpr int RB = 4;  // rows per batch (two batches of loads in registers)
+      const int lp = lane ^ 16;
+      float gq[4], gk[4], gqp[4], gkp[4];  // gamma of this lane's dims and of its partner's
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(r[j]);
+      for (int i = 0; i < 4; ++i) {
+        gq[i] = ep.gamma_q ? __bfloat162float(((const bf16*)ep.gamma_q)[4 * lane + i]) : 1.f;
+        gqp[i] = ep.gamma_q ? __bfloat162float(((const bf16*)ep.gamma_q)[4 * lp + i]) : 1.f;
+        gk[i] = ep.gamma_k ? __bfloat162float(((const bf16*)ep.gamma_k)[4 * lane + i]) : 1.f;
+        gkp[i] = ep.gamma_k ? __bfloat162float(((const bf16*)ep.gamma_k)[4 * lp + i]) : 1.f;
+      }
+      const float sg = lane < 16 ? -1.f : 1.f;  // rotate_half: [-x2; x1]
+      // row slots and RoPE rows of batch k + 1 are loaded while batch k computes
+      auto fetch = [&](int r0, int4 (&rs)[RB], float2 (&cs)[RB][4]) {
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+          const int r = r0 + i;
+          rs[i] = r < BM ? slots[r] : make_int4(0, 0, -1, 0);
+          if (m0 + r >= M) rs[i].z = -1;
         }
-        if (in) head_row(ep, m0 + row, n0 / 128 + hd, x);
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {  // rows that are not written read position 0
+          const float2* c = ep.rope + (size_t)max(rs[i].z, 0) * 64 + 4 * (lane & 15);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) cs[i][j] = c[j];
+        }
+      };
+      constexpr int kStride = (kThreads / 32) * RB;
+      int4 rs[RB];
+      float2 cs[RB][4];
+      if (warp * RB < BM) fetch(warp * RB, rs, cs);
+      for (int r0 = warp * RB; r0 < BM; r0 += kStride) {
+        int4 rs_n[RB];
+        float2 cs_n[RB][4];
+        if (r0 + kStride < BM) fetch(r0 + kStride, rs_n, cs_n);
+        // branch-free over the batch (the units interleave); only the stores are predicated
+        float4 xv[RB][NH], xp[RB][NH];
+#pragma unroll
+        for (int i = 0; i < RB; ++i)
+#pragma unroll
+          for (int hd = 0; hd < NH; ++hd) {
+            const float4* row4 = reinterpret_cast<const float4*>(stg + (r0 + i) * C::LD + hd * 128);
+            xv[i][hd] = row4[lane];
+            xp[i][hd] = row4[lp];
+          }
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+#pragma unroll
+          for (int hd = 0; hd < NH; ++hd) {
+            const int head = n0 / 128 + hd;
+            const int kind = head < ep.n_q ? 0 : (head < ep.n_q + ep.n_kv ? 1 : 2);  // Q, K, V
+            const bool qh = kind == 0, rot = kind < 2;
+            const float rn = rnorm[(r0 + i) * NH + hd];
+            const float4 x = xv[i][hd], o = xp[i][hd];
+            const float x0 = x.x * rn * (qh ? gq[0] : gk[0]), p0 = o.x * rn * (qh ? gqp[0] : gkp[0]);
+            const float x1 = x.y * rn * (qh ? gq[1] : gk[1]), p1 = o.y * rn * (qh ? gqp[1] : gkp[1]);
+            const float x2 = x.z * rn * (qh ? gq[2] : gk[2]), p2 = o.z * rn * (qh ? gqp[2] : gkp[2]);
+            const float x3 = x.w * rn * (qh ? gq[3] : gk[3]), p3 = o.w * rn * (qh ? gqp[3] : gkp[3]);
+            const float y0 = rot ? x0 * cs[i][0].x + sg * p0 * cs[i][0].y : x.x;
+            const float y1 = rot ? x1 * cs[i][1].x + sg * p1 * cs[i][1].y : x.y;
+            const float y2 = rot ? x2 * cs[i][2].x + sg * p2 * cs[i][2].y : x.z;
+            const float y3 = rot ? x3 * cs[i][3].x + sg * p3 * cs[i][3].y : x.w;
+            const int kvh = head - ep.n_q - (kind == 2 ? ep.n_kv : 0);
+            bf16* kvbase = (bf16*)(kind == 1 ? ep.cache_k : ep.cache_v);
+            bf16* dst = qh ? (bf16*)ep.q_out + (((size_t)rs[i].x * ep.n_q + head) * ep.bs + rs[i].y) * 128
+                           : kvbase + (((size_t)rs[i].x * ep.n_kv + kvh) * ep.capacity + rs[i].z) * 128;
+            uint2 w2;
+            w2.x = pack_bf16(y0, y1);
+            w2.y = pack_bf16(y2, y3);
+            if (rs[i].z >= 0) reinterpret_cast<uint2*>(dst)[lane] = w2;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+          rs[i] = rs_n[i];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) cs[i][j] = cs_n[i][j];
+        }
       }
     }
   }
@@ -356,7 +472,7 @@ cudaError_t launch(const TcGemmParams& p, dim3 grid, cudaStream_t s) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   LaunchScope ls_(DFLASH_KERNEL_GEMM, s);
-  gemm_tc_kernel<BN, HEADS><<<grid, kThreads, smem, s>>>(p);
+  gemm_tc_kernel<BN, HEADS><<<grid, gemm_threads(HEADS), smem, s>>>(p);
   return cudaGetLastError();
 }
 
