@@ -382,6 +382,7 @@ def run_ours(args, w):
     roofline = rf(dominant)
     others = {k: rf(k) for k in kernels if k != dominant and (k in costs or k == "attention")}
     prefill = run_prefill_gemms(args, w, dev, stream, D, pk) if w.prefill_inject else None
+    bookkeeping = time_accept(args, w, stream, D)
 
     # ---- end to end: host inputs in, host results out, through the same calls ----
     e2e = run_e2e(args, w, dev, x, stream, D)
@@ -399,6 +400,7 @@ def run_ours(args, w):
                       "eager launches; kernel durations from a second traced pass"}
     if prefill is not None:
         line["prefill_gemms"] = prefill
+    line["bookkeeping"] = bookkeeping
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, total, n, _ = oracle_sample_rate(w, budget_s=12.0)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count(),
@@ -517,6 +519,43 @@ def run_prefill_gemms(args, w, dev, stream, D, pk):
         if name in kernels:
             out[name] = {**roofline_for(name, kernels, costs, 0, pk), "avg_us": kernels[name]["avg_us"]}
     return out
+
+
+def time_accept(args, w, stream, D):
+    """dflash_accept at this batch: one round's acceptance lengths, next inject offsets,
+    next block starts and anchors from seeded draft / posterior tokens (launch-bound)."""
+    import torch
+    rng = np.random.Generator(np.random.PCG64(99))
+    B, bs = w.batch, w.bs
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()  # noqa: E731
+    block = dev(rng.integers(0, 1000, size=(B, bs)))
+    post = dev(rng.integers(0, 1000, size=(B, bs)))
+    ctx = dev(synth_lens(w))
+    outs = [torch.empty(n, dtype=torch.int32, device="cuda") for n in (B, B + 1, B, B)]
+    call = lambda: D.dflash_accept(block, post, ctx, *outs, stream=stream)  # noqa: E731
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                call()
+        return g
+
+    call()
+    torch.cuda.synchronize()
+    n = max(10, min(args.steps, 100))
+    D.dflash_trace_start(["accept"], n + 8)
+    g = capture(n)
+    g.replay()
+    torch.cuda.synchronize()
+    ms = [t for k, t in D.dflash_trace_stop() if k == "accept"]
+    return {"kernel": "accept", "launches": len(ms), "avg_us": 1e3 * sum(ms) / max(1, len(ms)),
+            "batch": B, "block": bs, "bound": "launch"}
+
+
+def synth_lens(w):
+    from speculative_decoding_draft_dflash_gb300 import synth
+    return synth.prefill_lens(w) + w.new_ctx
 
 
 def run_e2e(args, w, dev, x, stream, D):

@@ -236,6 +236,28 @@ dflash_status dflash_cache_crop(const dflash_kv_cache* cache, const int32_t* new
                                 cudaStream_t stream);
 
 /*
+ * Acceptance bookkeeping of a verified round, on the device, for every sequence b
+ * (DFlash KV Injection Walkthrough, Step 6: a = the number of leading i < bs - 1 with
+ * block_ids[b][i + 1] == posterior[b][i], i.e. cumprod then sum of the matches; Step 7:
+ * start += a + 1, the next round's context rows are the anchor's and the accepted
+ * tokens', and the target's token after the accepted prefix is the next anchor):
+ *   accept_len[b]   = a
+ *   next_cu_rows    = [0, a_0 + 1, a_0 + a_1 + 2, ...]: cu_rows of the next round's inject
+ *   ctx_next[b]     = ctx_len[b] + a + 1: the next block's first position, which is also
+ *                     the next round's crop target (ctx_len[b] is this round's)
+ *   next_anchor[b]  = posterior[b][a]
+ * The draft cache itself is cropped with dflash_cache_crop(ctx_len). Nothing is read back
+ * to the host.
+ *   block_ids, posterior  device int32 [batch][bs], bs >= 1
+ *   ctx_len               device int32 [batch]
+ *   accept_len, ctx_next, next_anchor  device int32 [batch]; next_cu_rows [batch + 1]
+ * Host errors: batch < 0, bs < 1, null or misaligned pointers (no launch).
+ */
+dflash_status dflash_accept(const int32_t* block_ids, const int32_t* posterior, int batch, int bs,
+                            const int32_t* ctx_len, int32_t* accept_len, int32_t* next_cu_rows,
+                            int32_t* ctx_next, int32_t* next_anchor, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's sticky
  * status word into *device_status (a mask of DFLASH_DEV_* bits). Returns
  * DFLASH_OK when the word was zero, DFLASH_ERR_DEVICE when not, and
@@ -259,6 +281,7 @@ const char* dflash_status_string(dflash_status s);
 #define DFLASH_KERNEL_CROP          7  /* crop */
 #define DFLASH_KERNEL_ROPE_TABLE    8  /* RoPE table fill */
 #define DFLASH_KERNEL_SCHEDULE      9  /* attention work list */
+#define DFLASH_KERNEL_ACCEPT       10  /* acceptance bookkeeping */
 
 /*
  * Starts recording a CUDA event pair around every launch whose kind bit

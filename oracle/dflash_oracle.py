@@ -379,3 +379,25 @@ def acceptance_length(block_ids, posterior):
             break
         n += 1
     return n
+
+
+def round_bookkeeping(block_ids, posterior, ctx_len):
+    """Acceptance and the next round's state for every sequence.
+
+    DFlash KV Injection Walkthrough, Step 6 (accepted length a = leading matches of
+    block[1:] against posterior[:-1]) and Step 7 (start += a + 1; the next round injects
+    the a + 1 context rows of the anchor and the accepted tokens; the target's token after
+    the accepted prefix becomes the next block's anchor).
+      block_ids, posterior  [B][bs] token ids
+      ctx_len               [B] draft cache length the round started the block at
+    Returns (a [B], next_cu_rows [B + 1], ctx_next [B], next_anchor [B]).
+    """
+    B = len(block_ids)
+    a = [acceptance_length(block_ids[b], posterior[b]) for b in range(B)]
+    counts = [x + 1 for x in a]
+    cu = [0]
+    for c in counts:
+        cu.append(cu[-1] + c)
+    ctx_next = [int(ctx_len[b]) + counts[b] for b in range(B)]
+    anchor = [posterior[b][a[b]] for b in range(B)]
+    return a, cu, ctx_next, anchor

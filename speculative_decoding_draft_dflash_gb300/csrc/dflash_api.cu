@@ -466,6 +466,22 @@ DFLASH_API dflash_status dflash_draft_layer(const dflash_dims* d, const dflash_k
   return cuda_status(e);
 }
 
+DFLASH_API dflash_status dflash_accept(const int32_t* block_ids, const int32_t* posterior,
+                                       int batch, int bs, const int32_t* ctx_len,
+                                       int32_t* accept_len, int32_t* next_cu_rows,
+                                       int32_t* ctx_next, int32_t* next_anchor,
+                                       cudaStream_t stream) {
+  if (batch < 0 || bs < 1) return DFLASH_ERR_INVALID_ARG;
+  if (!next_cu_rows || ((uintptr_t)next_cu_rows & 3)) return DFLASH_ERR_INVALID_ARG;
+  if (batch > 0) {
+    const void* ptrs[] = {block_ids, posterior, ctx_len, accept_len, ctx_next, next_anchor};
+    for (const void* q : ptrs)
+      if (!q || ((uintptr_t)q & 3)) return DFLASH_ERR_INVALID_ARG;
+  }
+  return cuda_status(accept_round(block_ids, posterior, batch, bs, ctx_len, accept_len,
+                                  next_cu_rows, ctx_next, next_anchor, stream));
+}
+
 DFLASH_API dflash_status dflash_cache_crop(const dflash_kv_cache* c, const int32_t* new_lens,
                                            cudaStream_t stream) {
   dflash_status st = check_cache(c, 0);

@@ -158,6 +158,9 @@ cudaError_t head_epilogue_bf16(const HeadEpilogue& e, cudaStream_t s);
 cudaError_t lens_advance(int32_t* lens, const int32_t* cu_rows, int batch, int bs, int M,
                          int capacity, int table_len, cudaStream_t s);
 
+cudaError_t accept_round(const int32_t* block_ids, const int32_t* posterior, int batch, int bs,
+                         const int32_t* ctx_len, int32_t* accept_len, int32_t* cu,
+                         int32_t* ctx_next, int32_t* anchor, cudaStream_t s);
 cudaError_t crop_lens(int32_t* lens, int n_layers, int batch, const int32_t* new_lens,
                       unsigned* status, cudaStream_t s);
 

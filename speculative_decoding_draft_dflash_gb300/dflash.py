@@ -24,7 +24,7 @@ DFLASH_F32, DFLASH_BF16 = 0, 1
 DEV_CAPACITY, DEV_ROPE, DEV_CROP, DEV_ROWS, DEV_TIMEOUT = 1, 2, 4, 8, 16
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE = range(6)
 KERNEL_NAMES = {1: "gemm", 2: "rmsnorm", 3: "head_epilogue", 4: "attention", 5: "combine",
-                6: "lens", 7: "crop", 8: "rope_table", 9: "schedule"}
+                6: "lens", 7: "crop", 8: "rope_table", 9: "schedule", 10: "accept"}
 KERNEL_IDS = {v: k for k, v in KERNEL_NAMES.items()}
 
 
@@ -61,6 +61,7 @@ def _load():
         "dflash_draft_layer": (c_int, [P, P, c_int, P, P, c_int, P, P, P, P, P, P, P, c_int, c_int,
                                        c_float, P, P, c_size_t, P]),
         "dflash_cache_crop": (c_int, [P, P, P]),
+        "dflash_accept": (c_int, [P, P, c_int, c_int, P, P, P, P, P, P]),
         "dflash_status_get": (c_int, [POINTER(c_uint), P]),
         "dflash_status_string": (ctypes.c_char_p, [c_int]),
         "dflash_trace_start": (c_int, [c_uint, c_int]),
@@ -212,6 +213,15 @@ def dflash_cache_crop(cache, new_lens, stream=None):
     desc = cache.desc if isinstance(cache, KVCache) else cache
     _check(_lib.dflash_cache_crop(ctypes.byref(desc), _ptr(new_lens), _stream(stream)),
            "dflash_cache_crop")
+
+
+def dflash_accept(block_ids, posterior, ctx_len, accept_len, next_cu_rows, ctx_next, next_anchor,
+                  stream=None):
+    """Acceptance bookkeeping of a verified round; block_ids / posterior are int32 [batch][bs]."""
+    batch, bs = (int(block_ids.shape[0]), int(block_ids.shape[1])) if block_ids.dim() == 2 else (0, 1)
+    _check(_lib.dflash_accept(_ptr(block_ids), _ptr(posterior), batch, bs, _ptr(ctx_len),
+                              _ptr(accept_len), _ptr(next_cu_rows), _ptr(ctx_next),
+                              _ptr(next_anchor), _stream(stream)), "dflash_accept")
 
 
 def dflash_status_get(stream=None):

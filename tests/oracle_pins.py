@@ -361,4 +361,20 @@ def pin_acceptance(O):
     assert O.acceptance_length([0, 5, 6, 7], [4, 6, 7, 0]) == 0
 
 
+def pin_round_bookkeeping(O):
+    """Step 6-7 state update on the walkthrough's example, plus its recurrence and edge cases."""
+    g = _golden("acceptance_walkthrough.json")
+    a, cu, ctx_next, anchor = O.round_bookkeeping([g["block_output_ids"]], [g["posterior"]],
+                                                  [g["start_before"]])
+    assert a == [g["acceptance_length"]]
+    assert cu == [0, g["new_context_rows"]]
+    assert ctx_next == [g["start_after"]]
+    assert anchor == ["in"]                       # the target's correction becomes the anchor
+    # all accepted: the bonus token after the block; none accepted: the target's first token
+    a, cu, ctx_next, anchor = O.round_bookkeeping([[9, 1, 2, 3], [9, 1, 2, 3], [7]],
+                                                  [[1, 2, 3, 4], [5, 2, 3, 4], [8]], [10, 20, 0])
+    assert a == [3, 0, 0] and cu == [0, 4, 5, 6]
+    assert ctx_next == [14, 21, 1] and anchor == [4, 5, 8]
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -139,3 +139,22 @@ def test_cache_and_window_arguments_rejected(D, lib):
     crop.restype = ctypes.c_int
     assert crop(ctypes.byref(cache), None, None) == 1
     assert crop(ctypes.byref(cache), P(1026), None) == 1
+
+
+def test_accept_arguments_rejected_before_launch(lib):
+    f = lib.dflash_accept
+    f.restype = ctypes.c_int
+    P = ctypes.c_void_p
+    base = [P(256), P(512), 4, 16, P(768), P(1024), P(1280), P(1536), P(1792), None]
+    a = list(base); a[2] = -1          # negative batch
+    assert f(*a) == 1
+    a = list(base); a[3] = 0           # empty blocks
+    assert f(*a) == 1
+    for i in (0, 1, 4, 5, 6, 7, 8):
+        a = list(base); a[i] = None
+        assert f(*a) == 1
+    a = list(base); a[6] = P(1282)     # cu_rows not 4-byte aligned
+    assert f(*a) == 1
+    a = list(base); a[2] = 0; a[0] = None   # no sequences: only cu_rows is needed
+    a[1] = a[4] = a[5] = a[7] = a[8] = None
+    assert f(*a) in (0, 4)             # launches (status 0) or, without a GPU, a CUDA error

@@ -97,7 +97,22 @@ def _acceptance_sum(block_ids, posterior):
     return sum(int(a == b) for a, b in zip(list(block_ids)[1:], list(posterior)[:-1]))
 
 
-_ORIG = {n: getattr(O, n) for n in ("attention_weights", "attention", "q_project", "kv_project")}
+def _bookkeeping_no_anchor_row(block_ids, posterior, ctx_len):
+    a, cu, ctx_next, anchor = _ORIG["round_bookkeeping"](block_ids, posterior, ctx_len)
+    cu2 = [0]
+    for x in a:                     # injects only the accepted tokens, not the anchor row
+        cu2.append(cu2[-1] + x)
+    return a, cu2, [c - 1 for c in ctx_next], anchor
+
+
+def _bookkeeping_anchor_late(block_ids, posterior, ctx_len):
+    a, cu, ctx_next, anchor = _ORIG["round_bookkeeping"](block_ids, posterior, ctx_len)
+    return a, cu, ctx_next, [posterior[b][min(a[b] + 1, len(posterior[b]) - 1)]
+                             for b in range(len(a))]
+
+
+_ORIG = {n: getattr(O, n) for n in ("attention_weights", "attention", "q_project", "kv_project",
+                                    "round_bookkeeping")}
 
 MUTATIONS = {
     "rmsnorm_drops_eps": ("rms_norm", _rms_no_eps),
@@ -117,6 +132,8 @@ MUTATIONS = {
     "v_normalised": ("kv_project", _kv_project_norms_v),
     "k_not_roped": ("kv_project", _kv_project_no_rope),
     "acceptance_counts_all_matches": ("acceptance_length", _acceptance_sum),
+    "next_round_drops_anchor_row": ("round_bookkeeping", _bookkeeping_no_anchor_row),
+    "next_anchor_one_late": ("round_bookkeeping", _bookkeeping_anchor_late),
 }
 
 
