@@ -248,6 +248,43 @@ def draft_attention_forward(C, H, W_Q, W_K, W_V, gamma_q, gamma_k, n_h, n_kv, d_
 
 
 # ---------------------------------------------------------------------------
+# Output projection and the rest of the draft layer (Steps 4.5, 5)
+# ---------------------------------------------------------------------------
+
+def o_proj(attn_out, W_O):
+    """Attn_out = concat[head_1 .. head_n_h] . W_O: the heads, concatenated per row in
+    head order ([rows][n_h * d_h], the layout Step 4.5 reshapes to), projected back to
+    the model width d. DFlash KV Injection Walkthrough, Step 4.5 (nn.Linear, no bias)."""
+    return np.asarray(attn_out, F64) @ np.asarray(W_O, F64).T
+
+
+def silu(x):
+    """x * sigmoid(x), the gate activation of the Qwen3 MLP (a reading: the pages name the
+    decoder layers but do not print their MLP)."""
+    x = np.asarray(x, F64)
+    return x / (1.0 + np.exp(-x))
+
+
+def mlp(x, W_gate, W_up, W_down):
+    """The decoder layer's feed-forward part, read as the Qwen3 SwiGLU MLP:
+    down( silu(x gate^T) * (x up^T) ). Weights [d_ff][d], [d_ff][d], [d][d_ff]."""
+    x = np.asarray(x, F64)
+    g = x @ np.asarray(W_gate, F64).T
+    u = x @ np.asarray(W_up, F64).T
+    return (silu(g) * u) @ np.asarray(W_down, F64).T
+
+
+def layer_output(x, attn_out, W_O, gamma_post, W_gate, W_up, W_down, eps):
+    """The rest of a draft decoder layer after its attention, read as the Qwen3 pre-norm
+    residual layer (Step 5 names the two decoder layers and the final RMSNorm only):
+        x1  = x + o_proj(attn_out)                       (Step 4.5, then the residual)
+        out = x1 + mlp(RMSNorm_post(x1))
+    x is the layer's residual input [rows][d] (the rows of the block)."""
+    x1 = np.asarray(x, F64) + o_proj(attn_out, W_O)
+    return x1 + mlp(rms_norm(x1, gamma_post, eps), W_gate, W_up, W_down)
+
+
+# ---------------------------------------------------------------------------
 # The draft KV cache and the four calls of the step (Steps 4.2-4.4, 7)
 # ---------------------------------------------------------------------------
 

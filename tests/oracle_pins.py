@@ -377,4 +377,62 @@ def pin_round_bookkeeping(O):
     assert ctx_next == [14, 21, 1] and anchor == [4, 5, 8]
 
 
+
+
+def pin_o_proj_shapes_and_identity(O):
+    """Step 4.5: [4, 8, 64] reshaped to [4, 512], projected to [4, 512]; W_O = I keeps the
+    concatenated heads; head blocks of W_O select heads."""
+    rng = np.random.default_rng(21)
+    attn = rng.standard_normal((4, 8, 64)).reshape(4, 512)
+    assert O.o_proj(attn, np.eye(512)).shape == (4, 512)
+    np.testing.assert_allclose(O.o_proj(attn, np.eye(512)), attn, rtol=0, atol=0)
+    W = np.zeros((64, 512))
+    W[:, 3 * 64:4 * 64] = np.eye(64)                   # picks head 3
+    np.testing.assert_allclose(O.o_proj(attn, W), attn[:, 192:256], rtol=0, atol=0)
+
+
+def pin_silu_closed_forms(O):
+    """silu(0) = 0, silu(x) -> x for large x, -> 0 for very negative x, silu(x) - silu(-x) = x."""
+    x = np.linspace(-6, 6, 25)
+    assert O.silu(np.zeros(3)).tolist() == [0.0, 0.0, 0.0]
+    np.testing.assert_allclose(O.silu(x) - O.silu(-x), x, rtol=1e-13, atol=1e-13)
+    assert abs(O.silu(40.0) - 40.0) < 1e-12 and abs(O.silu(-40.0)) < 1e-15
+    np.testing.assert_allclose(O.silu(1.0), 1.0 / (1.0 + np.exp(-1.0)), rtol=1e-15)
+
+
+def pin_mlp_brute_force(O):
+    """SwiGLU MLP against a pure-Python triple loop, and its degenerate weights."""
+    rng = np.random.default_rng(22)
+    d, f, n = 6, 5, 3
+    x = rng.standard_normal((n, d))
+    Wg, Wu, Wd = rng.standard_normal((f, d)), rng.standard_normal((f, d)), rng.standard_normal((d, f))
+    want = np.zeros((n, d))
+    for r in range(n):
+        h = []
+        for j in range(f):
+            g = sum(x[r, k] * Wg[j, k] for k in range(d))
+            u = sum(x[r, k] * Wu[j, k] for k in range(d))
+            h.append(g / (1.0 + np.exp(-g)) * u)
+        for i in range(d):
+            want[r, i] = sum(h[j] * Wd[i, j] for j in range(f))
+    np.testing.assert_allclose(O.mlp(x, Wg, Wu, Wd), want, rtol=1e-12, atol=1e-12)
+    assert not O.mlp(x, Wg, np.zeros_like(Wu), Wd).any()     # no up path -> nothing
+
+
+def pin_layer_output_residuals(O):
+    """Zero o_proj and zero MLP leave the residual stream; each path adds on top of it."""
+    rng = np.random.default_rng(23)
+    n, d, a, f = 3, 8, 8, 4
+    x, att = rng.standard_normal((n, d)), rng.standard_normal((n, a))
+    WO, Wg, Wu, Wd = (rng.standard_normal(s) for s in ((d, a), (f, d), (f, d), (d, f)))
+    g = np.ones(d)
+    np.testing.assert_allclose(O.layer_output(x, att, 0 * WO, g, Wg, Wu, 0 * Wd, 1e-6), x, atol=0)
+    x1 = x + att @ WO.T
+    np.testing.assert_allclose(O.layer_output(x, att, WO, g, Wg, Wu, 0 * Wd, 1e-6), x1, rtol=1e-13)
+    nrm = x1 / np.sqrt((x1 ** 2).mean(-1, keepdims=True) + 1e-6)
+    h = nrm @ Wg.T
+    want = x1 + ((h / (1 + np.exp(-h))) * (nrm @ Wu.T)) @ Wd.T
+    np.testing.assert_allclose(O.layer_output(x, att, WO, g, Wg, Wu, Wd, 1e-6), want, rtol=1e-12)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

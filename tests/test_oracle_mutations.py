@@ -111,6 +111,20 @@ def _bookkeeping_anchor_late(block_ids, posterior, ctx_len):
                              for b in range(len(a))]
 
 
+def _o_proj_untransposed(attn_out, W_O):
+    return np.asarray(attn_out, np.float64) @ np.asarray(W_O, np.float64)
+
+
+def _mlp_silu_on_up(x, W_gate, W_up, W_down):
+    x = np.asarray(x, np.float64)
+    return ((x @ np.asarray(W_gate).T) * O.silu(x @ np.asarray(W_up).T)) @ np.asarray(W_down).T
+
+
+def _layer_norm_before_residual(x, attn_out, W_O, gamma_post, W_gate, W_up, W_down, eps):
+    x1 = np.asarray(x, np.float64) + O.o_proj(attn_out, W_O)
+    return x1 + O.mlp(O.rms_norm(x, gamma_post, eps), W_gate, W_up, W_down)
+
+
 _ORIG = {n: getattr(O, n) for n in ("attention_weights", "attention", "q_project", "kv_project",
                                     "round_bookkeeping")}
 
@@ -134,6 +148,9 @@ MUTATIONS = {
     "acceptance_counts_all_matches": ("acceptance_length", _acceptance_sum),
     "next_round_drops_anchor_row": ("round_bookkeeping", _bookkeeping_no_anchor_row),
     "next_anchor_one_late": ("round_bookkeeping", _bookkeeping_anchor_late),
+    "o_proj_untransposed": ("o_proj", _o_proj_untransposed),
+    "mlp_silu_on_up_branch": ("mlp", _mlp_silu_on_up),
+    "post_norm_before_residual": ("layer_output", _layer_norm_before_residual),
 }
 
 
