@@ -383,6 +383,7 @@ def run_ours(args, w):
     others = {k: rf(k) for k in kernels if k != dominant and (k in costs or k == "attention")}
     prefill = run_prefill_gemms(args, w, dev, stream, D, pk) if w.prefill_inject else None
     bookkeeping = time_accept(args, w, stream, D)
+    layer_rest = time_layer_out(args, w, stream, D, pk) if w.dtype == "bf16" else None
 
     # ---- end to end: host inputs in, host results out, through the same calls ----
     e2e = run_e2e(args, w, dev, x, stream, D)
@@ -401,6 +402,8 @@ def run_ours(args, w):
     if prefill is not None:
         line["prefill_gemms"] = prefill
     line["bookkeeping"] = bookkeeping
+    if layer_rest is not None:
+        line["layer_output"] = layer_rest
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, total, n, _ = oracle_sample_rate(w, budget_s=12.0)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count(),
@@ -551,6 +554,54 @@ def time_accept(args, w, stream, D):
     ms = [t for k, t in D.dflash_trace_stop() if k == "accept"]
     return {"kernel": "accept", "launches": len(ms), "avg_us": 1e3 * sum(ms) / max(1, len(ms)),
             "batch": B, "block": bs, "bound": "launch"}
+
+
+def time_layer_out(args, w, stream, D, pk):
+    """The rest of a draft layer on the block rows (o_proj + residual, post norm, SwiGLU MLP +
+    residual) at this workload's width: time per call and the rooflines of its three GEMMs."""
+    import torch
+    from speculative_decoding_draft_dflash_gb300 import synth
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to("cuda", torch.bfloat16)  # noqa: E731
+    M, d, a, f = w.batch * w.bs, w.d, w.n_h * w.d_h, w.ffn
+    dims = D.make_dims(w.d, w.n_h, w.n_kv, w.d_h, w.k, w.bs, w.eps, w.dtype)
+    Wt = [dev(g(w, 0)) for g in (synth.W_O, synth.gamma_post, synth.W_gate, synth.W_up, synth.W_down)]
+    attn, x = dev(synth.attn_rows(w, 1, 0)), dev(synth.residual(w, 1, 0))
+    out = torch.empty_like(x)
+    ws = torch.empty(D.dflash_layer_out_workspace_bytes(dims, M, f), dtype=torch.uint8, device="cuda")
+    call = lambda: D.dflash_layer_out(dims, M, attn, x, Wt[0], Wt[1], f, Wt[2], Wt[3], Wt[4],  # noqa: E731
+                                      out, ws, stream)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                call()
+        return g
+
+    call()
+    torch.cuda.synchronize()
+    n = max(10, min(args.steps, 50))
+    g = capture(n)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = 1e3 * e0.elapsed_time(e1) / n
+    assert D.dflash_status_get(stream) == 0, "device status after the layer output"
+    pargs = argparse.Namespace(**{**vars(args), "steps": n})
+    kernels, _ = traced_kernels(pargs, D, stream, capture, lambda: [call() for _ in range(n)],
+                                ["gemm_o_proj", "gemm_gate_up", "gemm_down"])
+    costs = {"gemm_o_proj": gemm_cost(M, a, d), "gemm_gate_up": gemm_cost(M, d, 2 * f),
+             "gemm_down": gemm_cost(M, f, d)}
+    total_flops = sum(c[0] for c in costs.values())
+    return {"rows": M, "d": d, "d_ff": f, "us_per_call": us,
+            "tflops_per_call": total_flops / (us * 1e-6) / 1e12,
+            "gemms": {k: {**roofline_for(k, kernels, costs, 0, pk), "avg_us": kernels[k]["avg_us"]}
+                      for k in costs if k in kernels},
+            "timing": "one graph replay of the calls, no tracing; GEMM durations from a traced replay"}
 
 
 def synth_lens(w):

@@ -226,6 +226,36 @@ dflash_status dflash_draft_layer(const dflash_dims* dims, const dflash_kv_cache*
                                  void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * The rest of a draft decoder layer after its attention, for M rows (the blocks' rows):
+ *   x1  = x + attn_out W_O^T                         (Walkthrough Step 4.5: the heads,
+ *                                                     concatenated, times W_O)
+ *   out = x1 + W_down( silu(n W_gate^T) * (n W_up^T) ),  n = RMSNorm_post(x1)
+ * Step 5 of the walkthrough names the draft's decoder layers and the final norm but does
+ * not print them; the residual blocks and the SwiGLU MLP follow the Qwen3 decoder layer
+ * that the source guide's Qwen3DFlashAttention and Qwen3RMSNorm belong to.
+ *   attn_out    device [M][n_h * d_h] (dflash_block_attn's out)
+ *   x, x_out    device [M][d] residual stream in / out (x_out may be x)
+ *   W_O         device [d][n_h * d_h];  gamma_post device [d]
+ *   W_gate, W_up device [d_ff][d];      W_down     device [d][d_ff]
+ *   d_ff        > 0, a multiple of 4 (bf16: of 64); d a multiple of 4, at most 8192
+ *   workspace   dflash_layer_out_workspace_bytes(dims, M, d_ff) bytes, 256-byte aligned
+ * All pointers 16-byte aligned. Host errors as the other calls.
+ */
+size_t dflash_layer_out_workspace_bytes(const dflash_dims* dims, int M, int d_ff);
+dflash_status dflash_layer_out(const dflash_dims* dims, int M, const void* attn_out, const void* x,
+                               const void* W_O, const void* gamma_post, int d_ff,
+                               const void* W_gate, const void* W_up, const void* W_down,
+                               void* x_out, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * out = RMSNorm(x) * gamma over rows of width d (eps of dims): the layers' input norm and
+ * the final norm after the last draft layer (Walkthrough Step 5).
+ *   x, out  device [M][d], gamma device [d]; 16-byte aligned; d a multiple of 4, <= 8192
+ */
+dflash_status dflash_rms_norm(const dflash_dims* dims, int M, const void* x, const void* gamma,
+                              void* out, cudaStream_t stream);
+
+/*
  * crop(start) on every layer: lens[l][b] = new_lens[b] for all l. No cache
  * data moves. (DFlash source guide (II), part 4; DFlash KV Injection
  * Walkthrough, Step 7.) A target that is negative or above a layer's current

@@ -466,6 +466,59 @@ DFLASH_API dflash_status dflash_draft_layer(const dflash_dims* d, const dflash_k
   return cuda_status(e);
 }
 
+namespace {
+// shapes the layer-output kernels take: GEMM K and N in whole 64-wide blocks for the
+// tensor-core path, rows of whole float4 / 4-element groups for the row kernels
+dflash_status check_layer_out(const dflash_dims* d, int M, int d_ff) {
+  dflash_status st = check_dims(d);
+  if (st != DFLASH_OK) return st;
+  if (M < 0 || d_ff <= 0 || d_ff % 4 || !rows_ok(d->d)) return DFLASH_ERR_INVALID_ARG;
+  if (d->dtype == DFLASH_BF16 && (d_ff % 64 || (d->n_h * d->d_h) % 64))
+    return DFLASH_ERR_UNSUPPORTED;
+  return DFLASH_OK;
+}
+}  // namespace
+
+DFLASH_API size_t dflash_layer_out_workspace_bytes(const dflash_dims* d, int M, int d_ff) {
+  if (check_layer_out(d, M, d_ff) != DFLASH_OK) return 0;
+  Carver cv(nullptr, ~size_t(0));
+  carve_layer_out(cv, d->dtype, M, d->d, d->n_h * d->d_h, d_ff);
+  return cv.off > 256 ? cv.off : 256;
+}
+
+DFLASH_API dflash_status dflash_layer_out(const dflash_dims* d, int M, const void* attn_out,
+                                          const void* x, const void* W_O, const void* gamma_post,
+                                          int d_ff, const void* W_gate, const void* W_up,
+                                          const void* W_down, void* x_out, void* workspace,
+                                          size_t ws_bytes, cudaStream_t stream) {
+  dflash_status st = check_layer_out(d, M, d_ff);
+  if (st != DFLASH_OK) return st;
+  if (M == 0) return DFLASH_OK;
+  const void* ptrs[] = {attn_out, x, W_O, gamma_post, W_gate, W_up, W_down, x_out};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return DFLASH_ERR_INVALID_ARG;
+  if (!workspace || ((uintptr_t)workspace & 255)) return DFLASH_ERR_INVALID_ARG;
+  Carver cv(workspace, ws_bytes);
+  const LayerOutScratch sc = carve_layer_out(cv, d->dtype, M, d->d, d->n_h * d->d_h, d_ff);
+  if (!cv.ok) return DFLASH_ERR_WORKSPACE;
+  unsigned* status = status_word();
+  if (!status) return DFLASH_ERR_CUDA;
+  return cuda_status(layer_out(d->dtype, M, d->d, d->n_h * d->d_h, d_ff, attn_out, x, W_O,
+                               gamma_post, d->eps, W_gate, W_up, W_down, x_out, sc, status,
+                               stream));
+}
+
+DFLASH_API dflash_status dflash_rms_norm(const dflash_dims* d, int M, const void* x,
+                                         const void* gamma, void* out, cudaStream_t stream) {
+  dflash_status st = check_dims(d);
+  if (st != DFLASH_OK) return st;
+  if (M < 0 || !rows_ok(d->d)) return DFLASH_ERR_INVALID_ARG;
+  if (M == 0) return DFLASH_OK;
+  if (!x || !gamma || !out || !aligned16(x) || !aligned16(gamma) || !aligned16(out))
+    return DFLASH_ERR_INVALID_ARG;
+  return cuda_status(norm_rows(d->dtype, M, d->d, x, gamma, d->eps, out, stream));
+}
+
 DFLASH_API dflash_status dflash_accept(const int32_t* block_ids, const int32_t* posterior,
                                        int batch, int bs, const int32_t* ctx_len,
                                        int32_t* accept_len, int32_t* next_cu_rows,

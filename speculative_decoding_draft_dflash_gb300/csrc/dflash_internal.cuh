@@ -158,6 +158,25 @@ cudaError_t head_epilogue_bf16(const HeadEpilogue& e, cudaStream_t s);
 cudaError_t lens_advance(int32_t* lens, const int32_t* cu_rows, int batch, int bs, int M,
                          int capacity, int table_len, cudaStream_t s);
 
+// The rest of a draft decoder layer (layer_out.cu): o_proj + residual, post-attention
+// RMSNorm, SwiGLU MLP + residual; and a plain row RMSNorm.
+struct LayerOutScratch {
+  float* Y;    // o_proj / down split-K partials
+  float* Ygu;  // gate | up split-K partials
+  void* x1;    // residual after o_proj
+  void* n;     // RMSNorm_post(x1)
+  void* h;     // silu(gate) * up
+  int splits_o, splits_gu, splits_d;
+};
+bool rows_ok(int N);
+LayerOutScratch carve_layer_out(Carver& cv, int dtype, int M, int d, int a_dim, int d_ff);
+cudaError_t layer_out(int dtype, int M, int d, int a_dim, int d_ff, const void* attn_out,
+                      const void* x, const void* W_O, const void* gamma_post, float eps,
+                      const void* W_gate, const void* W_up, const void* W_down, void* x_out,
+                      const LayerOutScratch& sc, unsigned* status, cudaStream_t s);
+cudaError_t norm_rows(int dtype, int M, int N, const void* x, const void* gamma, float eps,
+                      void* out, cudaStream_t s);
+
 cudaError_t accept_round(const int32_t* block_ids, const int32_t* posterior, int batch, int bs,
                          const int32_t* ctx_len, int32_t* accept_len, int32_t* cu,
                          int32_t* ctx_next, int32_t* anchor, cudaStream_t s);

@@ -61,6 +61,9 @@ def _load():
         "dflash_draft_layer": (c_int, [P, P, c_int, P, P, c_int, P, P, P, P, P, P, P, c_int, c_int,
                                        c_float, P, P, c_size_t, P]),
         "dflash_cache_crop": (c_int, [P, P, P]),
+        "dflash_layer_out_workspace_bytes": (c_size_t, [P, c_int, c_int]),
+        "dflash_layer_out": (c_int, [P, c_int, P, P, P, P, c_int, P, P, P, P, P, c_size_t, P]),
+        "dflash_rms_norm": (c_int, [P, c_int, P, P, P, P]),
         "dflash_accept": (c_int, [P, P, c_int, c_int, P, P, P, P, P, P]),
         "dflash_status_get": (c_int, [POINTER(c_uint), P]),
         "dflash_status_string": (ctypes.c_char_p, [c_int]),
@@ -222,6 +225,25 @@ def dflash_accept(block_ids, posterior, ctx_len, accept_len, next_cu_rows, ctx_n
     _check(_lib.dflash_accept(_ptr(block_ids), _ptr(posterior), batch, bs, _ptr(ctx_len),
                               _ptr(accept_len), _ptr(next_cu_rows), _ptr(ctx_next),
                               _ptr(next_anchor), _stream(stream)), "dflash_accept")
+
+
+def dflash_layer_out_workspace_bytes(dims, M, d_ff):
+    return int(_lib.dflash_layer_out_workspace_bytes(ctypes.byref(dims), int(M), int(d_ff)))
+
+
+def dflash_layer_out(dims, M, attn_out, x, W_O, gamma_post, d_ff, W_gate, W_up, W_down, x_out,
+                     workspace, stream=None):
+    """x_out = x1 + MLP(RMSNorm_post(x1)), x1 = x + attn_out W_O^T (rows of the blocks)."""
+    _check(_lib.dflash_layer_out(ctypes.byref(dims), int(M), _ptr(attn_out), _ptr(x), _ptr(W_O),
+                                 _ptr(gamma_post), int(d_ff), _ptr(W_gate), _ptr(W_up),
+                                 _ptr(W_down), _ptr(x_out), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)),
+           "dflash_layer_out")
+
+
+def dflash_rms_norm(dims, M, x, gamma, out, stream=None):
+    _check(_lib.dflash_rms_norm(ctypes.byref(dims), int(M), _ptr(x), _ptr(gamma), _ptr(out),
+                                _stream(stream)), "dflash_rms_norm")
 
 
 def dflash_status_get(stream=None):

@@ -27,6 +27,7 @@ import numpy as np
 # stream tags (one per kind of array)
 _T_WFC, _T_WQ, _T_WK, _T_WV, _T_GAMMA = 1, 2, 3, 4, 5
 _T_HIDDEN, _T_BLOCK, _T_CACHE_K, _T_CACHE_V, _T_PREFILL_LEN, _T_ACCEPT = 6, 7, 8, 9, 10, 11
+_T_WO, _T_WGATE, _T_WUP, _T_WDOWN, _T_RESID, _T_ATTN = 12, 13, 14, 15, 16, 17
 
 
 @dataclass(frozen=True)
@@ -64,6 +65,11 @@ class Workload:
     seed: int = 0
     random_gamma: bool = False
     description: str = ""
+    d_ff: int = 0          # MLP width of the rest of the decoder layer; 0 = 3 * d
+
+    @property
+    def ffn(self):
+        return self.d_ff or 3 * self.d
 
     @property
     def G(self):
@@ -180,6 +186,40 @@ def gamma_q(w: Workload, layer: int):
 def gamma_k(w: Workload, layer: int):
     """k_norm gamma [d_h]."""
     return _gamma(w, w.d_h, 2, layer)
+
+
+def gamma_post(w: Workload, layer: int):
+    """post-attention RMSNorm gamma [d]."""
+    return _gamma(w, w.d, 3, layer)
+
+
+# ---- the rest of the decoder layer (o_proj, MLP) ----------------------------
+
+def W_O(w: Workload, layer: int):
+    return _normal(w, (w.d, w.n_h * w.d_h), 0.02, _T_WO, layer)
+
+
+def W_gate(w: Workload, layer: int):
+    return _normal(w, (w.ffn, w.d), 0.02, _T_WGATE, layer)
+
+
+def W_up(w: Workload, layer: int):
+    return _normal(w, (w.ffn, w.d), 0.02, _T_WUP, layer)
+
+
+def W_down(w: Workload, layer: int):
+    return _normal(w, (w.d, w.ffn), 0.02, _T_WDOWN, layer)
+
+
+def residual(w: Workload, rnd: int, layer: int):
+    """The residual stream entering a layer's output part, [B * bs][d] ~ N(0, 1)."""
+    return _normal(w, (w.batch * w.bs, w.d), 1.0, _T_RESID, rnd, layer)
+
+
+def attn_rows(w: Workload, rnd: int, layer: int):
+    """Stand-in attention output rows [B * bs][n_h * d_h] ~ N(0, 0.25) (values of V rows'
+    convex combinations) for exercising the layer output alone."""
+    return _normal(w, (w.batch * w.bs, w.n_h * w.d_h), 0.5, _T_ATTN, rnd, layer)
 
 
 # ---- schedule ------------------------------------------------------------

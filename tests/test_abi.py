@@ -158,3 +158,31 @@ def test_accept_arguments_rejected_before_launch(lib):
     a = list(base); a[2] = 0; a[0] = None   # no sequences: only cu_rows is needed
     a[1] = a[4] = a[5] = a[7] = a[8] = None
     assert f(*a) in (0, 4)             # launches (status 0) or, without a GPU, a CUDA error
+
+
+def test_layer_out_arguments_rejected_before_launch(D, lib):
+    dims = _dims(D)
+    ws = lib.dflash_layer_out_workspace_bytes
+    ws.restype = ctypes.c_size_t
+    assert ws(ctypes.byref(dims), 64, 1024) > 0
+    assert ws(ctypes.byref(dims), 64, 0) == 0 and ws(ctypes.byref(dims), 64, 1002) == 0
+    f = lib.dflash_layer_out
+    f.restype = ctypes.c_int
+    P = ctypes.c_void_p
+    base = [ctypes.byref(dims), 64, P(256), P(512), P(768), P(1024), 1024, P(1280), P(1536),
+            P(1792), P(2048), P(4096), ctypes.c_size_t(1 << 30), None]
+    for i in (2, 3, 4, 5, 7, 8, 9, 10, 11):
+        a = list(base); a[i] = None
+        assert f(*a) == 1
+    a = list(base); a[4] = P(770)       # W_O misaligned
+    assert f(*a) == 1
+    a = list(base); a[6] = 1000         # d_ff not a multiple of 64 on the bf16 path
+    assert f(*a) == 2
+    a = list(base); a[12] = ctypes.c_size_t(1000)
+    assert f(*a) == 3
+    a = list(base); a[1] = 0
+    assert f(*a) == 0
+    n = lib.dflash_rms_norm
+    n.restype = ctypes.c_int
+    assert n(ctypes.byref(dims), 4, None, P(256), P(512), None) == 1
+    assert n(ctypes.byref(dims), -1, P(256), P(256), P(512), None) == 1
