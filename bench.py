@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch every call eagerly")
+    ap.add_argument("--paged", action="store_true", help="paged KV cache (128-row pages)")
     return ap.parse_args()
 
 
@@ -301,7 +302,7 @@ def run_ours(args, w):
 
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
-    dev = DeviceWorkload(w)
+    dev = DeviceWorkload(w, paged=args.paged)
     L0 = synth.prefill_lens(w)
     counts = np.full(w.batch, w.new_ctx, dtype=np.int64)
     x = dev.round_inputs(1, L0, counts=counts, crop_to=L0)
@@ -391,7 +392,8 @@ def run_ours(args, w):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": config_of(w), "clocks": clk.summary(), "e2e": e2e,
+            "config": {**config_of(w), **({"cache": "paged, 128-row pages"} if args.paged else {})},
+            "clocks": clk.summary(), "e2e": e2e,
             "gpu_launches": int(launches), "roofline": roofline, "roofline_other": others,
             "kernels": kernels,
             "timing": ("value: one replay of a CUDA graph of the K steps, no tracing; kernel "

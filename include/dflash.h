@@ -83,17 +83,28 @@ typedef struct {
 
 /*
  * Draft KV cache, all device memory owned by the caller.
- *   k, v      [n_layers][batch][n_kv][capacity][d_h] elements of dims->dtype,
+ *   k, v      contiguous (block_table == NULL):
+ *               [n_layers][batch][n_kv][capacity][d_h] elements of dims->dtype
+ *             paged (block_table != NULL, bf16 only):
+ *               [n_layers][n_pages][n_kv][page_size][d_h]; logical slot s of
+ *               sequence b lives in page block_table[b][s / page_size] at row
+ *               s % page_size of every layer's pool
  *             16-byte aligned
  *   lens      int32 [n_layers][batch]: rows held per layer and sequence
+ *   capacity  logical rows per sequence (paged: a multiple of page_size)
+ *   block_table  device int32 [batch][capacity / page_size] page ids in [0, n_pages),
+ *             or NULL; page_size must be 128 (one page is one attention tile)
  * (DFlash source guide (II), part 4: the DynamicCache that update() appends
- * to and crop(start) truncates.)
+ * to and crop(start) truncates. A paged cache holds the same logical rows; the
+ * caller owns the page allocation, lengths and crops stay logical.)
  */
 typedef struct {
   void* k;
   void* v;
   int32_t* lens;
   int n_layers, batch, capacity;
+  const int32_t* block_table;
+  int page_size, n_pages;
 } dflash_kv_cache;
 
 /*

@@ -37,6 +37,7 @@ struct Params {
   int32_t* qstart;          // [batch]: first position of the block
   int32_t* lens_new;        // [batch]: length after the call
   int batch, n_kv, bs, window, capacity, table_len, max_splits, n_sm;
+  int align;                // key ranges start on multiples of this (paged cache: a page)
 };
 
 // Rows the inject of the same call appended for sequence b: all of its rows when they
@@ -63,6 +64,7 @@ __device__ __forceinline__ Range seq_range(const Params& p, int b) {
   r.start = l + injected_rows(p.pre_rows, p.pre_M, b, l, p.capacity, p.table_len);
   r.end = r.start + p.bs;
   r.lo = p.window > 0 ? max(0, r.start - p.window + 1) : 0;
+  r.lo -= r.lo % p.align;  // keys below the window's start are masked by the window test
   r.ok = r.start >= 0 && r.end <= p.capacity && r.end <= p.table_len;
   return r;
 }

@@ -68,6 +68,8 @@ struct AttnTcParams {
   CUtensorMap q;   // [B*n_h*bs][128] bf16, box rows 64 (NARROW) or 128
   CUtensorMap k;   // [B*n_kv*capacity][128] bf16 (this layer)
   CUtensorMap v;
+  const int32_t* table;   // paged cache: [batch][pps] page ids of 128-row pages, or null
+  int pps;
   const int32_t* qstart;  // [batch]: first position of each block (window test)
   int32_t* lens;          // [batch]: receives lens_new once the attention is done
   const int32_t* lens_new;
@@ -90,6 +92,13 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity, unsigned* s
       return;
     }
   }
+}
+
+// First row of the 128-key tile starting at key k0 (a multiple of 128 when paged) of
+// (sequence b, KV head kvh) in the K / V tensor maps.
+__device__ __forceinline__ int tile_row(const AttnTcParams& p, int b, int kvh, int k0) {
+  if (p.table) return (p.table[b * p.pps + (k0 >> 7)] * p.n_kv + kvh) * TK;
+  return (b * p.n_kv + kvh) * p.capacity + k0;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -210,9 +219,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         ptx::tma_load_2d(qd, &p.q, q_full0 + 8 * qb, 0, qrow);
         ptx::tma_load_2d(qd + HALF, &p.q, q_full0 + 8 * qb, 64, qrow);
         ++nq_loads;
-        const int kvrow = (b * p.n_kv + kvh) * p.capacity;
         const int ntiles = (it.z - it.y + TK - 1) / TK;
+        int row_next = tile_row(p, b, kvh, it.y);  // the next tile's row, fetched a tile ahead
         for (int j = 0; j < ntiles; ++j) {
+          const int row = row_next;
+          if (j + 1 < ntiles) row_next = tile_row(p, b, kvh, it.y + (j + 1) * TK);
           const int s = gk % PL::K_STAGES, u = gk / PL::K_STAGES;
           if (gk >= PL::K_STAGES &&
               !ptx::mbar_wait(k_empty0 + 8 * s, (u - 1) & 1, &abort_flag, p.status)) {
@@ -221,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           }
           const uint32_t kd = sbase + PL::OFF_K + s * TILE;
           ptx::mbar_arrive_expect_tx(k_full0 + 8 * s, TILE);
-          ptx::tma_load_2d_hint(kd, &p.k, k_full0 + 8 * s, 0, kvrow + it.y + j * TK, pol);
-          ptx::tma_load_2d_hint(kd + HALF, &p.k, k_full0 + 8 * s, 64, kvrow + it.y + j * TK, pol);
+          ptx::tma_load_2d_hint(kd, &p.k, k_full0 + 8 * s, 0, row, pol);
+          ptx::tma_load_2d_hint(kd + HALF, &p.k, k_full0 + 8 * s, 64, row, pol);
           ++gk;
         }
         if (stop) break;
@@ -246,9 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         ptx::mbar_arrive(it_empty0 + 8 * slot);
         if (it.x < 0) break;
         const int b = it.x / p.n_kv, kvh = it.x - b * p.n_kv;
-        const int kvrow = (b * p.n_kv + kvh) * p.capacity;
         const int ntiles = (it.z - it.y + TK - 1) / TK;
+        int row_next = tile_row(p, b, kvh, it.y);
         for (int j = 0; j < ntiles; ++j) {
+          const int row = row_next;
+          if (j + 1 < ntiles) row_next = tile_row(p, b, kvh, it.y + (j + 1) * TK);
           const int s = gv % PL::V_STAGES, u = gv / PL::V_STAGES;
           if (gv >= PL::V_STAGES &&
               !ptx::mbar_wait(v_empty0 + 8 * s, (u - 1) & 1, &abort_flag, p.status)) {
@@ -257,8 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           }
           const uint32_t vd = sbase + PL::OFF_V + s * TILE;
           ptx::mbar_arrive_expect_tx(v_full0 + 8 * s, TILE);
-          ptx::tma_load_2d_hint(vd, &p.v, v_full0 + 8 * s, 0, kvrow + it.y + j * TK, pol);
-          ptx::tma_load_2d_hint(vd + HALF, &p.v, v_full0 + 8 * s, 64, kvrow + it.y + j * TK, pol);
+          ptx::tma_load_2d_hint(vd, &p.v, v_full0 + 8 * s, 0, row, pol);
+          ptx::tma_load_2d_hint(vd + HALF, &p.v, v_full0 + 8 * s, 64, row, pol);
           ++gv;
         }
       }
@@ -635,6 +648,7 @@ sched::Params attn_sched_params(const AttnParams& a) {
   sp.table_len = a.table_len;
   sp.max_splits = a.n_chunks;  // ranges are cut into at most this many items
   sp.n_sm = sm_count();
+  sp.align = a.block_table ? TK : 1;
   return sp;
 }
 
@@ -645,10 +659,14 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   memset(&p, 0, sizeof(p));
   const int R = (a.n_h / a.n_kv) * a.bs;
   const bool narrow = R <= 64;
+  const long long kv_rows = a.block_table ? (long long)a.n_pages * a.n_kv * TK
+                                          : (long long)a.batch * a.n_kv * a.capacity;
   if (!encode_2d_bf16(&p.q, a.q, (long long)a.batch * a.n_h * a.bs, 128, narrow ? 64 : 128) ||
-      !encode_2d_bf16(&p.k, a.cache_k, (long long)a.batch * a.n_kv * a.capacity, 128, 128) ||
-      !encode_2d_bf16(&p.v, a.cache_v, (long long)a.batch * a.n_kv * a.capacity, 128, 128))
+      !encode_2d_bf16(&p.k, a.cache_k, kv_rows, 128, 128) ||
+      !encode_2d_bf16(&p.v, a.cache_v, kv_rows, 128, 128))
     return cudaErrorInvalidValue;
+  p.table = a.block_table;
+  p.pps = a.pages_per_seq;
   const int pairs = a.batch * a.n_kv;
   const sched::Params sp = attn_sched_params(a);
   p.max_splits = sp.max_splits;

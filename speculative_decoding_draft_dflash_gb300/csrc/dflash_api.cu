@@ -52,7 +52,17 @@ dflash_status check_cache(const dflash_kv_cache* c, int layer) {
   if (c->n_layers <= 0 || c->batch <= 0 || c->capacity <= 0) return DFLASH_ERR_INVALID_ARG;
   if (layer < 0 || layer >= c->n_layers) return DFLASH_ERR_INVALID_ARG;
   if (!aligned16(c->k) || !aligned16(c->v) || ((uintptr_t)c->lens & 3)) return DFLASH_ERR_INVALID_ARG;
+  if (c->block_table) {  // paged: 128-row pages (one attention tile each)
+    if (c->page_size != 128 || c->capacity % 128 || c->n_pages <= 0 ||
+        ((uintptr_t)c->block_table & 3))
+      return DFLASH_ERR_INVALID_ARG;
+  }
   return DFLASH_OK;
+}
+
+// the paged layout is served by the bf16 tensor-core path only
+dflash_status check_layout(const dflash_dims* d, const dflash_kv_cache* c) {
+  return c->block_table && d->dtype != DFLASH_BF16 ? DFLASH_ERR_UNSUPPORTED : DFLASH_OK;
 }
 
 size_t esize(const dflash_dims* d) { return d->dtype == DFLASH_F32 ? 4 : 2; }
@@ -228,7 +238,10 @@ DFLASH_API dflash_status dflash_ctx_project(const dflash_dims* d, const void* co
 
 namespace {
 
+// elements of one layer's K (or V): [batch][n_kv][capacity][d_h], or a pool of
+// [n_pages][n_kv][128][d_h] when paged
 size_t layer_elems(const dflash_dims* d, const dflash_kv_cache* c) {
+  if (c->block_table) return (size_t)c->n_pages * d->n_kv * 128 * d->d_h;
   return (size_t)c->batch * d->n_kv * c->capacity * d->d_h;
 }
 
@@ -259,6 +272,8 @@ HeadEpilogue inject_epilogue(const dflash_dims* d, const dflash_kv_cache* c, int
   ep.cache_v = (char*)c->v + (size_t)layer * layer_elems(d, c) * esize(d);
   ep.capacity = c->capacity;
   ep.status = status;
+  ep.block_table = c->block_table;
+  ep.pages_per_seq = c->block_table ? c->capacity / 128 : 0;
   return ep;
 }
 
@@ -289,6 +304,8 @@ HeadEpilogue block_epilogue(const dflash_dims* d, const dflash_kv_cache* c, int 
   ep.cache_v = (char*)c->v + (size_t)layer * layer_elems(d, c) * esize(d);
   ep.capacity = c->capacity;
   ep.status = status;
+  ep.block_table = c->block_table;
+  ep.pages_per_seq = c->block_table ? c->capacity / 128 : 0;
   return ep;
 }
 
@@ -319,6 +336,9 @@ AttnParams block_attention(const dflash_dims* d, const dflash_kv_cache* c, int l
   p.pre_M = 0;
   p.lens_out = nullptr;
   p.sched_ready = false;
+  p.block_table = c->block_table;
+  p.pages_per_seq = c->block_table ? c->capacity / 128 : 0;
+  p.n_pages = c->n_pages;
   return p;
 }
 
@@ -329,6 +349,8 @@ dflash_status check_inject(const dflash_dims* d, const dflash_kv_cache* c, int l
   dflash_status st = check_dims(d);
   if (st != DFLASH_OK) return st;
   st = check_cache(c, layer);
+  if (st != DFLASH_OK) return st;
+  st = check_layout(d, c);
   if (st != DFLASH_OK) return st;
   if (M < 0 || table_len < 0) return DFLASH_ERR_INVALID_ARG;
   if (M == 0) return DFLASH_OK;
@@ -346,6 +368,8 @@ dflash_status check_block(const dflash_dims* d, const dflash_kv_cache* c, int la
   dflash_status st = check_dims(d);
   if (st != DFLASH_OK) return st;
   st = check_cache(c, layer);
+  if (st != DFLASH_OK) return st;
+  st = check_layout(d, c);
   if (st != DFLASH_OK) return st;
   if (table_len < 0 || window < 0) return DFLASH_ERR_INVALID_ARG;
   if (window > 0 && window < d->block_size) return DFLASH_ERR_INVALID_ARG;

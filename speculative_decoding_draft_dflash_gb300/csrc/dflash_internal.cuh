@@ -132,8 +132,23 @@ struct HeadEpilogue {
   // sequence's block starts after the rows that inject appended (cu_rows, row count)
   const int32_t* pre_rows = nullptr;
   int pre_M = 0;
+  // paged cache: page ids [batch][pages_per_seq] of 128-row pages, or null (contiguous)
+  const int32_t* block_table = nullptr;
+  int pages_per_seq = 0;
 };
 cudaError_t head_epilogue(int dtype, const HeadEpilogue& e, cudaStream_t s);
+
+// Row index (in d_h-wide rows of one layer's K or V) of logical slot `pos` of sequence b,
+// KV head kvh: [b][kvh][capacity] contiguous, or page table[b][pos / 128] of a pool of
+// [n_pages][n_kv][128] rows.
+__device__ __forceinline__ size_t cache_row(const int32_t* table, int pages_per_seq, int n_kv,
+                                            int capacity, int b, int kvh, int pos) {
+  if (table) {
+    const int page = table[(size_t)b * pages_per_seq + (pos >> 7)];
+    return ((size_t)page * n_kv + kvh) * 128 + (pos & 127);
+  }
+  return ((size_t)b * n_kv + kvh) * capacity + pos;
+}
 
 // tcgen05 GEMM with the per-head epilogue fused (bf16, d_h = 128), for shapes
 // that fill the GPU without split-K (gemm_tc_heads_ok): the projection rows go
@@ -203,6 +218,8 @@ struct AttnParams {
   int pre_M;                // them), or null
   int32_t* lens_out;        // receives the lengths after the call (block appended), or null
   bool sched_ready;         // the work list was built by the projection launch
+  const int32_t* block_table;  // paged cache (128-row pages), or null
+  int pages_per_seq, n_pages;
   int batch, n_h, n_kv, d_h, bs, capacity, window, chunk, n_chunks, table_len;
   float scaling;
 };

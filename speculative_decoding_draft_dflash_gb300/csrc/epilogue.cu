@@ -201,7 +201,7 @@ __global__ void head_epilogue_kernel(HeadEpilogue e) {
   } else {
     const int kvh = head - e.n_q - (kind == 2 ? e.n_kv : 0);
     T* base = (T*)(kind == 1 ? e.cache_k : e.cache_v);
-    dst = base + (((size_t)b * e.n_kv + kvh) * e.capacity + pos) * e.d_h;
+    dst = base + cache_row(e.block_table, e.pages_per_seq, e.n_kv, e.capacity, b, kvh, pos) * e.d_h;
   }
   dst[i] = from_f<T>(x0);
   dst[i + half] = from_f<T>(x1);
@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(256) head_epilogue_bf16_kernel(HeadEpilogue e)
   } else {
     const int kvh = head - e.n_q - (kind == 2 ? e.n_kv : 0);
     bf16* base = (bf16*)(kind == 1 ? e.cache_k : e.cache_v);
-    dst = base + (((size_t)b * e.n_kv + kvh) * e.capacity + pos) * 128;
+    dst = base + cache_row(e.block_table, e.pages_per_seq, e.n_kv, e.capacity, b, kvh, pos) * 128;
   }
   __nv_bfloat162 lo2 = __floats2bfloat162_rn(x.x, x.y), hi2 = __floats2bfloat162_rn(x.z, x.w);
   uint2 u;

@@ -98,10 +98,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // table). Status bits as the per-head epilogue kernels set them; `first_tile` marks the
 // tile holding head 0, so each refused sequence is flagged once.
 struct RowSlot {
-  int b, t, pos;
+  int b, t, pos, page;  // page: the slot's page of a paged cache, else -1
 };
 __device__ __forceinline__ RowSlot row_slot(const HeadEpilogue& e, int row, bool first_tile) {
-  RowSlot rs{0, 0, -1};
+  RowSlot rs{0, 0, -1, -1};
   int n_b;
   if (e.cu_rows) {
     int lo = 0, hi = e.batch - 1;
@@ -130,6 +130,7 @@ __device__ __forceinline__ RowSlot row_slot(const HeadEpilogue& e, int row, bool
     return rs;
   }
   rs.pos = start + rs.t;
+  if (e.block_table) rs.page = e.block_table[(size_t)rs.b * e.pages_per_seq + (rs.pos >> 7)];
   return rs;
 }
 
@@ -162,6 +163,8 @@ __device__ __forceinline__ HeadEpilogue pick_epilogue(const TcGemmParams& p, boo
   DFLASH_PICK(status);
   DFLASH_PICK(pre_rows);
   DFLASH_PICK(pre_M);
+  DFLASH_PICK(block_table);
+  DFLASH_PICK(pages_per_seq);
 #undef DFLASH_PICK
   return e;
 }
@@ -308,9 +311,9 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
         }
       }
       if (HEADS) {
-        RowSlot rs{0, 0, -1};
+        RowSlot rs{0, 0, -1, -1};
         if (m0 + row < M) rs = row_slot(ep, m0 + row, n0 == 0);
-        slots[row] = make_int4(rs.b, rs.t, rs.pos, 0);
+        slots[row] = make_int4(rs.b, rs.t, rs.pos, rs.page);
 #pragma unroll
         for (int h = 0; h < NH; ++h) rnorm[row * NH + h] = 1.0f / sqrtf(ss[h] * (1.0f / 128.f) + ep.eps);
       }
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
 #pragma unroll
         for (int i = 0; i < RB; ++i) {
           const int r = r0 + i;
-          rs[i] = r < BM ? slots[r] : make_int4(0, 0, -1, 0);
+          rs[i] = r < BM ? slots[r] : make_int4(0, 0, -1, -1);
           if (m0 + r >= M) rs[i].z = -1;
         }
 #pragma unroll
@@ -396,7 +399,8 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
             const int kvh = head - ep.n_q - (kind == 2 ? ep.n_kv : 0);
             bf16* kvbase = (bf16*)(kind == 1 ? ep.cache_k : ep.cache_v);
             bf16* dst = qh ? (bf16*)ep.q_out + (((size_t)rs[i].x * ep.n_q + head) * ep.bs + rs[i].y) * 128
-                           : kvbase + (((size_t)rs[i].x * ep.n_kv + kvh) * ep.capacity + rs[i].z) * 128;
+                           : kvbase + (rs[i].w >= 0 ? ((size_t)rs[i].w * ep.n_kv + kvh) * 128 + (rs[i].z & 127)
+                                                    : ((size_t)rs[i].x * ep.n_kv + kvh) * ep.capacity + rs[i].z) * 128;
             uint2 w2;
             w2.x = pack_bf16(y0, y1);
             w2.y = pack_bf16(y2, y3);

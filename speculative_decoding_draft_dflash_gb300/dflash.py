@@ -41,7 +41,8 @@ class dflash_dims(ctypes.Structure):
 
 class dflash_kv_cache(ctypes.Structure):
     _fields_ = [("k", c_void_p), ("v", c_void_p), ("lens", c_void_p), ("n_layers", c_int),
-                ("batch", c_int), ("capacity", c_int)]
+                ("batch", c_int), ("capacity", c_int), ("block_table", c_void_p),
+                ("page_size", c_int), ("n_pages", c_int)]
 
 
 def _load():
@@ -129,18 +130,69 @@ def make_dims(d, n_h, n_kv, d_h, k_layers, block_size, eps=1e-6, dtype=DFLASH_BF
 class KVCache:
     """Device buffers of a draft KV cache (allocated by torch) and their C descriptor.
 
-    k, v: [n_layers][batch][n_kv][capacity][d_h]; lens: int32 [n_layers][batch].
+    Contiguous: k, v [n_layers][batch][n_kv][capacity][d_h].
+    Paged (page_table given, or paged=True): k, v [n_layers][n_pages][n_kv][page_size][d_h]
+    and block_table int32 [batch][capacity / page_size]; with paged=True the pages of
+    the sequences are a seeded permutation of the pool (so no page is where a contiguous
+    layout would put it). lens: int32 [n_layers][batch] in both layouts.
     """
 
-    def __init__(self, n_layers, batch, n_kv, capacity, d_h, dtype, device="cuda"):
+    PAGE = 128
+
+    def __init__(self, n_layers, batch, n_kv, capacity, d_h, dtype, device="cuda", paged=False,
+                 page_table=None, n_pages=None, seed=0):
         td = torch_dtype(dtype_code(dtype))
-        shape = (n_layers, batch, n_kv, capacity, d_h)
-        self.k = torch.zeros(shape, dtype=td, device=device)
-        self.v = torch.zeros(shape, dtype=td, device=device)
+        self.n_layers, self.batch, self.capacity, self.n_kv, self.d_h = (
+            n_layers, batch, capacity, n_kv, d_h)
         self.lens = torch.zeros((n_layers, batch), dtype=torch.int32, device=device)
-        self.n_layers, self.batch, self.capacity = n_layers, batch, capacity
-        self.desc = dflash_kv_cache(self.k.data_ptr(), self.v.data_ptr(), self.lens.data_ptr(),
-                                    n_layers, batch, capacity)
+        self.paged = paged or page_table is not None
+        if self.paged:
+            P = self.PAGE
+            assert capacity % P == 0
+            pps = capacity // P
+            if page_table is None:
+                n_pages = n_pages or batch * pps
+                g = torch.Generator().manual_seed(seed)
+                perm = torch.randperm(n_pages, generator=g)[:batch * pps]
+                page_table = perm.view(batch, pps).to(torch.int32)
+            self.block_table = page_table.to(device=device, dtype=torch.int32).contiguous()
+            self.n_pages = n_pages or int(self.block_table.max().item()) + 1
+            shape = (n_layers, self.n_pages, n_kv, P, d_h)
+            self.k = torch.zeros(shape, dtype=td, device=device)
+            self.v = torch.zeros(shape, dtype=td, device=device)
+            self.desc = dflash_kv_cache(self.k.data_ptr(), self.v.data_ptr(), self.lens.data_ptr(),
+                                        n_layers, batch, capacity, self.block_table.data_ptr(),
+                                        P, self.n_pages)
+        else:
+            shape = (n_layers, batch, n_kv, capacity, d_h)
+            self.k = torch.zeros(shape, dtype=td, device=device)
+            self.v = torch.zeros(shape, dtype=td, device=device)
+            self.desc = dflash_kv_cache(self.k.data_ptr(), self.v.data_ptr(), self.lens.data_ptr(),
+                                        n_layers, batch, capacity)
+
+    def _index(self, b, lo, hi):
+        """(pages, rows) of logical slots lo .. hi-1 of sequence b (paged layout)."""
+        s = torch.arange(lo, hi, device=self.block_table.device)
+        return self.block_table[b, s // self.PAGE].long(), s % self.PAGE
+
+    def rows(self, which, layer, b, lo, hi):
+        """Logical rows lo .. hi-1 of sequence b as [n_kv][hi - lo][d_h] (a copy when paged)."""
+        t = self.k if which == "k" else self.v
+        if not self.paged:
+            return t[layer, b, :, lo:hi]
+        pages, r = self._index(b, lo, hi)
+        return t[layer, pages, :, r].permute(1, 0, 2)
+
+    def set_rows(self, layer, b, K, V):
+        """Writes K, V [n_kv][n][d_h] to logical slots 0 .. n-1 of sequence b."""
+        n = K.shape[1]
+        if not self.paged:
+            self.k[layer, b, :, :n] = K
+            self.v[layer, b, :, :n] = V
+            return
+        pages, r = self._index(b, 0, n)
+        self.k[layer, pages, :, r] = K.permute(1, 0, 2).to(self.k.dtype)
+        self.v[layer, pages, :, r] = V.permute(1, 0, 2).to(self.v.dtype)
 
 
 # ---------------------------------------------------------------------------

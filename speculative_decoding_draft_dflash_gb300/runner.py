@@ -41,7 +41,7 @@ class RoundInputs:
 
 class DeviceWorkload:
     def __init__(self, w: synth.Workload, device="cuda", prefill=True, capacity=None,
-                 max_rows=None):
+                 max_rows=None, paged=False):
         self.w = w
         self.device = device
         self.dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
@@ -56,7 +56,11 @@ class DeviceWorkload:
         self.g_k = [dev(synth.gamma_k(w, l)) for l in range(w.n_layers)]
         self.capacity = capacity or w.capacity
         self.table_len = self.capacity
-        self.cache = D.KVCache(w.n_layers, w.batch, w.n_kv, self.capacity, w.d_h, w.dtype, device)
+        if paged:  # whole pages per sequence
+            self.capacity = -(-self.capacity // D.KVCache.PAGE) * D.KVCache.PAGE
+            self.table_len = self.capacity
+        self.cache = D.KVCache(w.n_layers, w.batch, w.n_kv, self.capacity, w.d_h, w.dtype, device,
+                               paged=paged, seed=w.seed)
         self.rope = torch.empty((self.table_len, w.d_h // 2, 2), dtype=torch.float32, device=device)
         D.dflash_rope_table_build(w.theta, w.d_h, self.table_len, self.rope)
         self.L0 = synth.prefill_lens(w)
@@ -92,8 +96,7 @@ class DeviceWorkload:
                 if n == 0:
                     continue
                 K, V = synth.cache_rows(w, l, b, n)
-                self.cache.k[l, b, :, :n] = _dev(K, self.dt, self.device)
-                self.cache.v[l, b, :, :n] = _dev(V, self.dt, self.device)
+                self.cache.set_rows(l, b, _dev(K, self.dt, self.device), _dev(V, self.dt, self.device))
         self.cache.lens.copy_(torch.from_numpy(
             np.tile(self.L0.astype(np.int32), (w.n_layers, 1))).to(self.device))
 

@@ -101,14 +101,14 @@ def oracle_rounds(w: synth.Workload, seqs, rounds=None):
 # device run
 # ---------------------------------------------------------------------------
 
-def device_rounds(w: synth.Workload, seqs, rounds=None, dev=None, fused_layer=True):
+def device_rounds(w: synth.Workload, seqs, rounds=None, dev=None, fused_layer=True, paged=False):
     """Runs the same schedule on the device for all sequences; returns host copies for ``seqs``."""
     import torch
     from speculative_decoding_draft_dflash_gb300 import dflash as D
     from speculative_decoding_draft_dflash_gb300.runner import DeviceWorkload
 
     rounds = rounds or w.rounds
-    dev = dev or DeviceWorkload(w)
+    dev = dev or DeviceWorkload(w, paged=paged)
     assert D.dflash_status_get() == 0
     results = []
     lens = synth.prefill_lens(w).copy()
@@ -127,8 +127,8 @@ def device_rounds(w: synth.Workload, seqs, rounds=None, dev=None, fused_layer=Tr
         for l in range(w.n_layers):
             o = dev.out[l].float().cpu().numpy()
             res["out"].append({b: o[b] for b in seqs})
-            res["rows"].append({b: (dev.cache.k[l, b, :, lens[b]:lens_block[l, b]].float().cpu().numpy(),
-                                    dev.cache.v[l, b, :, lens[b]:lens_block[l, b]].float().cpu().numpy())
+            res["rows"].append({b: (dev.cache.rows("k", l, b, lens[b], lens_block[l, b]).float().cpu().numpy(),
+                                    dev.cache.rows("v", l, b, lens[b], lens_block[l, b]).float().cpu().numpy())
                                 for b in seqs})
             res["lens_block"].append({b: int(lens_block[l, b]) for b in seqs})
         res["lens_block_all"] = lens_block

@@ -186,3 +186,23 @@ def test_layer_out_arguments_rejected_before_launch(D, lib):
     n.restype = ctypes.c_int
     assert n(ctypes.byref(dims), 4, None, P(256), P(512), None) == 1
     assert n(ctypes.byref(dims), -1, P(256), P(256), P(512), None) == 1
+
+
+def test_paged_cache_arguments_rejected(D, lib):
+    f = lib.dflash_kv_inject
+    f.restype = ctypes.c_int
+    P = ctypes.c_void_p
+    dims = _dims(D)
+    def call(cache, dm=dims):
+        return f(ctypes.byref(dm), ctypes.byref(cache), 0, P(256), P(512), 16, P(768), P(1024),
+                 P(1280), P(1536), 64, P(2048), ctypes.c_size_t(100), None)
+    bad_page = D.dflash_kv_cache(256, 512, 1024, 2, 4, 256, P(4096), 64, 8)
+    assert call(bad_page) == 1                      # pages must be 128 rows
+    bad_cap = D.dflash_kv_cache(256, 512, 1024, 2, 4, 200, P(4096), 128, 8)
+    assert call(bad_cap) == 1                       # capacity in whole pages
+    no_pages = D.dflash_kv_cache(256, 512, 1024, 2, 4, 256, P(4096), 128, 0)
+    assert call(no_pages) == 1
+    f32 = _dims(D, dtype=D.DFLASH_F32, d=512, n_h=8, n_kv=8, d_h=64)
+    paged = D.dflash_kv_cache(256, 512, 1024, 2, 4, 256, P(4096), 128, 8)
+    assert call(paged, f32) == 2                    # paged layout: bf16 path only
+    assert call(paged) == 3                         # valid paged cache, 100-byte workspace

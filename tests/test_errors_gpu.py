@@ -111,7 +111,7 @@ def test_ragged_inject_with_empty_sequences():
         K, V = O.kv_project(Cref[cu[b]:cu[b + 1]], synth.W_K(w, 0), synth.W_V(w, 0),
                             synth.gamma_k(w, 0), w.n_kv, w.d_h, w.eps,
                             L0[b] + np.arange(counts[b]), w.theta)
-        gk = dev.cache.k[0, b, :, L0[b]:L0[b] + counts[b]].float().cpu().numpy()
-        gv = dev.cache.v[0, b, :, L0[b]:L0[b] + counts[b]].float().cpu().numpy()
+        gk = dev.cache.rows("k", 0, b, L0[b], L0[b] + counts[b]).float().cpu().numpy()
+        gv = dev.cache.rows("v", 0, b, L0[b], L0[b] + counts[b]).float().cpu().numpy()
         harness.check_close(gk, K, w.dtype, f"K seq {b}")
         harness.check_close(gv, V, w.dtype, f"V seq {b}")

@@ -38,8 +38,8 @@ SMALL = {
 }
 
 
-def _run(w, seqs, fused_layer=True):
-    dev_res, dev = harness.device_rounds(w, seqs, fused_layer=fused_layer)
+def _run(w, seqs, fused_layer=True, paged=False):
+    dev_res, dev = harness.device_rounds(w, seqs, fused_layer=fused_layer, paged=paged)
     ora_res = harness.oracle_rounds(w, seqs)
     return harness.compare(w, dev_res, ora_res, seqs)
 
@@ -54,6 +54,13 @@ def test_walkthrough_f32():
 def test_small_workloads(name, layer_mode):
     w = SMALL[name]
     _run(w, list(range(w.batch)), fused_layer=layer_mode)
+
+
+@pytest.mark.parametrize("name", sorted(n for n in SMALL if SMALL[n].dtype == "bf16"))
+def test_small_workloads_paged(name, layer_mode):
+    """The same schedules on a paged cache: 128-row pages in a seeded permutation."""
+    w = SMALL[name]
+    _run(w, list(range(w.batch)), fused_layer=layer_mode, paged=True)
 
 
 def _sample(w, n, seed=11):
@@ -71,3 +78,10 @@ def _sample(w, n, seed=11):
 def test_full_size(name, n):
     w = W[name]
     _run(w, _sample(w, n))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,n", [("serve_b32", 3), ("hybrid_swa_b64", 2)])
+def test_full_size_paged(name, n):
+    w = W[name]
+    _run(w, _sample(w, n, seed=12), paged=True)
