@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch every call eagerly")
     ap.add_argument("--paged", action="store_true", help="paged KV cache (128-row pages)")
+    ap.add_argument("--round-only", action="store_true",
+                    help="skip the extra measurements (prefill GEMMs, bookkeeping, layer output)")
     return ap.parse_args()
 
 
@@ -382,9 +384,10 @@ def run_ours(args, w):
     dominant = max(kernels, key=lambda k: kernels[k]["share_of_step"] * (k in costs or k == "attention"))
     roofline = rf(dominant)
     others = {k: rf(k) for k in kernels if k != dominant and (k in costs or k == "attention")}
-    prefill = run_prefill_gemms(args, w, dev, stream, D, pk) if w.prefill_inject else None
-    bookkeeping = time_accept(args, w, stream, D)
-    layer_rest = time_layer_out(args, w, stream, D, pk) if w.dtype == "bf16" else None
+    extras = not args.round_only
+    prefill = run_prefill_gemms(args, w, dev, stream, D, pk) if w.prefill_inject and extras else None
+    bookkeeping = time_accept(args, w, stream, D) if extras else None
+    layer_rest = time_layer_out(args, w, stream, D, pk) if w.dtype == "bf16" and extras else None
 
     # ---- end to end: host inputs in, host results out, through the same calls ----
     e2e = run_e2e(args, w, dev, x, stream, D)
@@ -403,7 +406,8 @@ def run_ours(args, w):
                       "eager launches; kernel durations from a second traced pass"}
     if prefill is not None:
         line["prefill_gemms"] = prefill
-    line["bookkeeping"] = bookkeeping
+    if bookkeeping is not None:
+        line["bookkeeping"] = bookkeeping
     if layer_rest is not None:
         line["layer_output"] = layer_rest
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
