@@ -29,10 +29,15 @@ closed forms, library routines, brute force and the integer examples the
 walkthrough prints. Two readings stay "parity unpinned" by the pages: the
 rotate-half pairing (the pages' invariants hold for any pairing) and the edge
 keys of the sliding window. The element values of the walkthrough example are
-unpinned too: the page prints shapes only.
+unpinned too: the page prints shapes only. The fp8 cache format (E4M3, one scale
+per layer for K and for V) is a reading of a passage that names fp8 without
+fixing a format; the quantiser itself is pinned against a library conversion and
+closed-form codes.
 """
 
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -285,6 +290,60 @@ def layer_output(x, attn_out, W_O, gamma_post, W_gate, W_up, W_down, eps):
 
 
 # ---------------------------------------------------------------------------
+# fp8 (E4M3) cache storage
+# ---------------------------------------------------------------------------
+# KV Cache + Speculative Decoding Interview Cheat Sheet, section 2.1 (an fp8 cache
+# element takes one byte) and section 4.5 (KV quantisation, FP8 among the routes).
+# The pages fix neither the fp8 format nor the scaling, so the reading taken is the
+# plainest one: the E4M3 format without infinities (1 sign bit, 4 exponent bits with
+# bias 7, 3 mantissa bits; exponent and mantissa all ones is NaN, so the largest
+# finite value is 448), one scale per layer for K and one for V, the stored code is
+# x / scale rounded to the nearest finite value (ties to the even code, magnitudes
+# beyond 448 saturate to 448), and a cached element reads back as scale * value.
+
+def e4m3_value(code):
+    """Value of one E4M3 code (0..255), from its bit fields."""
+    code = int(code)
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 0x7
+    if e == 15 and m == 7:
+        return math.nan
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** (1 - 7)        # subnormal
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+# the 127 finite non-negative values, code 0 .. 126 (increasing with the code)
+_E4M3_POS = np.array([e4m3_value(c) for c in range(127)], dtype=F64)
+
+
+def e4m3_quantize(x):
+    """Codes (uint8) of x: nearest finite E4M3 value, ties to the even code, saturating."""
+    x = np.asarray(x, dtype=F64)
+    a = np.abs(x).ravel()
+    hi = np.clip(np.searchsorted(_E4M3_POS, a), 1, 126)   # first value >= a (clamped)
+    lo = hi - 1
+    d_lo, d_hi = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(a >= _E4M3_POS[126], 126, code)          # saturate at 448
+    code = code | np.where(np.signbit(x.ravel()), 0x80, 0)
+    code = np.where(np.isnan(a), 0x7F, code)
+    return code.astype(np.uint8).reshape(x.shape)
+
+
+def e4m3_dequantize(codes):
+    """Values of E4M3 codes."""
+    table = np.array([e4m3_value(c) for c in range(256)], dtype=F64)
+    return table[np.asarray(codes, dtype=np.int64)]
+
+
+def fp8_store(x, scale):
+    """What an fp8 cache holds for x: scale * value(code(x / scale))."""
+    return scale * e4m3_dequantize(e4m3_quantize(np.asarray(x, dtype=F64) / scale))
+
+
+# ---------------------------------------------------------------------------
 # The draft KV cache and the four calls of the step (Steps 4.2-4.4, 7)
 # ---------------------------------------------------------------------------
 
@@ -296,14 +355,26 @@ class DraftKVCache:
     Injection Walkthrough, Step 7: the cache grows round by round. Slot j of
     a sequence holds the row at absolute position j. ``capacity`` (optional)
     mirrors a fixed-size device cache: an append beyond it is refused.
+    ``fp8_scales`` (optional) = (k_scales, v_scales), one per layer: the cache
+    then stores rows as an E4M3 cache does (``fp8_store``); ``kraw`` / ``vraw``
+    keep the rows before quantisation.
     """
 
-    def __init__(self, n_layers, batch, n_kv, d_h, capacity=None):
+    def __init__(self, n_layers, batch, n_kv, d_h, capacity=None, fp8_scales=None):
         self.n_layers, self.batch, self.n_kv, self.d_h = n_layers, batch, n_kv, d_h
         self.capacity = capacity
+        self.fp8_scales = fp8_scales
         self.k = [[np.zeros((n_kv, 0, d_h)) for _ in range(batch)] for _ in range(n_layers)]
         self.v = [[np.zeros((n_kv, 0, d_h)) for _ in range(batch)] for _ in range(n_layers)]
+        self.kraw = [[np.zeros((n_kv, 0, d_h)) for _ in range(batch)] for _ in range(n_layers)]
+        self.vraw = [[np.zeros((n_kv, 0, d_h)) for _ in range(batch)] for _ in range(n_layers)]
         self.errors = 0
+
+    def _stored(self, layer, K, V):
+        K, V = np.asarray(K, dtype=F64), np.asarray(V, dtype=F64)
+        if self.fp8_scales is None:
+            return K, V
+        return (fp8_store(K, self.fp8_scales[0][layer]), fp8_store(V, self.fp8_scales[1][layer]))
 
     def length(self, layer, b):
         return self.k[layer][b].shape[1]
@@ -315,8 +386,9 @@ class DraftKVCache:
 
     def set_rows(self, layer, b, K, V):
         """Replace the cached rows of one sequence (used to seed a pre-filled cache)."""
-        self.k[layer][b] = np.asarray(K, dtype=F64).copy()
-        self.v[layer][b] = np.asarray(V, dtype=F64).copy()
+        self.kraw[layer][b] = np.asarray(K, dtype=F64).copy()
+        self.vraw[layer][b] = np.asarray(V, dtype=F64).copy()
+        self.k[layer][b], self.v[layer][b] = self._stored(layer, K, V)
 
     def append(self, layer, b, K, V):
         """Append rows [n_kv, n, d_h]; refused (error counted) beyond capacity."""
@@ -324,8 +396,11 @@ class DraftKVCache:
         if self.capacity is not None and self.length(layer, b) + n > self.capacity:
             self.errors += 1
             return False
-        self.k[layer][b] = np.concatenate([self.k[layer][b], K], axis=1)
-        self.v[layer][b] = np.concatenate([self.v[layer][b], V], axis=1)
+        Ks, Vs = self._stored(layer, K, V)
+        self.k[layer][b] = np.concatenate([self.k[layer][b], Ks], axis=1)
+        self.v[layer][b] = np.concatenate([self.v[layer][b], Vs], axis=1)
+        self.kraw[layer][b] = np.concatenate([self.kraw[layer][b], K], axis=1)
+        self.vraw[layer][b] = np.concatenate([self.vraw[layer][b], V], axis=1)
         return True
 
     def crop(self, new_lens):
@@ -341,8 +416,8 @@ class DraftKVCache:
                 if n < 0 or n > self.length(l, b):
                     self.errors += 1
                     continue
-                self.k[l][b] = self.k[l][b][:, :n]
-                self.v[l][b] = self.v[l][b][:, :n]
+                for rows in (self.k, self.v, self.kraw, self.vraw):
+                    rows[l][b] = rows[l][b][:, :n]
 
 
 def kv_inject(cache, layer, C, cu_rows, W_K, W_V, gamma_k, n_kv, d_h, eps, theta):

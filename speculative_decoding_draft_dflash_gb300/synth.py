@@ -66,6 +66,7 @@ class Workload:
     random_gamma: bool = False
     description: str = ""
     d_ff: int = 0          # MLP width of the rest of the decoder layer; 0 = 3 * d
+    kv: str = "bf16"       # cache element type: the storage type, or "fp8" (E4M3 codes)
 
     @property
     def ffn(self):
@@ -288,6 +289,14 @@ def block_embeddings(w: Workload, rnd: int, layer: int, b: int = None):
         return _normal(w, (w.bs, w.d), 1.0, _T_BLOCK, rnd, layer, b)
     return np.stack([_normal(w, (w.bs, w.d), 1.0, _T_BLOCK, rnd, layer, bb)
                      for bb in range(w.batch)], axis=0)
+
+
+def kv_scales(w: Workload):
+    """Per-layer (k_scales, v_scales) of an fp8 cache: fixed calibration constants that put
+    the synthetic K (unit RMS) and V (RMS about 1.3) well inside the E4M3 range."""
+    k = np.array([0.25 * (1 + 0.5 * l) for l in range(w.n_layers)], dtype=np.float64)
+    v = np.array([0.125 * (1 + 0.25 * l) for l in range(w.n_layers)], dtype=np.float64)
+    return k, v
 
 
 def cache_rows(w: Workload, layer: int, b: int, n: int = None):

@@ -49,7 +49,8 @@ def oracle_rounds(w: synth.Workload, seqs, rounds=None):
     rounds = rounds or w.rounds
     S = list(seqs)
     L0 = synth.prefill_lens(w)
-    cache = O.DraftKVCache(w.n_layers, len(S), w.n_kv, w.d_h, capacity=w.capacity)
+    cache = O.DraftKVCache(w.n_layers, len(S), w.n_kv, w.d_h, capacity=w.capacity,
+                           fp8_scales=synth.kv_scales(w) if w.kv == "fp8" else None)
     W_fc = synth.W_fc(w)
     g_h = synth.gamma_h(w)
     Wq = [synth.W_Q(w, l) for l in range(w.n_layers)]
@@ -89,6 +90,9 @@ def oracle_rounds(w: synth.Workload, seqs, rounds=None):
             lo = before
             res["rows"].append({b: (cache.k[l][i][:, lo[i]:], cache.v[l][i][:, lo[i]:])
                                 for i, b in enumerate(S)})
+            res.setdefault("rows_raw", []).append(
+                {b: (cache.kraw[l][i][:, lo[i]:], cache.vraw[l][i][:, lo[i]:])
+                 for i, b in enumerate(S)})
             res["lens_block"].append({b: int(cache.lens[l][i]) for i, b in enumerate(S)})
         O.cache_crop(cache, before + np.array([counts[b] for b in S]))
         res["lens_crop"] = {b: int(cache.lens[0][i]) for i, b in enumerate(S)}

@@ -435,4 +435,85 @@ def pin_layer_output_residuals(O):
     np.testing.assert_allclose(O.layer_output(x, att, WO, g, Wg, Wu, Wd, 1e-6), want, rtol=1e-12)
 
 
+# ---------------------------------------------------------------------------
+# fp8 (E4M3) cache storage
+# ---------------------------------------------------------------------------
+
+def _e4m3_sample():
+    """float32 values inside the finite E4M3 range: every code value, every midpoint
+    between neighbouring codes, and log-uniform random magnitudes, both signs."""
+    pos = np.array(_E4M3_FROM_BITS, dtype=np.float64)
+    mids = (pos[1:] + pos[:-1]) / 2
+    rng = np.random.default_rng(41)
+    rnd = np.exp2(rng.uniform(-12, np.log2(448.0), 4000))
+    a = np.concatenate([pos, mids, rnd, [448.0]])
+    a = np.concatenate([a, -a]).astype(np.float32)
+    return a
+
+
+# finite non-negative E4M3 values written out from the format (sign 0, exponent e with
+# bias 7, mantissa m): subnormals m * 2^-9, normals (1 + m/8) * 2^(e-7), up to 448
+_E4M3_FROM_BITS = [m * 2.0 ** -9 for m in range(8)] + \
+    [(1 + m / 8) * 2.0 ** (e - 7) for e in range(1, 16) for m in range(8) if not (e == 15 and m == 7)]
+
+
+def pin_e4m3_matches_torch(O):
+    """Round-trip through the quantiser = torch's float8_e4m3fn conversion (in range)."""
+    a = _e4m3_sample()
+    want = torch.from_numpy(a).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_dequantize(O.e4m3_quantize(a.astype(np.float64)))
+    np.testing.assert_array_equal(got, want)
+
+
+def pin_e4m3_codes_closed_form(O):
+    """Codes fixed by the format: ones, extremes, subnormal ties, saturation, NaN."""
+    cases = {1.0: 0x38, -1.0: 0xB8, 448.0: 0x7E, 500.0: 0x7E, -1e6: 0xFE, 2.0 ** -6: 0x08,
+             2.0 ** -9: 0x01, 7 * 2.0 ** -9: 0x07, 1.5 * 2.0 ** -9: 0x02, 2.0 ** -10: 0x00,
+             1.0625: 0x38, 1.1875: 0x3A, 0.0: 0x00, 240.0: 0x77}
+    got = O.e4m3_quantize(np.array(list(cases), dtype=np.float64))
+    assert got.tolist() == list(cases.values()), got.tolist()
+    assert O.e4m3_quantize(np.array([np.nan]))[0] & 0x7F == 0x7F
+    vals = O.e4m3_dequantize(np.arange(256))
+    assert np.isnan(vals[0x7F]) and np.isnan(vals[0xFF])
+    np.testing.assert_array_equal(vals[:0x7F], _E4M3_FROM_BITS)
+    np.testing.assert_array_equal(vals[0x80:0xFF], -np.array(_E4M3_FROM_BITS))
+    # every finite code is a fixed point of value -> code
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    np.testing.assert_array_equal(O.e4m3_quantize(O.e4m3_dequantize(codes)), codes)
+
+
+def pin_e4m3_error_bound(O):
+    """|x - value(code(x))| <= half the code spacing at x (2^-4 relative for normals)."""
+    rng = np.random.default_rng(43)
+    x = np.exp2(rng.uniform(-11, 8.8, 20000)) * rng.choice([-1, 1], 20000)
+    err = np.abs(x - O.e4m3_dequantize(O.e4m3_quantize(x)))
+    e = np.floor(np.log2(np.abs(x)))
+    spacing = np.where(e < -6, 2.0 ** -9, 2.0 ** (np.minimum(e, 8) - 3))
+    assert np.all(err <= spacing / 2 + 1e-300), float((err / spacing).max())
+
+
+def pin_fp8_cache_scale(O):
+    """A power-of-two scale leaves normal-range rows unchanged (exponent shift only), and
+    the cache holds scale * value: scales (2, 1/2) store what scales (1, 1) store."""
+    rng = np.random.default_rng(47)
+    K = np.exp2(rng.uniform(-3, 5, (2, 9, 8))) * rng.choice([-1, 1], (2, 9, 8))
+    V = np.exp2(rng.uniform(-3, 5, (2, 9, 8))) * rng.choice([-1, 1], (2, 9, 8))
+    c1 = O.DraftKVCache(1, 1, 2, 8, fp8_scales=([1.0], [1.0]))
+    c2 = O.DraftKVCache(1, 1, 2, 8, fp8_scales=([2.0], [0.5]))
+    c1.append(0, 0, K, V)
+    c2.append(0, 0, K, V)
+    np.testing.assert_array_equal(c2.k[0][0], c1.k[0][0])
+    np.testing.assert_array_equal(c2.v[0][0], c1.v[0][0])
+    np.testing.assert_array_equal(c2.kraw[0][0], K)
+    # relative error of a stored element is at most 2^-4 in the normal range
+    assert np.all(np.abs(c1.k[0][0] - K) <= np.abs(K) * 2.0 ** -4)
+    # a non-power-of-two scale: stored = s * value(code(x / s)), and crop cuts the raw rows too
+    c3 = O.DraftKVCache(1, 1, 2, 8, fp8_scales=([0.3], [3.0]))
+    c3.append(0, 0, K, V)
+    q = O.e4m3_quantize(K / 0.3)
+    np.testing.assert_allclose(c3.k[0][0], 0.3 * O.e4m3_dequantize(q), rtol=1e-15)
+    c3.crop([4])
+    assert c3.k[0][0].shape[1] == c3.kraw[0][0].shape[1] == c3.vraw[0][0].shape[1] == 4
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

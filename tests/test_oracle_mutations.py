@@ -125,7 +125,38 @@ def _layer_norm_before_residual(x, attn_out, W_O, gamma_post, W_gate, W_up, W_do
     return x1 + O.mlp(O.rms_norm(x, gamma_post, eps), W_gate, W_up, W_down)
 
 
-_ORIG = {n: getattr(O, n) for n in ("attention_weights", "attention", "q_project", "kv_project",
+def _e4m3_ties_away(x):
+    x = np.asarray(x, np.float64)
+    codes = _ORIG["e4m3_quantize"](x)
+    vals = O.e4m3_dequantize(codes)
+    up = _ORIG["e4m3_quantize"](np.nextafter(np.abs(x), np.inf) * np.sign(x))
+    tie = np.abs(np.abs(x) - np.abs(vals)) == np.abs(np.abs(O.e4m3_dequantize(up)) - np.abs(x))
+    return np.where(tie & (up != codes), up, codes).astype(np.uint8)
+
+
+def _e4m3_truncates(x):
+    x = np.asarray(x, np.float64)
+    codes = _ORIG["e4m3_quantize"](x)
+    over = np.abs(O.e4m3_dequantize(codes)) > np.abs(x)
+    return np.where(over & ((codes & 0x7F) > 0), codes - 1, codes).astype(np.uint8)
+
+
+def _e4m3_no_saturation(x):
+    x = np.asarray(x, np.float64)
+    codes = _ORIG["e4m3_quantize"](x)
+    return np.where(np.abs(x) > 448.0, 0x7F, codes).astype(np.uint8)
+
+
+def _e4m3_bias_8(code):
+    v = _ORIG["e4m3_value"](code)
+    return v / 2.0
+
+
+def _fp8_store_drops_scale(x, scale):
+    return O.e4m3_dequantize(O.e4m3_quantize(np.asarray(x, np.float64) / scale))
+
+
+_ORIG = {n: getattr(O, n) for n in ("e4m3_quantize", "e4m3_value", "attention_weights", "attention", "q_project", "kv_project",
                                     "round_bookkeeping")}
 
 MUTATIONS = {
@@ -151,6 +182,11 @@ MUTATIONS = {
     "o_proj_untransposed": ("o_proj", _o_proj_untransposed),
     "mlp_silu_on_up_branch": ("mlp", _mlp_silu_on_up),
     "post_norm_before_residual": ("layer_output", _layer_norm_before_residual),
+    "e4m3_ties_away_from_zero": ("e4m3_quantize", _e4m3_ties_away),
+    "e4m3_rounds_toward_zero": ("e4m3_quantize", _e4m3_truncates),
+    "e4m3_overflow_to_nan": ("e4m3_quantize", _e4m3_no_saturation),
+    "e4m3_exponent_bias_8": ("e4m3_value", _e4m3_bias_8),
+    "fp8_store_drops_scale": ("fp8_store", _fp8_store_drops_scale),
 }
 
 
