@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch every call eagerly")
     ap.add_argument("--paged", action="store_true", help="paged KV cache (128-row pages)")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="cache element type: bf16, or fp8 (E4M3 codes, per-layer scales)")
     ap.add_argument("--round-only", action="store_true",
                     help="skip the extra measurements (prefill GEMMs, bookkeeping, layer output)")
     return ap.parse_args()
@@ -130,17 +132,20 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def attention_bytes(w, starts, window=0):
-    """K/V rows read + Q read + output written, per layer launch (bf16).
+    """K/V rows read + Q read + output written, per layer launch (bf16 Q and output;
+    K/V bf16, or one byte per element for an fp8 cache, whose Q is two bytes per
+    element as well: the codes and the remainder codes).
 
     Keys read per sequence: [max(0, start - W + 1), start + bs) with a sliding
     window W, else [0, start + bs).
     """
     e = 2
+    ekv = 1 if w.kv == "fp8" else 2
     rows = 0
     for s in starts:
         lo = max(0, int(s) - window + 1) if window > 0 else 0
         rows += int(s) + w.bs - lo
-    kv = rows * w.n_kv * w.d_h * 2 * e
+    kv = rows * w.n_kv * w.d_h * 2 * ekv
     q = w.batch * w.n_h * w.bs * w.d_h * e
     out = w.batch * w.bs * w.n_h * w.d_h * e
     return int(kv + q + out)
@@ -151,12 +156,19 @@ def mean_attention_bytes(w, starts):
     return int(sum(attention_bytes(w, starts, win) for win in w.windows) / len(w.windows))
 
 
+TRAFFIC_RUN = None  # workload / cache element type / layout of this run
+
+
 def measured_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this run's
+    workload, cache element type and layout, and the kernel source is unchanged."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic_serve_b32.json")) as f:
-            t = json.load(f)[kernel]
+            rec = json.load(f)
+        if rec.get("run") != TRAFFIC_RUN:
+            return None
+        t = rec[kernel]
         with open(os.path.join(ROOT, t["source"]), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest()[:16] != t["sha256_16"]:
                 return None
@@ -194,7 +206,8 @@ def oracle_sample_rate(w, budget_s=12.0, max_steps=None):
     total = 0.0
     b = 0
     while (max_steps is None and total < budget_s) or (max_steps is not None and len(steps) < max_steps):
-        cache = O.DraftKVCache(w.n_layers, 1, w.n_kv, w.d_h)
+        cache = O.DraftKVCache(w.n_layers, 1, w.n_kv, w.d_h,
+                               fp8_scales=synth.kv_scales(w) if w.kv == "fp8" else None)
         for l in range(w.n_layers):
             K, V = synth.cache_rows(w, l, b, int(L0[b]))
             cache.set_rows(l, 0, K, V)
@@ -257,6 +270,8 @@ def config_of(w):
            "new_context_rows": w.new_ctx, "block_size": w.bs, "draft_layers": w.n_layers,
            "d": w.d, "n_h": w.n_h, "n_kv": w.n_kv, "d_h": w.d_h, "k_target_layers": w.k,
            "windows": list(w.windows)}
+    if w.kv == "fp8":
+        cfg["kv_cache"] = "fp8 E4M3 codes, one scale per layer for K and for V"
     mb = step_bytes(w, starts) / 1e6
     cfg["l2"] = (f"inputs larger than L2: every step reads the KV cache rows and the weights, "
                  f"{mb:.0f} MB in all, over the 129 MB L2" if mb > 129 else
@@ -718,6 +733,10 @@ def main():
     args = parse()
     from speculative_decoding_draft_dflash_gb300 import synth
     w = synth.WORKLOADS[args.workload]
+    if args.kv == "fp8":
+        w = w.replace(kv="fp8")
+    global TRAFFIC_RUN
+    TRAFFIC_RUN = f"{w.name}/{w.kv}/{'paged' if args.paged else 'contiguous'}"
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -50,7 +50,8 @@ typedef enum {
   DFLASH_ERR_DEVICE = 5        /* dflash_status_get: the device status word is non-zero */
 } dflash_status;
 
-typedef enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 } dflash_dtype;
+/* DFLASH_FP8_E4M3 is a cache element type only (dflash_kv_cache.kv_dtype). */
+typedef enum { DFLASH_F32 = 0, DFLASH_BF16 = 1, DFLASH_FP8_E4M3 = 2 } dflash_dtype;
 
 /* Bits of the device status word (dflash_status_get). */
 #define DFLASH_DEV_CAPACITY  1u  /* append beyond the cache capacity: sequence skipped */
@@ -94,9 +95,19 @@ typedef struct {
  *   capacity  logical rows per sequence (paged: a multiple of page_size)
  *   block_table  device int32 [batch][capacity / page_size] page ids in [0, n_pages),
  *             or NULL; page_size must be 128 (one page is one attention tile)
+ *   kv_dtype  element type of k and v: 0 (the same as dims->dtype), or
+ *             DFLASH_FP8_E4M3 (one byte per element; bf16 dims only, either layout):
+ *             the code of x / scale, rounded to the nearest finite E4M3 value
+ *             (ties to even, magnitudes beyond 448 saturate), which reads back as
+ *             scale * value
+ *   kv_scales fp8 only: HOST float [n_layers][2] = (k_scale, v_scale) per layer,
+ *             each finite and > 0, read when a call is made (a captured graph keeps
+ *             the values of its capture); NULL means 1 everywhere
  * (DFlash source guide (II), part 4: the DynamicCache that update() appends
  * to and crop(start) truncates. A paged cache holds the same logical rows; the
- * caller owns the page allocation, lengths and crops stay logical.)
+ * caller owns the page allocation, lengths and crops stay logical. KV Cache +
+ * Speculative Decoding Interview Cheat Sheet, sections 2.1 and 4.5: an fp8 cache
+ * element is one byte, half the bytes the attention streams.)
  */
 typedef struct {
   void* k;
@@ -105,6 +116,8 @@ typedef struct {
   int n_layers, batch, capacity;
   const int32_t* block_table;
   int page_size, n_pages;
+  int kv_dtype;
+  const float* kv_scales;
 } dflash_kv_cache;
 
 /*

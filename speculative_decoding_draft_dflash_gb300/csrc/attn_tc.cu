@@ -1,4 +1,4 @@
-// Block attention on tcgen05 tensor cores (bf16 path).
+// Block attention on tcgen05 tensor cores (bf16 path; bf16 or E4M3 cache).
 //
 // The R = G * bs block queries that share one KV head (G query heads x bs
 // block positions, at most 128) form the rows of one M=128 MMA tile, so every
@@ -27,6 +27,16 @@
 //   10         TMA: V tiles (released later than K, so on their own thread).
 // O is rescaled in TMEM only when a row's running maximum grows by more than
 // 2^8, so almost every tile skips it.
+//
+// fp8 (E4M3) cache (KV Cache + Speculative Decoding Interview Cheat Sheet,
+// sections 2.1 and 4.5: one byte per cached element): the MMAs run as
+// kind::f8f6f4 on the cached codes directly, so a tile is half the bytes of a
+// bf16 one. Q and P carry about bf16 precision as two E4M3 terms each, the
+// codes and the codes of the remainder (x ~ hi + lo), so S = Q_hi K^T + Q_lo K^T
+// and O += P_hi V + P_lo V: twice the MMAs of half the width, the same tensor
+// time as bf16. P is formed as 64 p with p <= 4 (rescale threshold 2^2), which
+// keeps it inside E4M3's range and its small values normal. The K scale folds
+// into the score scale and the V scale into the output.
 #include <float.h>
 
 #include <mutex>
@@ -38,35 +48,56 @@ namespace dflash {
 namespace {
 
 constexpr int TK = 128;                    // keys per tile
-constexpr uint32_t TILE = 128 * 128 * 2;   // 32 KB: one K or V tile (128 keys x 128 dims)
+constexpr uint32_t TILE = 128 * 128 * 2;   // 32 KB: one bf16 K or V tile (128 keys x 128 dims)
 constexpr uint32_t HALF = TILE / 2;        // one 64-column swizzled box
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
 constexpr int WARP_KQ = 8, WARP_MMA = 9, WARP_V = 10;
 constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 384;  // TMEM columns: S[2], O, P[2] (64 each)
-constexpr float kRescaleLog2 = 8.0f;
 constexpr int kRing = 4;                   // item ring slots
 
-// Shared-memory plan. NARROW (R <= 64): query rows 64-127 of an A tile are
-// padding, so the two Q buffers interleave (each only needs its rows 0-63 to
-// be its own) and K gets a third stage: a K tile must land before its S MMA,
-// which runs two tiles ahead of the PV MMA, so K loads need the longer lead.
-// WIDE (R > 64): plain double buffers.
-template <bool NARROW>
+// Shared-memory plan. bf16, NARROW (R <= 64): query rows 64-127 of an A tile are
+// padding, so the two Q buffers interleave (each only needs its rows 0-63 to be its
+// own) and K gets a third stage: a K tile must land before its S MMA, which runs two
+// tiles ahead of the PV MMA, so K loads need the longer lead. bf16, WIDE (R > 64):
+// plain double buffers.
+// fp8 (E4M3 cache): K / V tiles are 16 KB (one 128-byte row per key), so there is
+// room for four K and three V stages. A Q buffer holds the code rows of Q, then the
+// remainder-code rows (R rows of 128 B each, padded to 64 or 128); the S MMA reads
+// 128 rows from either, and a NARROW buffer's rows 64-127 fall on what follows it
+// (an 8 KB pad after the last one).
+template <bool NARROW, bool FP8>
 struct Plan {
-  static constexpr int K_STAGES = NARROW ? 3 : 2;
-  static constexpr int V_STAGES = 2;
-  static constexpr uint32_t Q_BYTES = NARROW ? 40960 : 2 * TILE;
+  static constexpr uint32_t TILE_B = FP8 ? TK * 128 : TILE;  // one K or V tile
+  static constexpr int K_STAGES = FP8 ? 4 : (NARROW ? 3 : 2);
+  static constexpr int V_STAGES = FP8 ? 3 : 2;
+  static constexpr uint32_t QPART = NARROW ? 8192 : 16384;   // fp8: code rows of one buffer
+  static constexpr uint32_t Q_BYTES = FP8 ? (NARROW ? 4 * QPART + 8192 : 4 * QPART)
+                                          : (NARROW ? 40960 : 2 * TILE);
+  static constexpr uint32_t Q_TX = FP8 ? 2 * QPART : (NARROW ? TILE / 2 : TILE);  // per Q load
   static constexpr uint32_t OFF_K = Q_BYTES;
-  static constexpr uint32_t OFF_V = OFF_K + K_STAGES * TILE;
-  static constexpr uint32_t OFF_BAR = OFF_V + V_STAGES * TILE;
-  static constexpr size_t SMEM = 1024 + OFF_BAR + 512;
-  __device__ static uint32_t q_base(int buf) { return NARROW ? buf * 8192u : buf * TILE; }
+  static constexpr uint32_t OFF_V = OFF_K + K_STAGES * TILE_B;
+  static constexpr uint32_t OFF_BAR = OFF_V + V_STAGES * TILE_B;
+  // mbarrier slots
+  static constexpr int B_QF = 0, B_QE = 2, B_KF = 4, B_KE = B_KF + K_STAGES;
+  static constexpr int B_VF = B_KE + K_STAGES, B_VE = B_VF + V_STAGES;
+  static constexpr int B_SF = B_VE + V_STAGES, B_SE = B_SF + 2, B_P = B_SE + 2, B_PV = B_P + 1;
+  static constexpr int B_ITF = B_PV + 2, B_ITE = B_ITF + kRing, B_FIN = B_ITE + kRing;
+  static constexpr int N_BARS = B_FIN + 1;
+  static constexpr uint32_t OFF_RING = OFF_BAR + ((8 * N_BARS + 15) & ~15);
+  static constexpr size_t SMEM = 1024 + OFF_RING + 16 * kRing;
+  // O is rescaled only when a row's running maximum grows by more than 2^this. fp8:
+  // P is stored as 64 p, and p <= 4 keeps 64 p inside E4M3's range (448).
+  static constexpr float RESCALE_LOG2 = FP8 ? 2.0f : 8.0f;
+  __device__ static uint32_t q_base(int buf) {
+    return FP8 ? buf * 2 * QPART : (NARROW ? buf * 8192u : buf * TILE);
+  }
 };
 
 struct AttnTcParams {
-  CUtensorMap q;   // [B*n_h*bs][128] bf16, box rows 64 (NARROW) or 128
-  CUtensorMap k;   // [B*n_kv*capacity][128] bf16 (this layer)
+  CUtensorMap q;   // [B*n_h*bs][128] bf16, box rows 64 (NARROW) or 128; fp8: the Q codes
+  CUtensorMap q_lo;  // fp8: the Q remainder codes (same shape)
+  CUtensorMap k;   // [B*n_kv*capacity][128] bf16 or E4M3 (this layer)
   CUtensorMap v;
   const int32_t* table;   // paged cache: [batch][pps] page ids of 128-row pages, or null
   int pps;
@@ -81,7 +112,8 @@ struct AttnTcParams {
   int* next_item;
   unsigned* status;
   int batch, n_h, n_kv, bs, G, R, capacity, window, table_len, max_splits;
-  float sl2;  // scaling * log2(e)
+  float sl2;      // scaling * log2(e) (fp8: times k_scale)
+  float v_scale;  // fp8: scale of the V codes
 };
 
 __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity, unsigned* status) {
@@ -117,6 +149,42 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, ui
       : "memory");
 }
 
+// kind::f8f6f4 (E4M3 x E4M3, fp32 accumulator, K = 32 per instruction): SS and TS forms.
+__device__ __forceinline__ void mma_f8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f8_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor: kind::f8f6f4, A = B = E4M3, D = f32, both K-major, M x N.
+constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// 32 lanes x 16 columns of 32-bit TMEM cells.
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // work list: one CTA (attn_sched.cuh), unless the projection launch built it
 // ---------------------------------------------------------------------------
@@ -127,14 +195,14 @@ __global__ void __launch_bounds__(1024) attn_schedule_kernel(sched::Params p) { 
 // ---------------------------------------------------------------------------
 // attention
 // ---------------------------------------------------------------------------
-template <bool NARROW>
+template <bool NARROW, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams p) {
-  using PL = Plan<NARROW>;
+  using PL = Plan<NARROW, FP8>;
   constexpr int NCOL = 64;  // S columns per softmax thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + PL::OFF_BAR);
-  int4* ring = (int4*)(smem + PL::OFF_BAR + 256);
+  int4* ring = (int4*)(smem + PL::OFF_RING);
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ float xch[2][2][128];  // tile maxima of the two column halves
@@ -145,14 +213,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const int n_soft = 64 * nq;                     // softmax threads
   const bool soft = warp < kSoftmaxWarps && (warp & 3) < nq;
   const uint32_t sbase = ptx::smem_u32(smem);
-  // barriers (8 bytes each): q 2+2, k 3+3, v 3+3, s 2+2, p 1, pv 2, items 4+4, MMA exit 1
-  const uint32_t q_full0 = ptx::smem_u32(bars + 0), q_empty0 = ptx::smem_u32(bars + 2);
-  const uint32_t k_full0 = ptx::smem_u32(bars + 4), k_empty0 = ptx::smem_u32(bars + 7);
-  const uint32_t v_full0 = ptx::smem_u32(bars + 10), v_empty0 = ptx::smem_u32(bars + 13);
-  const uint32_t s_full0 = ptx::smem_u32(bars + 16), s_free0 = ptx::smem_u32(bars + 18);
-  const uint32_t p_full = ptx::smem_u32(bars + 20), pv_done0 = ptx::smem_u32(bars + 21);
-  const uint32_t it_full0 = ptx::smem_u32(bars + 23), it_empty0 = ptx::smem_u32(bars + 27);
-  const uint32_t mma_fin = ptx::smem_u32(bars + 31);
+  // barriers (8 bytes each): q 2+2, k and v full+empty per stage, s 2+2, p 1, pv 2,
+  // items 4+4, MMA exit 1
+  const uint32_t q_full0 = ptx::smem_u32(bars + PL::B_QF), q_empty0 = ptx::smem_u32(bars + PL::B_QE);
+  const uint32_t k_full0 = ptx::smem_u32(bars + PL::B_KF), k_empty0 = ptx::smem_u32(bars + PL::B_KE);
+  const uint32_t v_full0 = ptx::smem_u32(bars + PL::B_VF), v_empty0 = ptx::smem_u32(bars + PL::B_VE);
+  const uint32_t s_full0 = ptx::smem_u32(bars + PL::B_SF), s_free0 = ptx::smem_u32(bars + PL::B_SE);
+  const uint32_t p_full = ptx::smem_u32(bars + PL::B_P), pv_done0 = ptx::smem_u32(bars + PL::B_PV);
+  const uint32_t it_full0 = ptx::smem_u32(bars + PL::B_ITF), it_empty0 = ptx::smem_u32(bars + PL::B_ITE);
+  const uint32_t mma_fin = ptx::smem_u32(bars + PL::B_FIN);
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -192,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     // ---------------------------------------------------- item fetch, Q and K loads
     if (lane == 0) {
       ptx::prefetch_tmap(&p.q);
+      if (FP8) ptx::prefetch_tmap(&p.q_lo);
       ptx::prefetch_tmap(&p.k);
       ptx::prefetch_tmap(&p.v);
       const uint64_t pol = ptx::policy_evict_first();
@@ -215,9 +285,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           break;
         const int qrow = (b * p.n_h + kvh * p.G) * p.bs;
         const uint32_t qd = sbase + PL::q_base(qb);
-        ptx::mbar_arrive_expect_tx(q_full0 + 8 * qb, NARROW ? TILE / 2 : TILE);
+        ptx::mbar_arrive_expect_tx(q_full0 + 8 * qb, PL::Q_TX);
         ptx::tma_load_2d(qd, &p.q, q_full0 + 8 * qb, 0, qrow);
-        ptx::tma_load_2d(qd + HALF, &p.q, q_full0 + 8 * qb, 64, qrow);
+        if (FP8)
+          ptx::tma_load_2d(qd + PL::QPART, &p.q_lo, q_full0 + 8 * qb, 0, qrow);
+        else
+          ptx::tma_load_2d(qd + HALF, &p.q, q_full0 + 8 * qb, 64, qrow);
         ++nq_loads;
         const int ntiles = (it.z - it.y + TK - 1) / TK;
         int row_next = tile_row(p, b, kvh, it.y);  // the next tile's row, fetched a tile ahead
@@ -230,10 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             stop = true;
             break;
           }
-          const uint32_t kd = sbase + PL::OFF_K + s * TILE;
-          ptx::mbar_arrive_expect_tx(k_full0 + 8 * s, TILE);
+          const uint32_t kd = sbase + PL::OFF_K + s * PL::TILE_B;
+          ptx::mbar_arrive_expect_tx(k_full0 + 8 * s, PL::TILE_B);
           ptx::tma_load_2d_hint(kd, &p.k, k_full0 + 8 * s, 0, row, pol);
-          ptx::tma_load_2d_hint(kd + HALF, &p.k, k_full0 + 8 * s, 64, row, pol);
+          if (!FP8) ptx::tma_load_2d_hint(kd + HALF, &p.k, k_full0 + 8 * s, 64, row, pol);
           ++gk;
         }
         if (stop) break;
@@ -268,10 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             stop = true;
             break;
           }
-          const uint32_t vd = sbase + PL::OFF_V + s * TILE;
-          ptx::mbar_arrive_expect_tx(v_full0 + 8 * s, TILE);
+          const uint32_t vd = sbase + PL::OFF_V + s * PL::TILE_B;
+          ptx::mbar_arrive_expect_tx(v_full0 + 8 * s, PL::TILE_B);
           ptx::tma_load_2d_hint(vd, &p.v, v_full0 + 8 * s, 0, row, pol);
-          ptx::tma_load_2d_hint(vd + HALF, &p.v, v_full0 + 8 * s, 64, row, pol);
+          if (!FP8) ptx::tma_load_2d_hint(vd + HALF, &p.v, v_full0 + 8 * s, 64, row, pol);
           ++gv;
         }
       }
@@ -281,8 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   } else if (warp == WARP_MMA) {
     // ---------------------------------------------------- MMA issue
     if (lane == 0) {
-      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, TK);
-      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, 128) | (1u << 16);  // V MN-major
+      constexpr uint32_t idesc_s = FP8 ? idesc_e4m3_f32(128, TK) : ptx::idesc_bf16_f32(128, TK);
+      constexpr uint32_t idesc_pv =  // V MN-major
+          (FP8 ? idesc_e4m3_f32(128, 128) : ptx::idesc_bf16_f32(128, 128)) | (1u << 16);
       int gt = 0;
       bool stop = false, issued = false;
       for (int n = 0; !stop; ++n) {
@@ -302,12 +376,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             return false;
           if (!ptx::mbar_wait(k_full0 + 8 * ks, ku & 1, &abort_flag, p.status)) return false;
           ptx::tc_fence_after();
-          const uint32_t ka = sbase + PL::OFF_K + ks * TILE;
+          const uint32_t ka = sbase + PL::OFF_K + ks * PL::TILE_B;
+          if (FP8) {
+            // S = Qcodes K^T + Qremainder K^T: 4 K-steps of 32 dims each
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-            ptx::mma_bf16(tmem + TM_S + s * TK, ptx::smem_desc_sw128(qa + off),
-                          ptx::smem_desc_sw128(ka + off), idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f8(tmem + TM_S + s * TK,
+                     ptx::smem_desc_sw128(qa + (kk >> 2) * PL::QPART + (kk & 3) * 32),
+                     ptx::smem_desc_sw128(ka + (kk & 3) * 32), idesc_s, kk > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
+              ptx::mma_bf16(tmem + TM_S + s * TK, ptx::smem_desc_sw128(qa + off),
+                            ptx::smem_desc_sw128(ka + off), idesc_s, kk > 0 ? 1u : 0u);
+            }
           }
           issued = true;
           ptx::mma_commit(k_empty0 + 8 * ks);
@@ -324,12 +407,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t va = sbase + PL::OFF_V + vs * TILE;
+          const uint32_t va = sbase + PL::OFF_V + vs * PL::TILE_B;
           const uint32_t pa = tmem + TM_P + (g & 1) * 64;
+          if (FP8) {
+            // O += Pcodes V + Premainder V: P columns 0-31 and 32-63, 32 keys per K-step
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(tmem + TM_O, pa + kk * 8, ptx::smem_desc_sw128_mn(va + kk * 2048, HALF),
-                        idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f8_ts(tmem + TM_O, pa + (kk >> 2) * 32 + (kk & 3) * 8,
+                        ptx::smem_desc_sw128_mn(va + (kk & 3) * 4096, PL::TILE_B), idesc_pv,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_ts(tmem + TM_O, pa + kk * 8, ptx::smem_desc_sw128_mn(va + kk * 2048, HALF),
+                          idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          }
           ptx::mma_commit(v_empty0 + 8 * vs);
           ptx::mma_commit(pv_done0 + 8 * (g & 1));
           if (j + 2 < T && !issue_s(j + 2)) {
@@ -409,12 +501,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         bool resc = false;
         if (m_ref == -INFINITY) {
           m_ref = mx;                      // nothing accumulated yet for this row
-        } else if (mx > m_ref + kRescaleLog2) {
+        } else if (mx > m_ref + PL::RESCALE_LOG2) {
           alpha = ptx::ex2(m_ref - mx);
           m_ref = mx;
           resc = true;
         }
-        const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+        // fp8: P = 64 p (2^6), whose small values stay normal E4M3 numbers
+        const float mu = ((m_ref == -INFINITY) ? 0.f : m_ref) - (FP8 ? 6.f : 0.f);
         const float2 sl2v = make_float2(p.sl2, p.sl2), nmu = make_float2(-mu, -mu);
         float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                           make_float2(0.f, 0.f)};
@@ -424,7 +517,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), sl2v, nmu);
           const float2 y = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
           acc2[(e >> 1) & 3] = __fadd2_rn(acc2[(e >> 1) & 3], y);
-          pk[e >> 1] = pack_bf16(y.x, y.y);
+          if (FP8) {
+            s[e] = y.x;
+            s[e + 1] = y.y;
+          } else {
+            pk[e >> 1] = pack_bf16(y.x, y.y);
+          }
         }
         const float2 a01 = __fadd2_rn(acc2[0], acc2[1]), a23 = __fadd2_rn(acc2[2], acc2[3]);
         l = l * alpha + ((a01.x + a01.y) + (a23.x + a23.y));
@@ -450,7 +548,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           if (!alive) break;
           ptx::tc_fence_after();
         }
-        ptx::tmem_st_32x32b_x32(tmem + lane_base + TM_P + sb * 64 + half * 32, pk);
+        if (FP8) {
+          // codes of P (columns 0-31 of the buffer) and of its remainder (32-63)
+          uint32_t hi[NCOL / 4], lo[NCOL / 4];
+#pragma unroll
+          for (int c = 0; c < NCOL / 4; ++c)
+            e4m3x4_split(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3], hi[c], lo[c]);
+          tmem_st_32x32b_x16(tmem + lane_base + TM_P + sb * 64 + half * 16, hi);
+          tmem_st_32x32b_x16(tmem + lane_base + TM_P + sb * 64 + 32 + half * 16, lo);
+        } else {
+          ptx::tmem_st_32x32b_x32(tmem + lane_base + TM_P + sb * 64 + half * 32, pk);
+        }
         ptx::tmem_st_wait();
         // keys past the range end in the last tile: zero their V rows (slots past the
         // cache length may hold anything, and 0 * NaN would poison O)
@@ -459,12 +567,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           const int vs = g % PL::V_STAGES, vu = g / PL::V_STAGES;
           alive = __all_sync(0xffffffffu, ptx::mbar_wait(v_full0 + 8 * vs, vu & 1, &abort_flag, p.status));
           if (!alive) break;
-          uint4* vz = reinterpret_cast<uint4*>(smem + PL::OFF_V + vs * TILE);
-          const int per_half = (TK - nvalid) * 8;  // 16-byte chunks per half
+          uint4* vz = reinterpret_cast<uint4*>(smem + PL::OFF_V + vs * PL::TILE_B);
+          const int per_half = (TK - nvalid) * 8;  // 16-byte chunks per half (fp8: per tile)
           const int me = half * 32 * nq + rt;
-          for (int idx = me; idx < 2 * per_half; idx += n_soft) {
-            const int h = idx / per_half, rem = idx - h * per_half;
-            vz[(h * HALF) / 16 + nvalid * 8 + rem] = make_uint4(0, 0, 0, 0);
+          if (FP8) {
+            for (int idx = me; idx < per_half; idx += n_soft) vz[nvalid * 8 + idx] = make_uint4(0, 0, 0, 0);
+          } else {
+            for (int idx = me; idx < 2 * per_half; idx += n_soft) {
+              const int h = idx / per_half, rem = idx - h * per_half;
+              vz[(h * HALF) / 16 + nvalid * 8 + rem] = make_uint4(0, 0, 0, 0);
+            }
           }
           ptx::fence_proxy_async_smem();
         }
@@ -493,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       if (!rvalid) continue;
       if (it.w < 0) {
         bf16* orow = p.out + ((size_t)(b * p.bs + t) * p.n_h + kvh * p.G + gq) * 128 + coff;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = l > 0.f ? (FP8 ? p.v_scale : 1.f) / l : 0.f;
 #pragma unroll
         for (int k = 0; k < NCOL / 8; ++k) {
           uint4 w;
@@ -506,8 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       } else {
         const size_t prow = ((size_t)it.x * p.max_splits + it.w) * p.R + rt;
         float4* a = reinterpret_cast<float4*>(p.part_acc + prow * 128 + coff);
+        const float vsc = FP8 ? p.v_scale : 1.f;
 #pragma unroll
-        for (int k = 0; k < NCOL / 4; ++k) a[k] = make_float4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
+        for (int k = 0; k < NCOL / 4; ++k)
+          a[k] = make_float4(s[4 * k] * vsc, s[4 * k + 1] * vsc, s[4 * k + 2] * vsc, s[4 * k + 3] * vsc);
         if (half == 0) p.part_ml[prow] = make_float2(m_ref, l);
       }
     }
@@ -606,14 +720,15 @@ int sm_count() {
   return count[dev];
 }
 
-template <bool NARROW>
+template <bool NARROW, bool FP8>
 cudaError_t launch_attn(const AttnTcParams& p, int grid, cudaStream_t s) {
-  const size_t smem = Plan<NARROW>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NARROW>,
+  const size_t smem = Plan<NARROW, FP8>::SMEM;
+  static_assert(Plan<NARROW, FP8>::SMEM <= 227 * 1024, "attention shared memory");
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NARROW, FP8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   LaunchScope ls_(DFLASH_KERNEL_ATTENTION, s);
-  attn_tc_kernel<NARROW><<<grid, kThreads, smem, s>>>(p);
+  attn_tc_kernel<NARROW, FP8><<<grid, kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -621,6 +736,8 @@ cudaError_t launch_attn(const AttnTcParams& p, int grid, cudaStream_t s) {
 
 // bf16 row-major [rows][cols] matrix, box {64, box_rows}, 128-byte swizzle (gemm_tc.cu)
 bool encode_2d_bf16(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows);
+// byte matrix [rows][128], box {128, box_rows}, 128-byte swizzle (gemm_tc.cu)
+bool encode_2d_u8(CUtensorMap* m, const void* base, long long rows, int box_rows);
 
 int attn_tc_chunk() { return TK * sched::kItemMinTiles; }
 
@@ -661,10 +778,18 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   const bool narrow = R <= 64;
   const long long kv_rows = a.block_table ? (long long)a.n_pages * a.n_kv * TK
                                           : (long long)a.batch * a.n_kv * a.capacity;
-  if (!encode_2d_bf16(&p.q, a.q, (long long)a.batch * a.n_h * a.bs, 128, narrow ? 64 : 128) ||
-      !encode_2d_bf16(&p.k, a.cache_k, kv_rows, 128, 128) ||
-      !encode_2d_bf16(&p.v, a.cache_v, kv_rows, 128, 128))
+  const long long q_rows = (long long)a.batch * a.n_h * a.bs;
+  if (a.fp8) {
+    // Q codes, then the remainder codes, 128 bytes per row
+    if (!encode_2d_u8(&p.q, a.q, q_rows, narrow ? 64 : 128) ||
+        !encode_2d_u8(&p.q_lo, (const char*)a.q + q_rows * 128, q_rows, narrow ? 64 : 128) ||
+        !encode_2d_u8(&p.k, a.cache_k, kv_rows, 128) || !encode_2d_u8(&p.v, a.cache_v, kv_rows, 128))
+      return cudaErrorInvalidValue;
+  } else if (!encode_2d_bf16(&p.q, a.q, q_rows, 128, narrow ? 64 : 128) ||
+             !encode_2d_bf16(&p.k, a.cache_k, kv_rows, 128, 128) ||
+             !encode_2d_bf16(&p.v, a.cache_v, kv_rows, 128, 128)) {
     return cudaErrorInvalidValue;
+  }
   p.table = a.block_table;
   p.pps = a.pages_per_seq;
   const int pairs = a.batch * a.n_kv;
@@ -689,7 +814,8 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   p.capacity = a.capacity;
   p.window = a.window;
   p.table_len = a.table_len;
-  p.sl2 = a.scaling * 1.4426950408889634f;
+  p.sl2 = a.scaling * 1.4426950408889634f * (a.fp8 ? a.k_scale : 1.f);
+  p.v_scale = a.fp8 ? a.v_scale : 1.f;
   cudaError_t e = cudaSuccess;
   if (!a.sched_ready) {
     LaunchScope ls_(DFLASH_KERNEL_SCHEDULE, s);
@@ -699,7 +825,10 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int max_items = pairs * p.max_splits;
   const int grid = sp.n_sm < max_items ? sp.n_sm : max_items;
-  e = narrow ? launch_attn<true>(p, grid, s) : launch_attn<false>(p, grid, s);
+  if (a.fp8)
+    e = narrow ? launch_attn<true, true>(p, grid, s) : launch_attn<false, true>(p, grid, s);
+  else
+    e = narrow ? launch_attn<true, false>(p, grid, s) : launch_attn<false, false>(p, grid, s);
   if (e != cudaSuccess) return e;
   // marked rows are at most pairs * R; a few waves of warps cover them
   const int rows = pairs * R;

@@ -57,15 +57,43 @@ dflash_status check_cache(const dflash_kv_cache* c, int layer) {
         ((uintptr_t)c->block_table & 3))
       return DFLASH_ERR_INVALID_ARG;
   }
+  if (c->kv_dtype == DFLASH_FP8_E4M3 && c->kv_scales) {
+    for (int i = 0; i < 2 * c->n_layers; ++i)
+      if (!(c->kv_scales[i] > 0.f) || !(c->kv_scales[i] < INFINITY)) return DFLASH_ERR_INVALID_ARG;
+  }
   return DFLASH_OK;
 }
 
-// the paged layout is served by the bf16 tensor-core path only
+bool kv_fp8(const dflash_kv_cache* c) { return c->kv_dtype == DFLASH_FP8_E4M3; }
+
+// The paged layout and the fp8 cache are served by the bf16 tensor-core path only;
+// the cache element type is the dims' one or E4M3.
 dflash_status check_layout(const dflash_dims* d, const dflash_kv_cache* c) {
-  return c->block_table && d->dtype != DFLASH_BF16 ? DFLASH_ERR_UNSUPPORTED : DFLASH_OK;
+  if (c->kv_dtype != 0 && c->kv_dtype != d->dtype && c->kv_dtype != DFLASH_FP8_E4M3)
+    return DFLASH_ERR_UNSUPPORTED;
+  if ((c->block_table || kv_fp8(c)) && d->dtype != DFLASH_BF16) return DFLASH_ERR_UNSUPPORTED;
+  return DFLASH_OK;
 }
 
 size_t esize(const dflash_dims* d) { return d->dtype == DFLASH_F32 ? 4 : 2; }
+
+// bytes of one cache element
+size_t kv_esize(const dflash_dims* d, const dflash_kv_cache* c) { return kv_fp8(c) ? 1 : esize(d); }
+
+float kv_scale(const dflash_kv_cache* c, int layer, int which) {
+  return kv_fp8(c) && c->kv_scales ? c->kv_scales[2 * layer + which] : 1.f;
+}
+
+// Fills the fp8 fields of a per-head epilogue: quantisation by the inverse scales, and
+// Q as codes + remainder codes (the remainder array follows the codes in q_out).
+void fp8_epilogue(HeadEpilogue& ep, const dflash_dims* d, const dflash_kv_cache* c, int layer) {
+  ep.kv_fp8 = kv_fp8(c);
+  if (!ep.kv_fp8) return;
+  ep.k_inv = 1.f / kv_scale(c, layer, 0);
+  ep.v_inv = 1.f / kv_scale(c, layer, 1);
+  if (ep.q_out)
+    ep.q_lo = (char*)ep.q_out + (size_t)c->batch * d->n_h * d->block_size * d->d_h;
+}
 
 dflash_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA; }
 
@@ -268,12 +296,13 @@ HeadEpilogue inject_epilogue(const dflash_dims* d, const dflash_kv_cache* c, int
   ep.bs = 0;
   ep.lens = c->lens + (size_t)layer * c->batch;
   ep.q_out = nullptr;
-  ep.cache_k = (char*)c->k + (size_t)layer * layer_elems(d, c) * esize(d);
-  ep.cache_v = (char*)c->v + (size_t)layer * layer_elems(d, c) * esize(d);
+  ep.cache_k = (char*)c->k + (size_t)layer * layer_elems(d, c) * kv_esize(d, c);
+  ep.cache_v = (char*)c->v + (size_t)layer * layer_elems(d, c) * kv_esize(d, c);
   ep.capacity = c->capacity;
   ep.status = status;
   ep.block_table = c->block_table;
   ep.pages_per_seq = c->block_table ? c->capacity / 128 : 0;
+  fp8_epilogue(ep, d, c, layer);
   return ep;
 }
 
@@ -300,12 +329,13 @@ HeadEpilogue block_epilogue(const dflash_dims* d, const dflash_kv_cache* c, int 
   ep.bs = d->block_size;
   ep.lens = c->lens + (size_t)layer * c->batch;
   ep.q_out = q_out;
-  ep.cache_k = (char*)c->k + (size_t)layer * layer_elems(d, c) * esize(d);
-  ep.cache_v = (char*)c->v + (size_t)layer * layer_elems(d, c) * esize(d);
+  ep.cache_k = (char*)c->k + (size_t)layer * layer_elems(d, c) * kv_esize(d, c);
+  ep.cache_v = (char*)c->v + (size_t)layer * layer_elems(d, c) * kv_esize(d, c);
   ep.capacity = c->capacity;
   ep.status = status;
   ep.block_table = c->block_table;
   ep.pages_per_seq = c->block_table ? c->capacity / 128 : 0;
+  fp8_epilogue(ep, d, c, layer);
   return ep;
 }
 
@@ -314,8 +344,8 @@ AttnParams block_attention(const dflash_dims* d, const dflash_kv_cache* c, int l
                            void* out, unsigned* status) {
   AttnParams p;
   p.q = s.q;
-  p.cache_k = (char*)c->k + (size_t)layer * layer_elems(d, c) * esize(d);
-  p.cache_v = (char*)c->v + (size_t)layer * layer_elems(d, c) * esize(d);
+  p.cache_k = (char*)c->k + (size_t)layer * layer_elems(d, c) * kv_esize(d, c);
+  p.cache_v = (char*)c->v + (size_t)layer * layer_elems(d, c) * kv_esize(d, c);
   p.lens = c->lens + (size_t)layer * c->batch;
   p.out = out;
   p.part_acc = s.part_acc;
@@ -339,6 +369,9 @@ AttnParams block_attention(const dflash_dims* d, const dflash_kv_cache* c, int l
   p.block_table = c->block_table;
   p.pages_per_seq = c->block_table ? c->capacity / 128 : 0;
   p.n_pages = c->n_pages;
+  p.fp8 = kv_fp8(c);
+  p.k_scale = kv_scale(c, layer, 0);
+  p.v_scale = kv_scale(c, layer, 1);
   return p;
 }
 

@@ -135,8 +135,40 @@ struct HeadEpilogue {
   // paged cache: page ids [batch][pages_per_seq] of 128-row pages, or null (contiguous)
   const int32_t* block_table = nullptr;
   int pages_per_seq = 0;
+  // fp8 (E4M3) cache: K / V rows are stored as codes of x * k_inv (x * v_inv), and Q as
+  // two E4M3 arrays, q_out = codes of q and q_lo = codes of the remainder q - value(q_out)
+  bool kv_fp8 = false;
+  float k_inv = 1.f, v_inv = 1.f;
+  void* q_lo = nullptr;
 };
 cudaError_t head_epilogue(int dtype, const HeadEpilogue& e, cudaStream_t s);
+
+// Four E4M3 codes of (a, b, c, d) * inv (round to nearest even, saturating), packed with
+// a in the lowest byte.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+// Values of the two E4M3 codes in the low (x) and high (y) byte of v.
+__device__ __forceinline__ float2 e4m3x2_value(uint16_t v) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  float2 f;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(f.x), "=f"(f.y)
+      : "r"(h2));
+  return f;
+}
+// E4M3 codes of four values and of their remainders: hi = codes(v), lo = codes(v - value(hi)).
+__device__ __forceinline__ void e4m3x4_split(float a, float b, float c, float d, uint32_t& hi,
+                                             uint32_t& lo) {
+  hi = e4m3x4(a, b, c, d);
+  const float2 v01 = e4m3x2_value((uint16_t)(hi & 0xFFFF));
+  const float2 v23 = e4m3x2_value((uint16_t)(hi >> 16));
+  lo = e4m3x4(a - v01.x, b - v01.y, c - v23.x, d - v23.y);
+}
 
 // Row index (in d_h-wide rows of one layer's K or V) of logical slot `pos` of sequence b,
 // KV head kvh: [b][kvh][capacity] contiguous, or page table[b][pos / 128] of a pool of
@@ -220,6 +252,10 @@ struct AttnParams {
   bool sched_ready;         // the work list was built by the projection launch
   const int32_t* block_table;  // paged cache (128-row pages), or null
   int pages_per_seq, n_pages;
+  // fp8 (E4M3) cache: q holds the codes of Q then those of its remainder; scores are
+  // scaled by k_scale and outputs by v_scale
+  bool fp8;
+  float k_scale, v_scale;
   int batch, n_h, n_kv, d_h, bs, capacity, window, chunk, n_chunks, table_len;
   float scaling;
 };

@@ -287,14 +287,30 @@ __global__ void __launch_bounds__(256) head_epilogue_bf16_kernel(HeadEpilogue e)
     x.z = x.z * c2.x + sg * o.z * c2.y;
     x.w = x.w * c3.x + sg * o.w * c3.y;
   }
-  bf16* dst;
+  // element offset of the destination row: Q, or the cache slot
+  size_t eoff;
   if (kind == 0) {
-    dst = (bf16*)e.q_out + (((size_t)b * e.n_q + head) * e.bs + t) * 128;
+    eoff = (((size_t)b * e.n_q + head) * e.bs + t) * 128;
   } else {
     const int kvh = head - e.n_q - (kind == 2 ? e.n_kv : 0);
-    bf16* base = (bf16*)(kind == 1 ? e.cache_k : e.cache_v);
-    dst = base + cache_row(e.block_table, e.pages_per_seq, e.n_kv, e.capacity, b, kvh, pos) * 128;
+    eoff = cache_row(e.block_table, e.pages_per_seq, e.n_kv, e.capacity, b, kvh, pos) * 128;
   }
+  char* base = (char*)(kind == 0 ? e.q_out : kind == 1 ? e.cache_k : e.cache_v);
+  if (e.kv_fp8) {
+    // E4M3: Q as codes + remainder codes, K / V as codes of x / scale
+    if (kind == 0) {
+      uint32_t hi, lo;
+      e4m3x4_split(x.x, x.y, x.z, x.w, hi, lo);
+      reinterpret_cast<uint32_t*>(base + eoff)[lane] = hi;
+      reinterpret_cast<uint32_t*>((char*)e.q_lo + eoff)[lane] = lo;
+    } else {
+      const float inv = kind == 1 ? e.k_inv : e.v_inv;
+      reinterpret_cast<uint32_t*>(base + eoff)[lane] =
+          e4m3x4(x.x * inv, x.y * inv, x.z * inv, x.w * inv);
+    }
+    return;
+  }
+  bf16* dst = (bf16*)base + eoff;
   __nv_bfloat162 lo2 = __floats2bfloat162_rn(x.x, x.y), hi2 = __floats2bfloat162_rn(x.z, x.w);
   uint2 u;
   u.x = *reinterpret_cast<uint32_t*>(&lo2);

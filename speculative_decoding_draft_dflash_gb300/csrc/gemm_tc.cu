@@ -165,6 +165,10 @@ __device__ __forceinline__ HeadEpilogue pick_epilogue(const TcGemmParams& p, boo
   DFLASH_PICK(pre_M);
   DFLASH_PICK(block_table);
   DFLASH_PICK(pages_per_seq);
+  DFLASH_PICK(kv_fp8);
+  DFLASH_PICK(k_inv);
+  DFLASH_PICK(v_inv);
+  DFLASH_PICK(q_lo);
 #undef DFLASH_PICK
   return e;
 }
@@ -397,14 +401,33 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
             const float y2 = rot ? x2 * cs[i][2].x + sg * p2 * cs[i][2].y : x.z;
             const float y3 = rot ? x3 * cs[i][3].x + sg * p3 * cs[i][3].y : x.w;
             const int kvh = head - ep.n_q - (kind == 2 ? ep.n_kv : 0);
-            bf16* kvbase = (bf16*)(kind == 1 ? ep.cache_k : ep.cache_v);
-            bf16* dst = qh ? (bf16*)ep.q_out + (((size_t)rs[i].x * ep.n_q + head) * ep.bs + rs[i].y) * 128
-                           : kvbase + (rs[i].w >= 0 ? ((size_t)rs[i].w * ep.n_kv + kvh) * 128 + (rs[i].z & 127)
-                                                    : ((size_t)rs[i].x * ep.n_kv + kvh) * ep.capacity + rs[i].z) * 128;
-            uint2 w2;
-            w2.x = pack_bf16(y0, y1);
-            w2.y = pack_bf16(y2, y3);
-            if (rs[i].z >= 0) reinterpret_cast<uint2*>(dst)[lane] = w2;
+            // element offset of the destination row (Q, or the cache slot)
+            const size_t eoff =
+                qh ? (((size_t)rs[i].x * ep.n_q + head) * ep.bs + rs[i].y) * 128
+                   : (rs[i].w >= 0 ? ((size_t)rs[i].w * ep.n_kv + kvh) * 128 + (rs[i].z & 127)
+                                   : ((size_t)rs[i].x * ep.n_kv + kvh) * ep.capacity + rs[i].z) * 128;
+            char* kvbase = (char*)(kind == 1 ? ep.cache_k : ep.cache_v);
+            if (ep.kv_fp8) {
+              // E4M3 rows: Q as codes + remainder codes, K / V as codes of x / scale
+              if (qh) {
+                uint32_t hi, lo;
+                e4m3x4_split(y0, y1, y2, y3, hi, lo);
+                if (rs[i].z >= 0) {
+                  reinterpret_cast<uint32_t*>((char*)ep.q_out + eoff)[lane] = hi;
+                  reinterpret_cast<uint32_t*>((char*)ep.q_lo + eoff)[lane] = lo;
+                }
+              } else {
+                const float inv = kind == 1 ? ep.k_inv : ep.v_inv;
+                const uint32_t c = e4m3x4(y0 * inv, y1 * inv, y2 * inv, y3 * inv);
+                if (rs[i].z >= 0) reinterpret_cast<uint32_t*>(kvbase + eoff)[lane] = c;
+              }
+            } else {
+              bf16* dst = qh ? (bf16*)ep.q_out + eoff : (bf16*)kvbase + eoff;
+              uint2 w2;
+              w2.x = pack_bf16(y0, y1);
+              w2.y = pack_bf16(y2, y3);
+              if (rs[i].z >= 0) reinterpret_cast<uint2*>(dst)[lane] = w2;
+            }
           }
         }
 #pragma unroll
@@ -492,6 +515,19 @@ bool encode_2d_bf16(CUtensorMap* m, const void* base, long long rows, int cols, 
   cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// byte matrix [rows][128], box {128 bytes, box_rows rows}, 128-byte swizzle, zero fill.
+bool encode_2d_u8(CUtensorMap* m, const void* base, long long rows, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -15,6 +15,7 @@ import ctypes
 import os
 from ctypes import POINTER, c_double, c_float, c_int, c_size_t, c_uint, c_void_p
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -42,7 +43,11 @@ class dflash_dims(ctypes.Structure):
 class dflash_kv_cache(ctypes.Structure):
     _fields_ = [("k", c_void_p), ("v", c_void_p), ("lens", c_void_p), ("n_layers", c_int),
                 ("batch", c_int), ("capacity", c_int), ("block_table", c_void_p),
-                ("page_size", c_int), ("n_pages", c_int)]
+                ("page_size", c_int), ("n_pages", c_int), ("kv_dtype", c_int),
+                ("kv_scales", c_void_p)]
+
+
+DFLASH_FP8_E4M3 = 2
 
 
 def _load():
@@ -135,13 +140,19 @@ class KVCache:
     and block_table int32 [batch][capacity / page_size]; with paged=True the pages of
     the sequences are a seeded permutation of the pool (so no page is where a contiguous
     layout would put it). lens: int32 [n_layers][batch] in both layouts.
+    kv="fp8": k, v hold E4M3 codes (uint8 tensors) of x / scale with kv_scales
+    [n_layers][2] = (k_scale, v_scale) per layer (default 1); rows() reads them back as
+    scale * value.
     """
 
     PAGE = 128
 
     def __init__(self, n_layers, batch, n_kv, capacity, d_h, dtype, device="cuda", paged=False,
-                 page_table=None, n_pages=None, seed=0):
-        td = torch_dtype(dtype_code(dtype))
+                 page_table=None, n_pages=None, seed=0, kv="bf16", kv_scales=None):
+        self.fp8 = kv == "fp8"
+        td = torch.uint8 if self.fp8 else torch_dtype(dtype_code(dtype))
+        self.scales = np.ones((n_layers, 2)) if kv_scales is None else np.asarray(kv_scales, float)
+        assert self.scales.shape == (n_layers, 2)
         self.n_layers, self.batch, self.capacity, self.n_kv, self.d_h = (
             n_layers, batch, capacity, n_kv, d_h)
         self.lens = torch.zeros((n_layers, batch), dtype=torch.int32, device=device)
@@ -169,23 +180,41 @@ class KVCache:
             self.v = torch.zeros(shape, dtype=td, device=device)
             self.desc = dflash_kv_cache(self.k.data_ptr(), self.v.data_ptr(), self.lens.data_ptr(),
                                         n_layers, batch, capacity)
+        if self.fp8:
+            # host array the descriptor points to; kept alive with the cache
+            self._scales_c = (c_float * (2 * n_layers))(*self.scales.ravel().tolist())
+            self.desc.kv_dtype = DFLASH_FP8_E4M3
+            self.desc.kv_scales = ctypes.addressof(self._scales_c)
 
     def _index(self, b, lo, hi):
         """(pages, rows) of logical slots lo .. hi-1 of sequence b (paged layout)."""
         s = torch.arange(lo, hi, device=self.block_table.device)
         return self.block_table[b, s // self.PAGE].long(), s % self.PAGE
 
-    def rows(self, which, layer, b, lo, hi):
-        """Logical rows lo .. hi-1 of sequence b as [n_kv][hi - lo][d_h] (a copy when paged)."""
+    def rows(self, which, layer, b, lo, hi, codes=False):
+        """Logical rows lo .. hi-1 of sequence b as [n_kv][hi - lo][d_h] (a copy when paged).
+        fp8: float32 values, scale * value(code), or value(code) with codes=True."""
         t = self.k if which == "k" else self.v
         if not self.paged:
-            return t[layer, b, :, lo:hi]
-        pages, r = self._index(b, lo, hi)
-        return t[layer, pages, :, r].permute(1, 0, 2)
+            x = t[layer, b, :, lo:hi]
+        else:
+            pages, r = self._index(b, lo, hi)
+            x = t[layer, pages, :, r].permute(1, 0, 2)
+        if not self.fp8:
+            return x
+        x = x.contiguous().view(torch.float8_e4m3fn).to(torch.float32)
+        return x if codes else x * float(self.scales[layer, 0 if which == "k" else 1])
+
+    def _store(self, which, layer, X):
+        if not self.fp8:
+            return X
+        s = float(self.scales[layer, 0 if which == "k" else 1])
+        return (X.float() / s).to(torch.float8_e4m3fn).view(torch.uint8)
 
     def set_rows(self, layer, b, K, V):
         """Writes K, V [n_kv][n][d_h] to logical slots 0 .. n-1 of sequence b."""
         n = K.shape[1]
+        K, V = self._store("k", layer, K), self._store("v", layer, V)
         if not self.paged:
             self.k[layer, b, :, :n] = K
             self.v[layer, b, :, :n] = V

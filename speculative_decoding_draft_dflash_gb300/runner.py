@@ -60,7 +60,8 @@ class DeviceWorkload:
             self.capacity = -(-self.capacity // D.KVCache.PAGE) * D.KVCache.PAGE
             self.table_len = self.capacity
         self.cache = D.KVCache(w.n_layers, w.batch, w.n_kv, self.capacity, w.d_h, w.dtype, device,
-                               paged=paged, seed=w.seed)
+                               paged=paged, seed=w.seed, kv=w.kv,
+                               kv_scales=np.stack(synth.kv_scales(w), axis=1))
         self.rope = torch.empty((self.table_len, w.d_h // 2, 2), dtype=torch.float32, device=device)
         D.dflash_rope_table_build(w.theta, w.d_h, self.table_len, self.rope)
         self.L0 = synth.prefill_lens(w)

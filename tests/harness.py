@@ -45,7 +45,14 @@ def oracle_rounds(w: synth.Workload, seqs, rounds=None):
     Returns a list (one entry per round) of dicts with, per sequence b in seqs:
     C[b] [n_b, d], out[l][b] [bs, n_h*d_h], rows[l][b] = (K, V) rows appended this
     round (context then block), lens_block[l][b], lens_crop[b].
+
+    fp8 cache: an E4M3 code is an integer decided by floating point, so the oracle takes
+    that decision from the value the device takes it from: the context rows C as the
+    device stores them (rounded to bf16) feed the inject. Everything downstream stays
+    float64.
     """
+    as_stored = (lambda C: synth.to_storage(w, C).astype(np.float64)) if w.kv == "fp8" else \
+        (lambda C: C)
     rounds = rounds or w.rounds
     S = list(seqs)
     L0 = synth.prefill_lens(w)
@@ -59,7 +66,8 @@ def oracle_rounds(w: synth.Workload, seqs, rounds=None):
     gq = [synth.gamma_q(w, l) for l in range(w.n_layers)]
     gk = [synth.gamma_k(w, l) for l in range(w.n_layers)]
     if w.prefill_inject:
-        Cs = [O.ctx_project(synth.hidden_states_rows(w, 0, b, L0[b]), W_fc, g_h, w.eps) for b in S]
+        Cs = [as_stored(O.ctx_project(synth.hidden_states_rows(w, 0, b, L0[b]), W_fc, g_h, w.eps))
+              for b in S]
         cu = synth.cu_rows([L0[b] for b in S])
         for l in range(w.n_layers):
             O.kv_inject(cache, l, np.concatenate(Cs), cu, Wk[l], Wv[l], gk[l], w.n_kv, w.d_h,
@@ -73,8 +81,8 @@ def oracle_rounds(w: synth.Workload, seqs, rounds=None):
     for rnd in range(1, rounds + 1):
         counts = synth.accepted_plus_one(w, rnd)
         before = cache.lens[0].copy()
-        Cs = [O.ctx_project(synth.hidden_states_rows(w, rnd, b, counts[b]), W_fc, g_h, w.eps)
-              for b in S]
+        Cs = [as_stored(O.ctx_project(synth.hidden_states_rows(w, rnd, b, counts[b]), W_fc, g_h,
+                                      w.eps)) for b in S]
         cu = synth.cu_rows([counts[b] for b in S])
         res = {"C": {}, "out": [], "rows": [], "lens_block": [], "before": {}}
         for i, b in enumerate(S):
@@ -134,6 +142,10 @@ def device_rounds(w: synth.Workload, seqs, rounds=None, dev=None, fused_layer=Tr
             res["rows"].append({b: (dev.cache.rows("k", l, b, lens[b], lens_block[l, b]).float().cpu().numpy(),
                                     dev.cache.rows("v", l, b, lens[b], lens_block[l, b]).float().cpu().numpy())
                                 for b in seqs})
+            if dev.cache.fp8:
+                res.setdefault("codes", []).append(
+                    {b: tuple(dev.cache.rows(x, l, b, lens[b], lens_block[l, b], codes=True)
+                              .cpu().numpy() for x in ("k", "v")) for b in seqs})
             res["lens_block"].append({b: int(lens_block[l, b]) for b in seqs})
         res["lens_block_all"] = lens_block
         from speculative_decoding_draft_dflash_gb300 import dflash as D2
@@ -166,6 +178,43 @@ def compare(w, dev_res, ora_res, seqs):
                     g["out"][l][b], o["out"][l][b], w.dtype, f"round {r + 1} layer {l} out seq {b}")
                 gk, gv = g["rows"][l][b]
                 ok, ov = o["rows"][l][b]
+                if w.kv == "fp8":
+                    ks, vs = synth.kv_scales(w)
+                    for name, got, raw, sc in (("K", g["codes"][l][b][0], o["rows_raw"][l][b][0], ks[l]),
+                                               ("V", g["codes"][l][b][1], o["rows_raw"][l][b][1], vs[l])):
+                        check_fp8_codes(got, raw / sc, f"round {r + 1} layer {l} {name} codes seq {b}")
+                    continue
                 check_close(gk, ok, w.dtype, f"round {r + 1} layer {l} K rows seq {b}")
                 check_close(gv, ov, w.dtype, f"round {r + 1} layer {l} V rows seq {b}")
     return report
+
+
+def check_fp8_codes(got, y, what, max_frac=1e-2, rel_delta=2e-3):
+    """Device E4M3 values ``got`` (codes read back, before the scale) against the oracle's
+    unquantised rows ``y`` (already divided by the scale), [..., d_h].
+
+    The code is an integer decided by floating point, and the two sides decide from
+    values that differ slightly: the oracle takes the context rows C as stored in bf16,
+    but the device rounds a float32 C and the oracle a float64 one, and the two roundings
+    differ at a fraction of the elements of C; with the float32 accumulation on top, a
+    cached element differs by up to about 1e-3 of its row's RMS. So: (1) every code must
+    be a correct rounding of some value within ``rel_delta`` x (row RMS) of y, i.e. lie
+    between the codes of y - delta and y + delta (rounding is monotone); (2) at most
+    ``max_frac`` of the codes may differ from the oracle's own rounding of y (a wrong
+    rounding mode or scale changes far more).
+    """
+    got = np.asarray(got, dtype=np.float64)
+    y = np.asarray(y, dtype=np.float64)
+    assert got.shape == y.shape, f"{what}: shape {got.shape} vs {y.shape}"
+    want = O.e4m3_dequantize(O.e4m3_quantize(y))
+    diff = got != want
+    frac = float(diff.mean()) if diff.size else 0.0
+    assert frac <= max_frac, f"{what}: {frac:.2e} of the codes differ from the oracle's rounding"
+    if diff.any():
+        delta = rel_delta * np.sqrt(np.mean(y * y, axis=-1, keepdims=True))
+        lo = O.e4m3_dequantize(O.e4m3_quantize(y - delta))
+        hi = O.e4m3_dequantize(O.e4m3_quantize(y + delta))
+        ok = (got >= lo) & (got <= hi)
+        assert ok.all(), (f"{what}: {int((~ok).sum())} codes are no rounding of a value "
+                          f"within {rel_delta} x row RMS")
+    return frac

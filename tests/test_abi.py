@@ -206,3 +206,34 @@ def test_paged_cache_arguments_rejected(D, lib):
     paged = D.dflash_kv_cache(256, 512, 1024, 2, 4, 256, P(4096), 128, 8)
     assert call(paged, f32) == 2                    # paged layout: bf16 path only
     assert call(paged) == 3                         # valid paged cache, 100-byte workspace
+
+
+def test_fp8_cache_arguments_rejected(D, lib):
+    f = lib.dflash_kv_inject
+    f.restype = ctypes.c_int
+    P = ctypes.c_void_p
+    dims = _dims(D)
+    f32 = _dims(D, dtype=D.DFLASH_F32, d=512, n_h=8, n_kv=8, d_h=64)
+
+    def call(cache, dm=dims):
+        return f(ctypes.byref(dm), ctypes.byref(cache), 0, P(256), P(512), 16, P(768), P(1024),
+                 P(1280), P(1536), 64, P(2048), ctypes.c_size_t(100), None)
+
+    def cache(kv_dtype, scales=None, paged=False):
+        s = None if scales is None else (ctypes.c_float * 4)(*scales)
+        c = D.dflash_kv_cache(256, 512, 1024, 2, 4, 256, P(4096) if paged else None,
+                              128 if paged else 0, 8 if paged else 0, kv_dtype,
+                              ctypes.addressof(s) if s is not None else None)
+        c._keep = s
+        return c
+
+    fp8 = D.DFLASH_FP8_E4M3
+    assert call(cache(fp8, (0.5, 0.25, 1.0, 2.0))) == 3     # valid, 100-byte workspace
+    assert call(cache(fp8)) == 3                            # no scales: 1 everywhere
+    assert call(cache(fp8, (0.5, 0.25, 1.0, 2.0), paged=True)) == 3
+    assert call(cache(D.DFLASH_BF16)) == 3                  # the dims' own type
+    assert call(cache(fp8, (0.5, 0.25, 1.0, 2.0)), f32) == 2  # fp8: bf16 dims only
+    assert call(cache(7)) == 2                              # unknown element type
+    for bad in ((0.5, 0.0, 1.0, 2.0), (0.5, -1.0, 1.0, 2.0), (0.5, 0.25, float("nan"), 2.0),
+                (0.5, 0.25, 1.0, float("inf"))):
+        assert call(cache(fp8, bad)) == 1, bad

@@ -85,3 +85,30 @@ def test_full_size(name, n):
 def test_full_size_paged(name, n):
     w = W[name]
     _run(w, _sample(w, n, seed=12), paged=True)
+
+
+# fp8 (E4M3) cache: the GQA (NARROW tile) case with a window, the MHA case with an odd
+# block and a prefill by projection + inject, and the G = 8 case (128 query rows, WIDE)
+FP8 = {n.replace("bf16", "fp8"): SMALL[n].replace(name=n.replace("bf16", "fp8"), kv="fp8")
+       for n in ("small_gqa_bf16", "small_mha_bf16", "small_g8_bf16")}
+
+
+@pytest.mark.parametrize("name", sorted(FP8))
+def test_small_workloads_fp8(name, layer_mode):
+    w = FP8[name]
+    _run(w, list(range(w.batch)), fused_layer=layer_mode)
+
+
+@pytest.mark.parametrize("name", sorted(FP8))
+def test_small_workloads_fp8_paged(name):
+    w = FP8[name]
+    _run(w, list(range(w.batch)), paged=True)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,n,paged", [("serve_b32", 3, False), ("long_ctx_b4", 1, False),
+                                          ("hybrid_swa_b64", 2, True)])
+def test_full_size_fp8(name, n, paged):
+    w = W[name].replace(kv="fp8")
+    _run(w, _sample(w, n, seed=13), paged=paged)
+
