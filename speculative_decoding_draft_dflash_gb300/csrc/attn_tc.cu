@@ -24,7 +24,9 @@
 //              (three stages for R <= 64);
 //   9          MMA: S_j = Q K_j^T (two TMEM S buffers), O += P_j V_j (P from
 //              TMEM, V read MN-major from shared memory);
-//   10         TMA: V tiles (released later than K, so on their own thread).
+//   10         TMA: V tiles (released later than K, so on their own thread);
+//   2,3,6,7    fp8 cache with R <= 64 only: V tile conversion to f16 (these warps
+//              serve TMEM lanes 64-127, which then hold no query rows).
 // O is rescaled in TMEM only when a row's running maximum grows by more than
 // 2^8, so almost every tile skips it.
 //
@@ -68,27 +70,35 @@ constexpr int kRing = 4;                   // item ring slots
 // (an 8 KB pad after the last one).
 template <bool NARROW, bool FP8>
 struct Plan {
-  static constexpr uint32_t TILE_B = FP8 ? TK * 128 : TILE;  // one K or V tile
-  static constexpr int K_STAGES = FP8 ? 4 : (NARROW ? 3 : 2);
+  // fp8 with R <= 64: the warps of TMEM lane quarters 2 and 3 hold no query rows, so
+  // they convert each V tile to f16 (zeroing rows past the key range) and the PV MMA
+  // runs as kind::f16 with P in f16: one pack per two values instead of a code split.
+  static constexpr bool CONV = FP8 && NARROW;
+  static constexpr uint32_t TILE_B = FP8 ? TK * 128 : TILE;  // one K or V tile (as loaded)
+  static constexpr int K_STAGES = FP8 ? (CONV ? 3 : 4) : (NARROW ? 3 : 2);
   static constexpr int V_STAGES = FP8 ? 3 : 2;
+  static constexpr int C_STAGES = CONV ? 2 : 0;              // converted (f16) V tiles
   static constexpr uint32_t QPART = NARROW ? 8192 : 16384;   // fp8: code rows of one buffer
   static constexpr uint32_t Q_BYTES = FP8 ? (NARROW ? 4 * QPART + 8192 : 4 * QPART)
                                           : (NARROW ? 40960 : 2 * TILE);
   static constexpr uint32_t Q_TX = FP8 ? 2 * QPART : (NARROW ? TILE / 2 : TILE);  // per Q load
   static constexpr uint32_t OFF_K = Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + K_STAGES * TILE_B;
-  static constexpr uint32_t OFF_BAR = OFF_V + V_STAGES * TILE_B;
+  static constexpr uint32_t OFF_C = OFF_V + V_STAGES * TILE_B;
+  static constexpr uint32_t OFF_BAR = OFF_C + C_STAGES * TILE;
   // mbarrier slots
   static constexpr int B_QF = 0, B_QE = 2, B_KF = 4, B_KE = B_KF + K_STAGES;
   static constexpr int B_VF = B_KE + K_STAGES, B_VE = B_VF + V_STAGES;
-  static constexpr int B_SF = B_VE + V_STAGES, B_SE = B_SF + 2, B_P = B_SE + 2, B_PV = B_P + 1;
+  static constexpr int B_CF = B_VE + V_STAGES, B_CE = B_CF + C_STAGES;
+  static constexpr int B_SF = B_CE + C_STAGES, B_SE = B_SF + 2, B_P = B_SE + 2, B_PV = B_P + 1;
   static constexpr int B_ITF = B_PV + 2, B_ITE = B_ITF + kRing, B_FIN = B_ITE + kRing;
   static constexpr int N_BARS = B_FIN + 1;
   static constexpr uint32_t OFF_RING = OFF_BAR + ((8 * N_BARS + 15) & ~15);
   static constexpr size_t SMEM = 1024 + OFF_RING + 16 * kRing;
-  // O is rescaled only when a row's running maximum grows by more than 2^this. fp8:
-  // P is stored as 64 p, and p <= 4 keeps 64 p inside E4M3's range (448).
-  static constexpr float RESCALE_LOG2 = FP8 ? 2.0f : 8.0f;
+  // O is rescaled only when a row's running maximum grows by more than 2^this. fp8 with
+  // P in E4M3 codes: P is stored as 64 p, and p <= 4 keeps 64 p inside E4M3's range (448).
+  static constexpr bool P_CODES = FP8 && !CONV;
+  static constexpr float RESCALE_LOG2 = P_CODES ? 2.0f : 8.0f;
   __device__ static uint32_t q_base(int buf) {
     return FP8 ? buf * 2 * QPART : (NARROW ? buf * 8192u : buf * TILE);
   }
@@ -169,6 +179,24 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t tmem_d, uint32_t tmem_a, uint
       : "memory");
 }
 
+// Instruction descriptor: kind::f16 with A = B = f16, D = f32, both K-major, M x N.
+constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));  // a -> low half
+  return r;
+}
+
+// Two E4M3 codes (low byte first) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two));
+  return r;
+}
+
 // Instruction descriptor: kind::f8f6f4, A = B = E4M3, D = f32, both K-major, M x N.
 constexpr uint32_t idesc_e4m3_f32(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -212,12 +240,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const int nq = (p.R + 31) >> 5;                 // TMEM lane quarters holding query rows
   const int n_soft = 64 * nq;                     // softmax threads
   const bool soft = warp < kSoftmaxWarps && (warp & 3) < nq;
+  // V converters (PL::CONV): the warps of lane quarters 2 and 3, one key row per thread
+  const bool conv = PL::CONV && warp < kSoftmaxWarps && (warp & 3) >= 2;
+  constexpr int kConv = PL::CONV ? 128 : 0;
   const uint32_t sbase = ptx::smem_u32(smem);
   // barriers (8 bytes each): q 2+2, k and v full+empty per stage, s 2+2, p 1, pv 2,
   // items 4+4, MMA exit 1
   const uint32_t q_full0 = ptx::smem_u32(bars + PL::B_QF), q_empty0 = ptx::smem_u32(bars + PL::B_QE);
   const uint32_t k_full0 = ptx::smem_u32(bars + PL::B_KF), k_empty0 = ptx::smem_u32(bars + PL::B_KE);
   const uint32_t v_full0 = ptx::smem_u32(bars + PL::B_VF), v_empty0 = ptx::smem_u32(bars + PL::B_VE);
+  const uint32_t c_full0 = ptx::smem_u32(bars + PL::B_CF), c_empty0 = ptx::smem_u32(bars + PL::B_CE);
   const uint32_t s_full0 = ptx::smem_u32(bars + PL::B_SF), s_free0 = ptx::smem_u32(bars + PL::B_SE);
   const uint32_t p_full = ptx::smem_u32(bars + PL::B_P), pv_done0 = ptx::smem_u32(bars + PL::B_PV);
   const uint32_t it_full0 = ptx::smem_u32(bars + PL::B_ITF), it_empty0 = ptx::smem_u32(bars + PL::B_ITE);
@@ -238,13 +270,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
     for (int i = 0; i < PL::V_STAGES; ++i) {
       ptx::mbar_init(v_full0 + 8 * i, 1);
-      ptx::mbar_init(v_empty0 + 8 * i, 1);
+      ptx::mbar_init(v_empty0 + 8 * i, PL::CONV ? kConv : 1);  // converters read the tile
+    }
+    for (int i = 0; i < PL::C_STAGES; ++i) {
+      ptx::mbar_init(c_full0 + 8 * i, kConv);
+      ptx::mbar_init(c_empty0 + 8 * i, 1);
     }
     ptx::mbar_init(p_full, n_soft);
     ptx::mbar_init(mma_fin, 1);
     for (int i = 0; i < kRing; ++i) {
       ptx::mbar_init(it_full0 + 8 * i, 1);
-      ptx::mbar_init(it_empty0 + 8 * i, 2 + n_soft);
+      ptx::mbar_init(it_empty0 + 8 * i, 2 + n_soft + kConv);
     }
     ptx::fence_mbar_init();
   }
@@ -356,7 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     if (lane == 0) {
       constexpr uint32_t idesc_s = FP8 ? idesc_e4m3_f32(128, TK) : ptx::idesc_bf16_f32(128, TK);
       constexpr uint32_t idesc_pv =  // V MN-major
-          (FP8 ? idesc_e4m3_f32(128, 128) : ptx::idesc_bf16_f32(128, 128)) | (1u << 16);
+          (PL::P_CODES ? idesc_e4m3_f32(128, 128)
+                       : PL::CONV ? idesc_f16_f32(128, 128) : ptx::idesc_bf16_f32(128, 128)) |
+          (1u << 16);
       int gt = 0;
       bool stop = false, issued = false;
       for (int n = 0; !stop; ++n) {
@@ -400,16 +438,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         };
         if (!issue_s(0) || (T > 1 && !issue_s(1))) break;
         for (int j = 0; j < T; ++j) {
-          const int g = base + j, vs = g % PL::V_STAGES, vu = g / PL::V_STAGES;
+          const int g = base + j;
+          // the V tile: as loaded, or (CONV) its f16 conversion
+          const int vs = PL::CONV ? g % PL::C_STAGES : g % PL::V_STAGES;
+          const int vu = PL::CONV ? g / PL::C_STAGES : g / PL::V_STAGES;
+          const uint32_t vfull = PL::CONV ? c_full0 : v_full0;
           if (!ptx::mbar_wait(p_full, g & 1, &abort_flag, p.status) ||
-              !ptx::mbar_wait(v_full0 + 8 * vs, vu & 1, &abort_flag, p.status)) {
+              !ptx::mbar_wait(vfull + 8 * vs, vu & 1, &abort_flag, p.status)) {
             stop = true;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t va = sbase + PL::OFF_V + vs * PL::TILE_B;
+          const uint32_t va = PL::CONV ? sbase + PL::OFF_C + vs * TILE
+                                       : sbase + PL::OFF_V + vs * PL::TILE_B;
           const uint32_t pa = tmem + TM_P + (g & 1) * 64;
-          if (FP8) {
+          if (PL::P_CODES) {
             // O += Pcodes V + Premainder V: P columns 0-31 and 32-63, 32 keys per K-step
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
@@ -422,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
               mma_bf16_ts(tmem + TM_O, pa + kk * 8, ptx::smem_desc_sw128_mn(va + kk * 2048, HALF),
                           idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
           }
-          ptx::mma_commit(v_empty0 + 8 * vs);
+          ptx::mma_commit((PL::CONV ? c_empty0 : v_empty0) + 8 * vs);
           ptx::mma_commit(pv_done0 + 8 * (g & 1));
           if (j + 2 < T && !issue_s(j + 2)) {
             stop = true;
@@ -437,6 +480,58 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         ptx::mma_commit(mma_fin);
         drain(mma_fin, 0, p.status);
       }
+    }
+  } else if (conv) {
+    // ---------------------------------------------------- V conversion (E4M3 -> f16)
+    // thread = key row k of the tile: 8 chunks of 16 codes -> 16 chunks of 8 f16 values,
+    // both tiles in the 128-byte swizzled layout the MMA reads (chunk c of row k at
+    // c ^ (k & 7)); rows past the key range are written as zeros
+    const int k = (warp >> 2) * 64 + ((warp & 3) - 2) * 32 + lane;
+    const int sw = k & 7;
+    int gv = 0;
+    for (int n = 0;; ++n) {
+      const int slot = n % kRing;
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(it_full0 + 8 * slot, (n / kRing) & 1, &abort_flag, p.status)))
+        break;
+      const int4 it = ring[slot];
+      ptx::mbar_arrive(it_empty0 + 8 * slot);
+      if (it.x < 0) break;
+      const int T = (it.z - it.y + TK - 1) / TK;
+      bool alive = true;
+      for (int j = 0; j < T; ++j) {
+        const int g = gv + j, vs = g % PL::V_STAGES, cs = g % PL::C_STAGES;
+        alive = __all_sync(0xffffffffu, ptx::mbar_wait(v_full0 + 8 * vs, (g / PL::V_STAGES) & 1,
+                                                       &abort_flag, p.status));
+        if (alive && g >= PL::C_STAGES)
+          alive = __all_sync(0xffffffffu, ptx::mbar_wait(c_empty0 + 8 * cs, ((g / PL::C_STAGES) - 1) & 1,
+                                                         &abort_flag, p.status));
+        if (!alive) break;
+        const uint8_t* src = smem + PL::OFF_V + vs * PL::TILE_B + k * 128;
+        uint8_t* dst = smem + PL::OFF_C + cs * TILE + k * 128;
+        const bool valid = it.y + j * TK + k < it.z;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 x = valid ? *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4))
+                                : make_uint4(0, 0, 0, 0);
+          uint4 lo, hi;
+          lo.x = e4m3x2_to_f16x2(x.x);
+          lo.y = e4m3x2_to_f16x2(x.x >> 16);
+          lo.z = e4m3x2_to_f16x2(x.y);
+          lo.w = e4m3x2_to_f16x2(x.y >> 16);
+          hi.x = e4m3x2_to_f16x2(x.z);
+          hi.y = e4m3x2_to_f16x2(x.z >> 16);
+          hi.z = e4m3x2_to_f16x2(x.w);
+          hi.w = e4m3x2_to_f16x2(x.w >> 16);
+          const int h = c >> 2, c2 = 2 * (c & 3);  // f16 half (64 dims) and its chunk
+          *reinterpret_cast<uint4*>(dst + h * HALF + ((c2 ^ sw) << 4)) = lo;
+          *reinterpret_cast<uint4*>(dst + h * HALF + (((c2 + 1) ^ sw) << 4)) = hi;
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(c_full0 + 8 * cs);
+        ptx::mbar_arrive(v_empty0 + 8 * vs);
+      }
+      if (!alive) break;
+      gv += T;
     }
   } else if (soft) {
     // ---------------------------------------------------- softmax
@@ -506,8 +601,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           m_ref = mx;
           resc = true;
         }
-        // fp8: P = 64 p (2^6), whose small values stay normal E4M3 numbers
-        const float mu = ((m_ref == -INFINITY) ? 0.f : m_ref) - (FP8 ? 6.f : 0.f);
+        // P in E4M3 codes: P = 64 p (2^6), whose small values stay normal E4M3 numbers
+        const float mu = ((m_ref == -INFINITY) ? 0.f : m_ref) - (PL::P_CODES ? 6.f : 0.f);
         const float2 sl2v = make_float2(p.sl2, p.sl2), nmu = make_float2(-mu, -mu);
         float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                           make_float2(0.f, 0.f)};
@@ -517,11 +612,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), sl2v, nmu);
           const float2 y = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
           acc2[(e >> 1) & 3] = __fadd2_rn(acc2[(e >> 1) & 3], y);
-          if (FP8) {
+          if (PL::P_CODES) {
             s[e] = y.x;
             s[e + 1] = y.y;
           } else {
-            pk[e >> 1] = pack_bf16(y.x, y.y);
+            pk[e >> 1] = PL::CONV ? pack_f16(y.x, y.y) : pack_bf16(y.x, y.y);
           }
         }
         const float2 a01 = __fadd2_rn(acc2[0], acc2[1]), a23 = __fadd2_rn(acc2[2], acc2[3]);
@@ -548,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           if (!alive) break;
           ptx::tc_fence_after();
         }
-        if (FP8) {
+        if (PL::P_CODES) {
           // codes of P (columns 0-31 of the buffer) and of its remainder (32-63)
           uint32_t hi[NCOL / 4], lo[NCOL / 4];
 #pragma unroll
@@ -563,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         // keys past the range end in the last tile: zero their V rows (slots past the
         // cache length may hold anything, and 0 * NaN would poison O)
         const int nvalid = it.z - (it.y + j * TK);
-        if (j == T - 1 && nvalid < TK) {
+        if (!PL::CONV && j == T - 1 && nvalid < TK) {
           const int vs = g % PL::V_STAGES, vu = g / PL::V_STAGES;
           alive = __all_sync(0xffffffffu, ptx::mbar_wait(v_full0 + 8 * vs, vu & 1, &abort_flag, p.status));
           if (!alive) break;
