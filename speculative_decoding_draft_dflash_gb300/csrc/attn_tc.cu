@@ -20,13 +20,16 @@
 //              and S columns 64(w/4)..+63: two threads per row, exchanging the
 //              tile maximum and the row sum through shared memory. P (bf16) is
 //              stored into TMEM and read from there by the PV MMA.
-//   8          TMA: the Q tile of each item (double-buffered) and K tiles
+//   8 (6)      TMA: the Q tile of each item (double-buffered) and K tiles
 //              (three stages for R <= 64);
-//   9          MMA: S_j = Q K_j^T (two TMEM S buffers), O += P_j V_j (P from
-//              TMEM, V read MN-major from shared memory);
+//   9 (7)      MMA: S_j = Q K_j^T (two TMEM S buffers), O += P_j V_j (P from
+//              TMEM, V read MN-major from shared memory); S_{j+2} is issued
+//              before PV_j;
 //   10         TMA: V tiles (released later than K, so on their own thread);
 //   2,3,6,7    fp8 cache with R <= 64 only: V tile conversion to f16 (these warps
 //              serve TMEM lanes 64-127, which then hold no query rows).
+// In parentheses: the warp for a bf16 cache with R <= 64, which keeps these
+// single-thread roles off the two sub-partitions the softmax then runs on.
 // O is rescaled in TMEM only when a row's running maximum grows by more than
 // 2^8, so almost every tile skips it.
 //
@@ -54,7 +57,6 @@ constexpr uint32_t TILE = 128 * 128 * 2;   // 32 KB: one bf16 K or V tile (128 k
 constexpr uint32_t HALF = TILE / 2;        // one 64-column swizzled box
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
-constexpr int WARP_KQ = 8, WARP_MMA = 9, WARP_V = 10;
 constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 384;  // TMEM columns: S[2], O, P[2] (64 each)
 constexpr int kRing = 4;                   // item ring slots
 
@@ -74,8 +76,16 @@ struct Plan {
   // they convert each V tile to f16 (zeroing rows past the key range) and the PV MMA
   // runs as kind::f16 with P in f16: one pack per two values instead of a code split.
   static constexpr bool CONV = FP8 && NARROW;
+  // Warp roles. A warp issues on sub-partition (warp % 4), and only the warps of
+  // sub-partition q can touch TMEM lanes 32q..32q+31. With R <= 64 the softmax lives on
+  // sub-partitions 0-1. bf16: the K/Q producer and the MMA issuer then move to warps 6
+  // and 7 (sub-partitions 2-3) instead of competing with the softmax for issue slots,
+  // and warps 8, 9 stay idle. fp8: warps 2, 3, 6 and 7 convert V (one key row per
+  // thread), which needs all four; the producer and issuer stay on 8 and 9.
+  static constexpr int W_KQ = NARROW && !CONV ? 6 : 8, W_MMA = NARROW && !CONV ? 7 : 9;
+  static constexpr int W_V = 10;
   static constexpr uint32_t TILE_B = FP8 ? TK * 128 : TILE;  // one K or V tile (as loaded)
-  static constexpr int K_STAGES = FP8 ? (CONV ? 3 : 4) : (NARROW ? 3 : 2);
+  static constexpr int K_STAGES = FP8 ? 4 : (NARROW ? 3 : 2);
   static constexpr int V_STAGES = FP8 ? 3 : 2;
   static constexpr int C_STAGES = CONV ? 2 : 0;              // converted (f16) V tiles
   static constexpr uint32_t QPART = NARROW ? 8192 : 16384;   // fp8: code rows of one buffer
@@ -90,7 +100,7 @@ struct Plan {
   static constexpr int B_QF = 0, B_QE = 2, B_KF = 4, B_KE = B_KF + K_STAGES;
   static constexpr int B_VF = B_KE + K_STAGES, B_VE = B_VF + V_STAGES;
   static constexpr int B_CF = B_VE + V_STAGES, B_CE = B_CF + C_STAGES;
-  static constexpr int B_SF = B_CE + C_STAGES, B_SE = B_SF + 2, B_P = B_SE + 2, B_PV = B_P + 1;
+  static constexpr int B_SF = B_CE + C_STAGES, B_SE = B_SF + 2, B_P = B_SE + 2, B_PV = B_P + 2;
   static constexpr int B_ITF = B_PV + 2, B_ITE = B_ITF + kRing, B_FIN = B_ITE + kRing;
   static constexpr int N_BARS = B_FIN + 1;
   static constexpr uint32_t OFF_RING = OFF_BAR + ((8 * N_BARS + 15) & ~15);
@@ -244,14 +254,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const bool conv = PL::CONV && warp < kSoftmaxWarps && (warp & 3) >= 2;
   constexpr int kConv = PL::CONV ? 128 : 0;
   const uint32_t sbase = ptx::smem_u32(smem);
-  // barriers (8 bytes each): q 2+2, k and v full+empty per stage, s 2+2, p 1, pv 2,
+  // barriers (8 bytes each): q 2+2, k and v full+empty per stage, s 2+2, p 2, pv 2,
   // items 4+4, MMA exit 1
   const uint32_t q_full0 = ptx::smem_u32(bars + PL::B_QF), q_empty0 = ptx::smem_u32(bars + PL::B_QE);
   const uint32_t k_full0 = ptx::smem_u32(bars + PL::B_KF), k_empty0 = ptx::smem_u32(bars + PL::B_KE);
   const uint32_t v_full0 = ptx::smem_u32(bars + PL::B_VF), v_empty0 = ptx::smem_u32(bars + PL::B_VE);
   const uint32_t c_full0 = ptx::smem_u32(bars + PL::B_CF), c_empty0 = ptx::smem_u32(bars + PL::B_CE);
   const uint32_t s_full0 = ptx::smem_u32(bars + PL::B_SF), s_free0 = ptx::smem_u32(bars + PL::B_SE);
-  const uint32_t p_full = ptx::smem_u32(bars + PL::B_P), pv_done0 = ptx::smem_u32(bars + PL::B_PV);
+  const uint32_t p_full0 = ptx::smem_u32(bars + PL::B_P), pv_done0 = ptx::smem_u32(bars + PL::B_PV);
   const uint32_t it_full0 = ptx::smem_u32(bars + PL::B_ITF), it_empty0 = ptx::smem_u32(bars + PL::B_ITE);
   const uint32_t mma_fin = ptx::smem_u32(bars + PL::B_FIN);
 
@@ -276,7 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       ptx::mbar_init(c_full0 + 8 * i, kConv);
       ptx::mbar_init(c_empty0 + 8 * i, 1);
     }
-    ptx::mbar_init(p_full, n_soft);
+    // one per P buffer: the softmax may finish tiles g and g + 1 before the MMA thread
+    // looks for tile g, but not tile g + 2 (that needs PV_g)
+    ptx::mbar_init(p_full0, n_soft);
+    ptx::mbar_init(p_full0 + 8, n_soft);
     ptx::mbar_init(mma_fin, 1);
     for (int i = 0; i < kRing; ++i) {
       ptx::mbar_init(it_full0 + 8 * i, 1);
@@ -284,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
     ptx::fence_mbar_init();
   }
-  if (warp == WARP_MMA) {
+  if (warp == PL::W_MMA) {
     ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), 512);
     ptx::tmem_relinquish();
   }
@@ -293,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == WARP_KQ) {
+  if (warp == PL::W_KQ) {
     // ---------------------------------------------------- item fetch, Q and K loads
     if (lane == 0) {
       ptx::prefetch_tmap(&p.q);
@@ -353,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (int g = gk > PL::K_STAGES ? gk - PL::K_STAGES : 0; g < gk; ++g)
         drain(k_full0 + 8 * (g % PL::K_STAGES), (g / PL::K_STAGES) & 1, p.status);
     }
-  } else if (warp == WARP_V) {
+  } else if (warp == PL::W_V) {
     // ---------------------------------------------------- V loads
     if (lane == 0) {
       const uint64_t pol = ptx::policy_evict_first();
@@ -387,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (int g = gv > PL::V_STAGES ? gv - PL::V_STAGES : 0; g < gv; ++g)
         drain(v_full0 + 8 * (g % PL::V_STAGES), (g / PL::V_STAGES) & 1, p.status);
     }
-  } else if (warp == WARP_MMA) {
+  } else if (warp == PL::W_MMA) {
     // ---------------------------------------------------- MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc_s = FP8 ? idesc_e4m3_f32(128, TK) : ptx::idesc_bf16_f32(128, TK);
@@ -438,12 +451,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         };
         if (!issue_s(0) || (T > 1 && !issue_s(1))) break;
         for (int j = 0; j < T; ++j) {
+          // S of tile j + 2 goes first: its buffer is free once the softmax has read S_j
+          // (early in that tile's softmax), while PV_j waits for the end of it; issued the
+          // other way round, each S would queue behind a PV that waited for a softmax.
+          if (j + 2 < T && !issue_s(j + 2)) {
+            stop = true;
+            break;
+          }
           const int g = base + j;
           // the V tile: as loaded, or (CONV) its f16 conversion
           const int vs = PL::CONV ? g % PL::C_STAGES : g % PL::V_STAGES;
           const int vu = PL::CONV ? g / PL::C_STAGES : g / PL::V_STAGES;
           const uint32_t vfull = PL::CONV ? c_full0 : v_full0;
-          if (!ptx::mbar_wait(p_full, g & 1, &abort_flag, p.status) ||
+          if (!ptx::mbar_wait(p_full0 + 8 * (g & 1), (g >> 1) & 1, &abort_flag, p.status) ||
               !ptx::mbar_wait(vfull + 8 * vs, vu & 1, &abort_flag, p.status)) {
             stop = true;
             break;
@@ -467,10 +487,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           }
           ptx::mma_commit((PL::CONV ? c_empty0 : v_empty0) + 8 * vs);
           ptx::mma_commit(pv_done0 + 8 * (g & 1));
-          if (j + 2 < T && !issue_s(j + 2)) {
-            stop = true;
-            break;
-          }
         }
         gt = base + T;
       }
@@ -676,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           ptx::fence_proxy_async_smem();
         }
         ptx::tc_fence_before();
-        ptx::mbar_arrive(p_full);
+        ptx::mbar_arrive(p_full0 + 8 * sb);
       }
       if (!alive) break;
       gt += T;
@@ -723,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == WARP_MMA) {
+  if (warp == PL::W_MMA) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
