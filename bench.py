@@ -165,10 +165,7 @@ def measured_traffic(kernel):
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic_serve_b32.json")) as f:
-            rec = json.load(f)
-        if rec.get("run") != TRAFFIC_RUN:
-            return None
-        t = rec[kernel]
+            t = json.load(f)["runs"][TRAFFIC_RUN][kernel]
         with open(os.path.join(ROOT, t["source"]), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest()[:16] != t["sha256_16"]:
                 return None
