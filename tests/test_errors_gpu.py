@@ -13,15 +13,16 @@ def _dev(w, **kw):
     return DeviceWorkload(w, **kw)
 
 
-def _tiny():
+def _tiny(kv="bf16"):
     return synth.WORKLOADS["serve_b32"].replace(
         name="tiny", d=256, n_h=4, n_kv=2, k=1, batch=3, n_layers=1, windows=(0,),
-        prefill_lo=10, prefill_hi=60, rounds=1, seed=9)
+        prefill_lo=10, prefill_hi=60, rounds=1, seed=9, kv=kv)
 
 
-def test_capacity_overflow_skips_sequence_and_flags(layer_mode):
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_capacity_overflow_skips_sequence_and_flags(layer_mode, kv):
     from speculative_decoding_draft_dflash_gb300 import dflash as D
-    w = _tiny()
+    w = _tiny(kv)
     L0 = synth.prefill_lens(w)
     cap = int(L0.max()) + 10          # the longest sequence cannot take its 16 context rows
     dev = _dev(w, capacity=cap)
@@ -60,9 +61,10 @@ def test_crop_beyond_length_refused():
     assert dev.cache.lens.cpu().numpy()[0].tolist() == [L0[0], 0, 0]
 
 
-def test_rope_table_too_short_flags(layer_mode):
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_rope_table_too_short_flags(layer_mode, kv):
     from speculative_decoding_draft_dflash_gb300 import dflash as D
-    w = _tiny()
+    w = _tiny(kv)
     dev = _dev(w)
     L0 = synth.prefill_lens(w)
     x = dev.round_inputs(1, L0)
@@ -115,3 +117,19 @@ def test_ragged_inject_with_empty_sequences():
         gv = dev.cache.rows("v", 0, b, L0[b], L0[b] + counts[b]).float().cpu().numpy()
         harness.check_close(gk, K, w.dtype, f"K seq {b}")
         harness.check_close(gv, V, w.dtype, f"V seq {b}")
+
+
+def test_fp8_refused_rows_leave_cache_untouched():
+    """A refused append writes no code: the fp8 cache bytes past a refused sequence's
+    length keep their previous content (the zeros the cache was created with)."""
+    from speculative_decoding_draft_dflash_gb300 import dflash as D
+    w = _tiny("fp8")
+    L0 = synth.prefill_lens(w)
+    cap = int(L0.max()) + 10
+    dev = _dev(w, capacity=cap)
+    x = dev.round_inputs(1, L0)
+    dev.run_round(x, crop=False)
+    assert D.dflash_status_get() & D.DEV_CAPACITY
+    b = int(np.argmax(L0))
+    tail = dev.cache.k[0, b, :, int(L0[b]):]
+    assert torch.all(tail == 0)
