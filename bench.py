@@ -400,6 +400,8 @@ def run_ours(args, w):
     prefill = run_prefill_gemms(args, w, dev, stream, D, pk) if w.prefill_inject and extras else None
     bookkeeping = time_accept(args, w, stream, D) if extras else None
     layer_rest = time_layer_out(args, w, stream, D, pk) if w.dtype == "bf16" and extras else None
+    fp8 = (time_fp8_cache(args, w, stream, D, pk)
+           if w.dtype == "bf16" and w.kv == "bf16" and extras and world == 1 else None)
 
     # ---- end to end: host inputs in, host results out, through the same calls ----
     e2e = run_e2e(args, w, dev, x, stream, D)
@@ -418,6 +420,8 @@ def run_ours(args, w):
                       "eager launches; kernel durations from a second traced pass"}
     if prefill is not None:
         line["prefill_gemms"] = prefill
+    if fp8 is not None:
+        line["kv_fp8"] = fp8
     if bookkeeping is not None:
         line["bookkeeping"] = bookkeeping
     if layer_rest is not None:
@@ -539,6 +543,58 @@ def run_prefill_gemms(args, w, dev, stream, D, pk):
     for name in ("gemm_fc", "gemm_kv"):
         if name in kernels:
             out[name] = {**roofline_for(name, kernels, costs, 0, pk), "avg_us": kernels[name]["avg_us"]}
+    return out
+
+
+def time_fp8_cache(args, w, stream, D, pk):
+    """The same draft round on an fp8 (E4M3) cache: step rate, and the attention's duration
+    and HBM fraction with the cache read at one byte per element (a second device copy of
+    the workload; the bf16 one above is left as it was)."""
+    import torch
+    from speculative_decoding_draft_dflash_gb300 import synth
+    from speculative_decoding_draft_dflash_gb300.runner import DeviceWorkload
+    w8 = w.replace(kv="fp8")
+    dev = DeviceWorkload(w8, paged=args.paged)
+    L0 = synth.prefill_lens(w8)
+    x = dev.round_inputs(1, L0, counts=np.full(w8.batch, w8.new_ctx, dtype=np.int64), crop_to=L0)
+    step = lambda: dev.run_round(x, crop=True, stream=stream)  # noqa: E731
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = max(10, min(args.steps, 50))
+
+    def capture(k):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(k):
+                step()
+        return g
+
+    g = capture(n)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    D.dflash_trace_start(["attention"], 4 * n * w8.n_layers)
+    gT = capture(n)
+    gT.replay()
+    torch.cuda.synchronize()
+    att = [t for k, t in D.dflash_trace_stop() if k == "attention"]
+    assert D.dflash_status_get(stream) == 0, "device status after the fp8 cache run"
+    avg = sum(att) / max(1, len(att))
+    by = mean_attention_bytes(w8, L0 + w8.new_ctx)
+    ach = by / (avg * 1e-3) / 1e9
+    out = {"value": whole_job_rate(1, w8, ms), "unit": UNIT, "ms_per_step": ms, "steps": n,
+           "attention": {"avg_us": 1e3 * avg, "algorithmic_bytes_per_launch": by,
+                         "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / pk["hbm_gbs"]},
+           "cache": "E4M3 codes, one scale per layer for K and for V"}
+    del dev
+    torch.cuda.empty_cache()
     return out
 
 
