@@ -378,6 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const int4 it = ring[slot];
         ptx::mbar_arrive(it_empty0 + 8 * slot);
         if (it.x < 0) break;
+        // At the start every CTA asks HBM for its first tiles at once, and the first S
+        // needs only Q and K_0: V waits until K_0 has landed, so that it is not queued
+        // ahead of it (V_0 is needed only after the first tile's softmax).
+        if (n == 0 && !ptx::mbar_wait(k_full0, 0, &abort_flag, p.status)) break;
         const int b = it.x / p.n_kv, kvh = it.x - b * p.n_kv;
         const int ntiles = (it.z - it.y + TK - 1) / TK;
         int row_next = tile_row(p, b, kvh, it.y);
