@@ -125,7 +125,7 @@ struct AttnTcParams {
   int32_t* lens;          // [batch]: receives lens_new once the attention is done
   const int32_t* lens_new;
   bf16* out;
-  float* part_acc;       // [pair][max_splits][R][128]
+  float* part_acc;       // [pair][max_splits][R][128] bf16: a split's normalised output
   float2* part_ml;       // [pair][max_splits][R]
   const int4* items;     // {pair, k_begin, k_end, split (-1 = whole range)}
   const int* n_items;
@@ -731,12 +731,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           reinterpret_cast<uint4*>(orow)[k] = w;
         }
       } else {
+        // a split range's partial: its normalised output O / l (bf16, like the final rows)
+        // and its (maximum, sum); the combine weights each by 2^(max - M) * sum
         const size_t prow = ((size_t)it.x * p.max_splits + it.w) * p.R + rt;
-        float4* a = reinterpret_cast<float4*>(p.part_acc + prow * 128 + coff);
-        const float vsc = FP8 ? p.v_scale : 1.f;
+        bf16* a = reinterpret_cast<bf16*>(p.part_acc) + prow * 128 + coff;
+        const float inv = l > 0.f ? (FP8 ? p.v_scale : 1.f) / l : 0.f;
 #pragma unroll
-        for (int k = 0; k < NCOL / 4; ++k)
-          a[k] = make_float4(s[4 * k] * vsc, s[4 * k + 1] * vsc, s[4 * k + 2] * vsc, s[4 * k + 3] * vsc);
+        for (int k = 0; k < NCOL / 8; ++k) {
+          uint4 w;
+          w.x = pack_bf16(s[8 * k + 0] * inv, s[8 * k + 1] * inv);
+          w.y = pack_bf16(s[8 * k + 2] * inv, s[8 * k + 3] * inv);
+          w.z = pack_bf16(s[8 * k + 4] * inv, s[8 * k + 5] * inv);
+          w.w = pack_bf16(s[8 * k + 6] * inv, s[8 * k + 7] * inv);
+          reinterpret_cast<uint4*>(a)[k] = w;
+        }
         if (half == 0) p.part_ml[prow] = make_float2(m_ref, l);
       }
     }
@@ -762,16 +770,16 @@ __device__ __forceinline__ void combine_row(const AttnTcParams& p, const int* sp
   bf16* orow = p.out + ((size_t)(b * p.bs + t) * p.n_h + kvh * p.G + gq) * 128;
   float o[4] = {0.f, 0.f, 0.f, 0.f};
   if (n > 1) {
-    // row maximum and sum over the splits, lane-strided, then the weighted rows; the
-    // rows of the first kPre splits are requested before the (max, sum) pairs are read
+    // each split holds its normalised output (bf16) and (max, sum): the row is
+    // sum_c w_c out_c / sum_c w_c with w_c = 2^(max_c - M) sum_c. Lane-strided (max, sum)
+    // reductions; the rows of the first kPre splits are requested before them.
     constexpr int kPre = 4;
     const size_t base = (size_t)pr * p.max_splits * p.R + r;
-    const float4* acc = reinterpret_cast<const float4*>(p.part_acc + base * 128) + lane;
-    const size_t acc_stride4 = (size_t)p.R * 32;  // one split, in float4
-    float4 pre[kPre];
+    const uint2* acc = reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(p.part_acc) + base * 128) + lane;
+    const size_t acc_stride = (size_t)p.R * 32;  // one split, in 4-value groups
+    uint2 pre[kPre];
 #pragma unroll
-    for (int c = 0; c < kPre; ++c)
-      pre[c] = c < n ? acc[c * acc_stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < kPre; ++c) pre[c] = c < n ? acc[c * acc_stride] : make_uint2(0u, 0u);
     float M = -INFINITY;
     for (int c = lane; c < n; c += 32) M = fmaxf(M, p.part_ml[base + (size_t)c * p.R].x);
     M = warp_max(M);
@@ -781,19 +789,21 @@ __device__ __forceinline__ void combine_row(const AttnTcParams& p, const int* sp
       if (ml.y > 0.f) L += ptx::ex2(ml.x - M) * ml.y;
     }
     L = warp_sum(L);
-    auto add = [&](int c, const float4& x) {
+    auto add = [&](int c, const uint2& x) {
       const float2 ml = p.part_ml[base + (size_t)c * p.R];
-      const float w = ml.y > 0.f ? ptx::ex2(ml.x - M) : 0.f;
-      o[0] += w * x.x;
-      o[1] += w * x.y;
-      o[2] += w * x.z;
-      o[3] += w * x.w;
+      const float w = ml.y > 0.f ? ptx::ex2(ml.x - M) * ml.y : 0.f;
+      const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
+      const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
+      o[0] += w * v01.x;
+      o[1] += w * v01.y;
+      o[2] += w * v23.x;
+      o[3] += w * v23.y;
     };
 #pragma unroll
     for (int c = 0; c < kPre; ++c)
       if (c < n) add(c, pre[c]);
 #pragma unroll 4
-    for (int c = kPre; c < n; ++c) add(c, acc[c * acc_stride4]);
+    for (int c = kPre; c < n; ++c) add(c, acc[c * acc_stride]);
     const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[e] *= inv;
