@@ -316,7 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const uint64_t pol = ptx::policy_evict_first();
       const int n_items = *p.n_items;
       int gk = 0, n = 0, nq_loads = 0;
-      int idx = atomicAdd(p.next_item, 1);
+      // the first wave takes items 0 .. grid - 1 in CTA order (the list's largest, which
+      // the counter would hand out first anyway) without a round trip to the counter
+      int idx = blockIdx.x;
       bool stop = false;
       for (;; ++n) {
         const int slot = n % kRing;
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         ring[slot] = it;
         ptx::mbar_arrive(it_full0 + 8 * slot);  // release: the ring entry is visible to waiters
         if (it.x < 0) break;
-        idx = atomicAdd(p.next_item, 1);         // prefetch the next item's index
+        idx = gridDim.x + atomicAdd(p.next_item, 1);  // prefetch the next item's index
         const int b = it.x / p.n_kv, kvh = it.x - b * p.n_kv;
         const int qb = n & 1;
         if (n >= 2 && !ptx::mbar_wait(q_empty0 + 8 * qb, ((n >> 1) - 1) & 1, &abort_flag, p.status))
