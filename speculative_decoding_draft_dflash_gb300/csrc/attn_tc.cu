@@ -11,8 +11,10 @@
 //                          (sequence, KV head) key range into work items of
 //                          near-equal 128-key tiles, sized so the GPU gets a
 //                          few items per SM, and lists them longest first;
-//   attn_tc_kernel         persistent, one CTA per SM, items fetched with an
-//                          atomic counter (greedy longest-first);
+//   attn_tc_kernel         persistent, one CTA per SM; CTA i starts with item i,
+//                          later items come from an atomic counter (greedy
+//                          longest-first). A split range leaves its output
+//                          normalised in bf16 with its (max, sum);
 //   attn_combine_kernel    merges the partial results of split ranges.
 //
 // attn_tc_kernel roles (warp: job):
@@ -25,7 +27,8 @@
 //   9 (7)      MMA: S_j = Q K_j^T (two TMEM S buffers), O += P_j V_j (P from
 //              TMEM, V read MN-major from shared memory); S_{j+2} is issued
 //              before PV_j;
-//   10         TMA: V tiles (released later than K, so on their own thread);
+//   10         TMA: V tiles (released later than K, so on their own thread;
+//              the first waits for the first K tile, which the first S needs);
 //   2,3,6,7    fp8 cache with R <= 64 only: V tile conversion to f16 (these warps
 //              serve TMEM lanes 64-127, which then hold no query rows).
 // In parentheses: the warp for a bf16 cache with R <= 64, which keeps these
@@ -40,8 +43,10 @@
 // codes and the codes of the remainder (x ~ hi + lo), so S = Q_hi K^T + Q_lo K^T
 // and O += P_hi V + P_lo V: twice the MMAs of half the width, the same tensor
 // time as bf16. P is formed as 64 p with p <= 4 (rescale threshold 2^2), which
-// keeps it inside E4M3's range and its small values normal. The K scale folds
-// into the score scale and the V scale into the output.
+// keeps it inside E4M3's range and its small values normal. With R <= 64 the
+// warps of lane quarters 2-3 convert V to f16 instead and PV runs as kind::f16
+// with P in f16. The K scale folds into the score scale and the V scale into
+// the output.
 #include <float.h>
 
 #include <mutex>
