@@ -10,7 +10,10 @@
 //               frees each stage ("empty" mbarrier) and finally signals "done";
 //   warps 2-5   epilogue: one thread per tile row moves the accumulator from TMEM
 //               (tcgen05.ld of its lanes) into a staging tile in shared memory; then
-//               all six warps store from there with coalesced accesses.
+//               all six warps store from there with coalesced accesses. With the
+//               heads epilogue these warps use the mainloop's time: each resolves its
+//               row's destination and copies the row's RoPE cos/sin into spare TMEM
+//               columns, so the epilogue itself issues no dependent global loads.
 // The activations arrive as up to eight K-segments (the k target layers'
 // hidden states of the context projection), each with its own tensor map;
 // the weights as up to three matrices stacked along N (W_Q | W_K | W_V).
@@ -70,11 +73,13 @@ struct Cfg {
   static constexpr uint32_t B_BYTES = BN * BK * 2;
   static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
-  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + 256;
+  // pipeline stages, barriers (256 B), then gamma_q / gamma_k as fp32 (heads epilogue)
+  static constexpr uint32_t OFF_GAMMA = STAGES * STAGE + 256;
+  static constexpr size_t SMEM = 1024 + (size_t)OFF_GAMMA + 2 * 128 * 4;
   // epilogue staging tile over the stages: BM rows of BN fp32, padded, then row slots
   static constexpr int LD = BN + 4;
   static constexpr uint32_t STG_BYTES = BM * LD * 4;
-  static_assert(STG_BYTES + BM * 16 + BM * 8 <= STAGES * STAGE, "staging tile exceeds the stages");
+  static_assert(STG_BYTES + BM * 16 <= STAGES * STAGE, "staging tile exceeds the stages");
 };
 
 // Waits without honouring the abort flag (used to drain in-flight work before exit).
@@ -184,7 +189,10 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
   constexpr int NH = BN >= 128 ? BN / 128 : 1;                // heads per tile (heads epilogue)
   float* stg = reinterpret_cast<float*>(smem);                // epilogue only
   int4* slots = reinterpret_cast<int4*>(smem + C::STG_BYTES);  // epilogue only
-  float* rnorm = reinterpret_cast<float*>(slots + BM);         // epilogue only: [BM][NH]
+  float* gam = reinterpret_cast<float*>(smem + C::OFF_GAMMA);   // heads: gamma_q, gamma_k
+  // TMEM: the accumulator in columns [0, BN); heads: the row's RoPE (cos, sin) pairs in
+  // [BN, BN + 128)
+  constexpr uint32_t TMEM_COLS = HEADS ? 2 * BN : BN;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -227,7 +235,7 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
     for (int i = 0; i < w_count; ++i) ptx::prefetch_tmap(&bmap[i]);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), BN);
+    ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), TMEM_COLS);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -281,26 +289,84 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
   } else {
     // phase 1: TMEM -> a staging tile in the pipeline's shared memory (free once every
     // MMA is done), one row per thread; rows padded by 4 floats so the float4 stores of a
-    // warp spread over all banks. The row's destination is resolved here too.
+    // warp spread over all banks.
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 are this warp's
     const int row = q * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    float* srow = stg + row * C::LD;
+    RowSlot rs{0, 0, -1, -1};
+    if (HEADS) {
+      // while the MMAs run: the row's destination, gamma, and the row's RoPE pairs
+      // (cos, sin of its position, 128 floats) into TMEM columns BN .. BN + 127
+      if (m0 + row < M) rs = row_slot(ep, m0 + row, n0 == 0);
+      const int et = threadIdx.x - 64;  // 0 .. 127
+      gam[et] = ep.gamma_q ? __bfloat162float(((const bf16*)ep.gamma_q)[et]) : 1.f;
+      gam[128 + et] = ep.gamma_k ? __bfloat162float(((const bf16*)ep.gamma_k)[et]) : 1.f;
+      const bool ropes = n0 / 128 < ep.n_q + ep.n_kv;  // the tile's first head is a Q or K head
+      __syncwarp();  // row_slot's search diverges; tcgen05.st is .sync.aligned
+      if (ropes) {
+        // the table is 8-byte aligned: float2 loads
+        const float2* cs = ep.rope + (size_t)max(rs.pos, 0) * 64;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float2 f = cs[c * 16 + j];
+            v[2 * j] = __float_as_uint(f.x);
+            v[2 * j + 1] = __float_as_uint(f.y);
+          }
+          ptx::tmem_st_32x32b_x32(tmem + lane_base + (uint32_t)(BN + 32 * c), v);
+        }
+        ptx::tmem_st_wait();
+      }
+      ptx::named_sync(2, 128);  // gamma staged by all four warps
+    }
     // warp-uniform: tcgen05.ld below is a .sync.aligned instruction
     const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(done, 0, &abort_flag, p.status));
     ptx::tc_fence_after();
-    if (ok) {
-      float* srow = stg + row * C::LD;
-      float ss[NH] = {};  // per-head sum of squares of this row (heads: RMSNorm)
+    if (ok && !HEADS) {
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
+        ptx::tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)(c * 32), r);
         ptx::tmem_ld_wait();
         float4* d = reinterpret_cast<float4*>(srow + c * 32);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           d[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-        if (HEADS) {
+      }
+    } else if (ok) {
+      // the finished row: per-head RMSNorm (Q, K heads: sum of squares over the head's
+      // 128 dims, then x / rms * gamma) and rotate_half RoPE on the pairs (i, i + 64);
+      // V heads as they are
+      slots[row] = make_int4(rs.b, rs.t, rs.pos, rs.page);
+#pragma unroll 1
+      for (int hd = 0; hd < NH; ++hd) {
+        const int head = n0 / 128 + hd;
+        const int kind = head < ep.n_q ? 0 : (head < ep.n_q + ep.n_kv ? 1 : 2);  // Q, K, V
+        const uint32_t hcol = (uint32_t)(hd * 128);
+        if (kind == 2) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(tmem + lane_base + hcol + (uint32_t)(c * 32), r);
+            ptx::tmem_ld_wait();
+            float4* d = reinterpret_cast<float4*>(srow + hd * 128 + c * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              d[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          }
+          continue;
+        }
+        float ssq = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(tmem + lane_base + hcol + (uint32_t)(c * 32), r);
+          ptx::tmem_ld_wait();
           float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
@@ -309,17 +375,40 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
             a2 = fmaf(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 2]), a2);
             a3 = fmaf(__uint_as_float(r[j + 3]), __uint_as_float(r[j + 3]), a3);
           }
-#pragma unroll
-          for (int h = 0; h < NH; ++h)
-            if (c / 4 == h) ss[h] += (a0 + a1) + (a2 + a3);
+          ssq += (a0 + a1) + (a2 + a3);
         }
-      }
-      if (HEADS) {
-        RowSlot rs{0, 0, -1, -1};
-        if (m0 + row < M) rs = row_slot(ep, m0 + row, n0 == 0);
-        slots[row] = make_int4(rs.b, rs.t, rs.pos, rs.page);
+        const float rn = 1.0f / sqrtf(ssq * (1.0f / 128.f) + ep.eps);
+        const float* g = gam + (kind == 0 ? 0 : 128);
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          // dims i = 32c + e and their partners i + 64, with the pairs' (cos, sin)
+          uint32_t xa[32], xb[32];
+          ptx::tmem_ld_32x32b_x32(tmem + lane_base + hcol + (uint32_t)(c * 32), xa);
+          ptx::tmem_ld_32x32b_x32(tmem + lane_base + hcol + (uint32_t)(64 + c * 32), xb);
 #pragma unroll
-        for (int h = 0; h < NH; ++h) rnorm[row * NH + h] = 1.0f / sqrtf(ss[h] * (1.0f / 128.f) + ep.eps);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t cs[32];
+            ptx::tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)(BN + 64 * c + 32 * hh), cs);
+            ptx::tmem_ld_wait();
+            float ya[16], yb[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int i = 32 * c + 16 * hh + e;
+              const float a = __uint_as_float(xa[16 * hh + e]) * rn * g[i];
+              const float b = __uint_as_float(xb[16 * hh + e]) * rn * g[i + 64];
+              const float co = __uint_as_float(cs[2 * e]), si = __uint_as_float(cs[2 * e + 1]);
+              ya[e] = a * co - b * si;
+              yb[e] = b * co + a * si;
+            }
+            float4* da = reinterpret_cast<float4*>(srow + hd * 128 + 32 * c + 16 * hh);
+            float4* db = reinterpret_cast<float4*>(srow + hd * 128 + 64 + 32 * c + 16 * hh);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              da[j] = make_float4(ya[4 * j], ya[4 * j + 1], ya[4 * j + 2], ya[4 * j + 3]);
+              db[j] = make_float4(yb[4 * j], yb[4 * j + 1], yb[4 * j + 2], yb[4 * j + 3]);
+            }
+          }
+        }
       }
     }
   }
@@ -336,105 +425,48 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
         for (int j = lane; j < BN / 4; j += 32) dst[j] = src[j];
       }
     } else {
-      // one warp per (row, head): lane l holds dims 4l .. 4l+3 and reads its RoPE partner
-      // dims (i +- 64, lane l ^ 16) from the staging tile as well; the norm scale came with
-      // the row. Rows go in batches of RB per warp, all loads of a batch issued first.
-      constexpr int RB = 4;  // rows per batch (two batches of loads in registers)
-      const int lp = lane ^ 16;
-      float gq[4], gk[4], gqp[4], gkp[4];  // gamma of this lane's dims and of its partner's
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        gq[i] = ep.gamma_q ? __bfloat162float(((const bf16*)ep.gamma_q)[4 * lane + i]) : 1.f;
-        gqp[i] = ep.gamma_q ? __bfloat162float(((const bf16*)ep.gamma_q)[4 * lp + i]) : 1.f;
-        gk[i] = ep.gamma_k ? __bfloat162float(((const bf16*)ep.gamma_k)[4 * lane + i]) : 1.f;
-        gkp[i] = ep.gamma_k ? __bfloat162float(((const bf16*)ep.gamma_k)[4 * lp + i]) : 1.f;
-      }
-      const float sg = lane < 16 ? -1.f : 1.f;  // rotate_half: [-x2; x1]
-      // row slots and RoPE rows of batch k + 1 are loaded while batch k computes
-      auto fetch = [&](int r0, int4 (&rs)[RB], float2 (&cs)[RB][4]) {
+      // one warp per (row, head) of the finished rows: lane l stores dims 4l .. 4l+3
+      constexpr int RB = 4;  // rows per batch
+      for (int r0 = warp * RB; r0 < BM; r0 += (kThreads / 32) * RB) {
 #pragma unroll
         for (int i = 0; i < RB; ++i) {
           const int r = r0 + i;
-          rs[i] = r < BM ? slots[r] : make_int4(0, 0, -1, -1);
-          if (m0 + r >= M) rs[i].z = -1;
-        }
-#pragma unroll
-        for (int i = 0; i < RB; ++i) {  // rows that are not written read position 0
-          const float2* c = ep.rope + (size_t)max(rs[i].z, 0) * 64 + 4 * (lane & 15);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) cs[i][j] = c[j];
-        }
-      };
-      constexpr int kStride = (kThreads / 32) * RB;
-      int4 rs[RB];
-      float2 cs[RB][4];
-      if (warp * RB < BM) fetch(warp * RB, rs, cs);
-      for (int r0 = warp * RB; r0 < BM; r0 += kStride) {
-        int4 rs_n[RB];
-        float2 cs_n[RB][4];
-        if (r0 + kStride < BM) fetch(r0 + kStride, rs_n, cs_n);
-        // branch-free over the batch (the units interleave); only the stores are predicated
-        float4 xv[RB][NH], xp[RB][NH];
-#pragma unroll
-        for (int i = 0; i < RB; ++i)
-#pragma unroll
-          for (int hd = 0; hd < NH; ++hd) {
-            const float4* row4 = reinterpret_cast<const float4*>(stg + (r0 + i) * C::LD + hd * 128);
-            xv[i][hd] = row4[lane];
-            xp[i][hd] = row4[lp];
-          }
-#pragma unroll
-        for (int i = 0; i < RB; ++i) {
+          if (r >= BM) break;
+          const int4 rs = slots[r];
+          if (rs.z < 0 || m0 + r >= M) continue;  // warp-uniform
 #pragma unroll
           for (int hd = 0; hd < NH; ++hd) {
             const int head = n0 / 128 + hd;
             const int kind = head < ep.n_q ? 0 : (head < ep.n_q + ep.n_kv ? 1 : 2);  // Q, K, V
-            const bool qh = kind == 0, rot = kind < 2;
-            const float rn = rnorm[(r0 + i) * NH + hd];
-            const float4 x = xv[i][hd], o = xp[i][hd];
-            const float x0 = x.x * rn * (qh ? gq[0] : gk[0]), p0 = o.x * rn * (qh ? gqp[0] : gkp[0]);
-            const float x1 = x.y * rn * (qh ? gq[1] : gk[1]), p1 = o.y * rn * (qh ? gqp[1] : gkp[1]);
-            const float x2 = x.z * rn * (qh ? gq[2] : gk[2]), p2 = o.z * rn * (qh ? gqp[2] : gkp[2]);
-            const float x3 = x.w * rn * (qh ? gq[3] : gk[3]), p3 = o.w * rn * (qh ? gqp[3] : gkp[3]);
-            const float y0 = rot ? x0 * cs[i][0].x + sg * p0 * cs[i][0].y : x.x;
-            const float y1 = rot ? x1 * cs[i][1].x + sg * p1 * cs[i][1].y : x.y;
-            const float y2 = rot ? x2 * cs[i][2].x + sg * p2 * cs[i][2].y : x.z;
-            const float y3 = rot ? x3 * cs[i][3].x + sg * p3 * cs[i][3].y : x.w;
+            const bool qh = kind == 0;
+            const float4 y = reinterpret_cast<const float4*>(stg + r * C::LD + hd * 128)[lane];
             const int kvh = head - ep.n_q - (kind == 2 ? ep.n_kv : 0);
             // element offset of the destination row (Q, or the cache slot)
             const size_t eoff =
-                qh ? (((size_t)rs[i].x * ep.n_q + head) * ep.bs + rs[i].y) * 128
-                   : (rs[i].w >= 0 ? ((size_t)rs[i].w * ep.n_kv + kvh) * 128 + (rs[i].z & 127)
-                                   : ((size_t)rs[i].x * ep.n_kv + kvh) * ep.capacity + rs[i].z) * 128;
+                qh ? (((size_t)rs.x * ep.n_q + head) * ep.bs + rs.y) * 128
+                   : (rs.w >= 0 ? ((size_t)rs.w * ep.n_kv + kvh) * 128 + (rs.z & 127)
+                                : ((size_t)rs.x * ep.n_kv + kvh) * ep.capacity + rs.z) * 128;
             char* kvbase = (char*)(kind == 1 ? ep.cache_k : ep.cache_v);
             if (ep.kv_fp8) {
               // E4M3 rows: Q as codes + remainder codes, K / V as codes of x / scale
               if (qh) {
                 uint32_t hi, lo;
-                e4m3x4_split(y0, y1, y2, y3, hi, lo);
-                if (rs[i].z >= 0) {
-                  reinterpret_cast<uint32_t*>((char*)ep.q_out + eoff)[lane] = hi;
-                  reinterpret_cast<uint32_t*>((char*)ep.q_lo + eoff)[lane] = lo;
-                }
+                e4m3x4_split(y.x, y.y, y.z, y.w, hi, lo);
+                reinterpret_cast<uint32_t*>((char*)ep.q_out + eoff)[lane] = hi;
+                reinterpret_cast<uint32_t*>((char*)ep.q_lo + eoff)[lane] = lo;
               } else {
                 const float inv = kind == 1 ? ep.k_inv : ep.v_inv;
-                const uint32_t c = e4m3x4(y0 * inv, y1 * inv, y2 * inv, y3 * inv);
-                if (rs[i].z >= 0) reinterpret_cast<uint32_t*>(kvbase + eoff)[lane] = c;
+                reinterpret_cast<uint32_t*>(kvbase + eoff)[lane] =
+                    e4m3x4(y.x * inv, y.y * inv, y.z * inv, y.w * inv);
               }
             } else {
               bf16* dst = qh ? (bf16*)ep.q_out + eoff : (bf16*)kvbase + eoff;
               uint2 w2;
-              w2.x = pack_bf16(y0, y1);
-              w2.y = pack_bf16(y2, y3);
-              if (rs[i].z >= 0) reinterpret_cast<uint2*>(dst)[lane] = w2;
+              w2.x = pack_bf16(y.x, y.y);
+              w2.y = pack_bf16(y.z, y.w);
+              reinterpret_cast<uint2*>(dst)[lane] = w2;
             }
           }
-        }
-#pragma unroll
-        for (int i = 0; i < RB; ++i) {
-          rs[i] = rs_n[i];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) cs[i][j] = cs_n[i][j];
         }
       }
     }
@@ -443,7 +475,7 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, BN);
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
