@@ -10,24 +10,26 @@
 //               frees each stage ("empty" mbarrier) and finally signals "done";
 //   warps 2-5   epilogue: one thread per tile row moves the accumulator from TMEM
 //               (tcgen05.ld of its lanes) into a staging tile in shared memory; then
-//               all six warps store from there with coalesced accesses. With the
-//               heads epilogue these warps use the mainloop's time: each resolves its
-//               row's destination and copies the row's RoPE cos/sin into spare TMEM
+//               the CTA's threads copy the staged rows out. With the heads epilogue
+//               these warps use the mainloop's time: each resolves its row's
+//               destination and copies the row's RoPE cos/sin into spare TMEM
 //               columns, so the epilogue itself issues no dependent global loads.
 // The activations arrive as up to eight K-segments (the k target layers'
 // hidden states of the context projection), each with its own tensor map;
 // the weights as up to three matrices stacked along N (W_Q | W_K | W_V).
 //
-// Two epilogues:
+// Two epilogues, both leaving the staged tile by bulk copies (cp.async.bulk, one per
+// contiguous destination row), so the store phase costs a few instructions per row:
 //   fp32 store   the tile (a split-K partial) goes to Y; the context
 //                projection's RMSNorm kernel sums the splits;
 //   heads        (no split-K) whole 128-dim heads per tile (BN = 128 or 256).
-//                A warp per (row, head) applies the per-head RMSNorm (Q and K
-//                heads), rotates the pair (i, i + 64) at the row's absolute
-//                position and stores the bf16 row into the Q buffer or the
-//                row's cache slot (DFlash KV Injection Walkthrough, Steps
-//                4.1-4.3; DFlash source guide (II), parts 1-4). Shapes that need
-//                split-K use the fp32 store and a separate epilogue kernel.
+//                The row's thread applies the per-head RMSNorm (Q and K heads),
+//                rotates the pair (i, i + 64) at the row's absolute position and
+//                stages the row in its stored form (bf16, or E4M3 codes); one copy
+//                per (row, head) puts it into the Q buffer or the row's cache slot
+//                (DFlash KV Injection Walkthrough, Steps 4.1-4.3; DFlash source
+//                guide (II), parts 1-4). Shapes that need split-K use the fp32
+//                store and a separate epilogue kernel.
 #include <cstdlib>
 #include <mutex>
 
@@ -79,6 +81,10 @@ struct Cfg {
   // epilogue staging tile over the stages: BM rows of BN fp32, padded, then row slots
   static constexpr int LD = BN + 4;
   static constexpr uint32_t STG_BYTES = BM * LD * 4;
+  // heads: the finished rows in their stored form, 256 bytes per head (bf16, or E4M3 codes
+  // with Q's remainder codes in the second half), rows 16 bytes apart from the bank pattern
+  static constexpr uint32_t RSB = 2 * BN + 16;
+  static_assert(BM * RSB <= STG_BYTES, "byte staging exceeds the fp32 staging area");
   static_assert(STG_BYTES + BM * 16 <= STAGES * STAGE, "staging tile exceeds the stages");
 };
 
@@ -96,6 +102,41 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsign
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Sixteen finished values (dims d0 .. d0 + 15 of one head) into the head's 256-byte slot
+// of the byte staging row: bf16 at 2 d0; E4M3 K / V codes of v * inv at d0; Q as codes at
+// d0 and remainder codes at 128 + d0.
+__device__ __forceinline__ void put16(uint8_t* slot, int d0, const float (&v)[16], bool fp8, bool q,
+                                      float inv) {
+  if (!fp8) {
+    uint4 w0, w1;
+    w0.x = pack_bf16(v[0], v[1]);
+    w0.y = pack_bf16(v[2], v[3]);
+    w0.z = pack_bf16(v[4], v[5]);
+    w0.w = pack_bf16(v[6], v[7]);
+    w1.x = pack_bf16(v[8], v[9]);
+    w1.y = pack_bf16(v[10], v[11]);
+    w1.z = pack_bf16(v[12], v[13]);
+    w1.w = pack_bf16(v[14], v[15]);
+    reinterpret_cast<uint4*>(slot + 2 * d0)[0] = w0;
+    reinterpret_cast<uint4*>(slot + 2 * d0)[1] = w1;
+  } else if (q) {
+    uint4 hi, lo;
+    e4m3x4_split(v[0], v[1], v[2], v[3], hi.x, lo.x);
+    e4m3x4_split(v[4], v[5], v[6], v[7], hi.y, lo.y);
+    e4m3x4_split(v[8], v[9], v[10], v[11], hi.z, lo.z);
+    e4m3x4_split(v[12], v[13], v[14], v[15], hi.w, lo.w);
+    *reinterpret_cast<uint4*>(slot + d0) = hi;
+    *reinterpret_cast<uint4*>(slot + 128 + d0) = lo;
+  } else {
+    uint4 c;
+    c.x = e4m3x4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+    c.y = e4m3x4(v[4] * inv, v[5] * inv, v[6] * inv, v[7] * inv);
+    c.z = e4m3x4(v[8] * inv, v[9] * inv, v[10] * inv, v[11] * inv);
+    c.w = e4m3x4(v[12] * inv, v[13] * inv, v[14] * inv, v[15] * inv);
+    *reinterpret_cast<uint4*>(slot + d0) = c;
+  }
 }
 
 // Sequence, index and position of projection row `row`, or pos = -1 when the row is
@@ -347,17 +388,20 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
         const int head = n0 / 128 + hd;
         const int kind = head < ep.n_q ? 0 : (head < ep.n_q + ep.n_kv ? 1 : 2);  // Q, K, V
         const uint32_t hcol = (uint32_t)(hd * 128);
+        uint8_t* hslot = smem + row * C::RSB + hd * 256;
         if (kind == 2) {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t r[32];
             ptx::tmem_ld_32x32b_x32(tmem + lane_base + hcol + (uint32_t)(c * 32), r);
             ptx::tmem_ld_wait();
-            float4* d = reinterpret_cast<float4*>(srow + hd * 128 + c * 32);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              d[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            for (int hh = 0; hh < 2; ++hh) {
+              float v[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[16 * hh + e]);
+              put16(hslot, 32 * c + 16 * hh, v, ep.kv_fp8, false, ep.v_inv);
+            }
           }
           continue;
         }
@@ -400,76 +444,49 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
               ya[e] = a * co - b * si;
               yb[e] = b * co + a * si;
             }
-            float4* da = reinterpret_cast<float4*>(srow + hd * 128 + 32 * c + 16 * hh);
-            float4* db = reinterpret_cast<float4*>(srow + hd * 128 + 64 + 32 * c + 16 * hh);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              da[j] = make_float4(ya[4 * j], ya[4 * j + 1], ya[4 * j + 2], ya[4 * j + 3]);
-              db[j] = make_float4(yb[4 * j], yb[4 * j + 1], yb[4 * j + 2], yb[4 * j + 3]);
-            }
+            put16(hslot, 32 * c + 16 * hh, ya, ep.kv_fp8, kind == 0, ep.k_inv);
+            put16(hslot, 64 + 32 * c + 16 * hh, yb, ep.kv_fp8, kind == 0, ep.k_inv);
           }
         }
       }
     }
   }
-  // phase 2, all warps: coalesced stores from the staging tile
+  if (warp >= 2) ptx::fence_proxy_async_smem();  // staged rows leave by bulk copy
+  // phase 2, all warps: bulk copies from the staging tile
   ptx::named_sync(1, kThreads);
   if (!abort_flag) {
     if (!HEADS) {
-      // fp32 partial rows: one warp per row, lanes along the row
+      // fp32 partial rows, one contiguous copy each
       float* ybase = p.Y + (size_t)blockIdx.z * M * p.ldY + n0;
-      for (int r = warp; r < BM && m0 + r < M; r += kThreads / 32) {
-        const float4* src = reinterpret_cast<const float4*>(stg + r * C::LD);
-        float4* dst = reinterpret_cast<float4*>(ybase + (size_t)(m0 + r) * p.ldY);
-#pragma unroll
-        for (int j = lane; j < BN / 4; j += 32) dst[j] = src[j];
-      }
+      for (int r = threadIdx.x; r < BM && m0 + r < M; r += kThreads)
+        ptx::bulk_store(ybase + (size_t)(m0 + r) * p.ldY, ptx::smem_u32(stg + r * C::LD), BN * 4);
     } else {
-      // one warp per (row, head) of the finished rows: lane l stores dims 4l .. 4l+3
-      constexpr int RB = 4;  // rows per batch
-      for (int r0 = warp * RB; r0 < BM; r0 += (kThreads / 32) * RB) {
-#pragma unroll
-        for (int i = 0; i < RB; ++i) {
-          const int r = r0 + i;
-          if (r >= BM) break;
-          const int4 rs = slots[r];
-          if (rs.z < 0 || m0 + r >= M) continue;  // warp-uniform
-#pragma unroll
-          for (int hd = 0; hd < NH; ++hd) {
-            const int head = n0 / 128 + hd;
-            const int kind = head < ep.n_q ? 0 : (head < ep.n_q + ep.n_kv ? 1 : 2);  // Q, K, V
-            const bool qh = kind == 0;
-            const float4 y = reinterpret_cast<const float4*>(stg + r * C::LD + hd * 128)[lane];
-            const int kvh = head - ep.n_q - (kind == 2 ? ep.n_kv : 0);
-            // element offset of the destination row (Q, or the cache slot)
-            const size_t eoff =
-                qh ? (((size_t)rs.x * ep.n_q + head) * ep.bs + rs.y) * 128
-                   : (rs.w >= 0 ? ((size_t)rs.w * ep.n_kv + kvh) * 128 + (rs.z & 127)
-                                : ((size_t)rs.x * ep.n_kv + kvh) * ep.capacity + rs.z) * 128;
-            char* kvbase = (char*)(kind == 1 ? ep.cache_k : ep.cache_v);
-            if (ep.kv_fp8) {
-              // E4M3 rows: Q as codes + remainder codes, K / V as codes of x / scale
-              if (qh) {
-                uint32_t hi, lo;
-                e4m3x4_split(y.x, y.y, y.z, y.w, hi, lo);
-                reinterpret_cast<uint32_t*>((char*)ep.q_out + eoff)[lane] = hi;
-                reinterpret_cast<uint32_t*>((char*)ep.q_lo + eoff)[lane] = lo;
-              } else {
-                const float inv = kind == 1 ? ep.k_inv : ep.v_inv;
-                reinterpret_cast<uint32_t*>(kvbase + eoff)[lane] =
-                    e4m3x4(y.x * inv, y.y * inv, y.z * inv, y.w * inv);
-              }
-            } else {
-              bf16* dst = qh ? (bf16*)ep.q_out + eoff : (bf16*)kvbase + eoff;
-              uint2 w2;
-              w2.x = pack_bf16(y.x, y.y);
-              w2.y = pack_bf16(y.z, y.w);
-              reinterpret_cast<uint2*>(dst)[lane] = w2;
-            }
-          }
+      // one copy per (row, head): the row's Q row, or its cache slot (bf16: 256 bytes;
+      // E4M3: 128 bytes of codes, and for Q 128 bytes of remainder codes)
+      for (int u = threadIdx.x; u < BM * NH; u += kThreads) {
+        const int r = u / NH, hd = u - r * NH;
+        const int4 rs = slots[r];
+        if (rs.z < 0 || m0 + r >= M) continue;
+        const int head = n0 / 128 + hd;
+        const int kind = head < ep.n_q ? 0 : (head < ep.n_q + ep.n_kv ? 1 : 2);  // Q, K, V
+        const bool qh = kind == 0;
+        const int kvh = head - ep.n_q - (kind == 2 ? ep.n_kv : 0);
+        // element offset of the destination row (Q, or the cache slot)
+        const size_t eoff =
+            qh ? (((size_t)rs.x * ep.n_q + head) * ep.bs + rs.y) * 128
+               : (rs.w >= 0 ? ((size_t)rs.w * ep.n_kv + kvh) * 128 + (rs.z & 127)
+                            : ((size_t)rs.x * ep.n_kv + kvh) * ep.capacity + rs.z) * 128;
+        char* dbase = (char*)(qh ? ep.q_out : (kind == 1 ? ep.cache_k : ep.cache_v));
+        const uint32_t src = ptx::smem_u32(smem + r * C::RSB + hd * 256);
+        if (!ep.kv_fp8) {
+          ptx::bulk_store(dbase + eoff * 2, src, 256);
+        } else {
+          ptx::bulk_store(dbase + eoff, src, 128);
+          if (qh) ptx::bulk_store((char*)ep.q_lo + eoff, src + 128, 128);
         }
       }
     }
+    ptx::bulk_commit_wait_all();
   }
   ptx::tc_fence_before();
   __syncthreads();
