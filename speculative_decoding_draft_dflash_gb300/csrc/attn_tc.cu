@@ -93,6 +93,7 @@ struct Plan {
   static constexpr int K_STAGES = FP8 ? 4 : (NARROW ? 3 : 2);
   static constexpr int V_STAGES = FP8 ? 3 : 2;
   static constexpr int C_STAGES = CONV ? 2 : 0;              // converted (f16) V tiles
+  static constexpr int C_RING = CONV ? C_STAGES : 1;         // its ring size in index math
   static constexpr uint32_t QPART = NARROW ? 8192 : 16384;   // fp8: code rows of one buffer
   static constexpr uint32_t Q_BYTES = FP8 ? (NARROW ? 4 * QPART + 8192 : 4 * QPART)
                                           : (NARROW ? 40960 : 2 * TILE);
@@ -139,6 +140,7 @@ struct AttnTcParams {
   int batch, n_h, n_kv, bs, G, R, capacity, window, table_len, max_splits;
   float sl2;      // scaling * log2(e) (fp8: times k_scale)
   float v_scale;  // fp8: scale of the V codes
+  int out_v8;     // out is 32-byte aligned: rows leave in 32-byte stores
 };
 
 __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity, unsigned* status) {
@@ -526,11 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const int T = (it.z - it.y + TK - 1) / TK;
       bool alive = true;
       for (int j = 0; j < T; ++j) {
-        const int g = gv + j, vs = g % PL::V_STAGES, cs = g % PL::C_STAGES;
+        const int g = gv + j, vs = g % PL::V_STAGES, cs = g % PL::C_RING;
         alive = __all_sync(0xffffffffu, ptx::mbar_wait(v_full0 + 8 * vs, (g / PL::V_STAGES) & 1,
                                                        &abort_flag, p.status));
-        if (alive && g >= PL::C_STAGES)
-          alive = __all_sync(0xffffffffu, ptx::mbar_wait(c_empty0 + 8 * cs, ((g / PL::C_STAGES) - 1) & 1,
+        if (alive && g >= PL::C_RING)
+          alive = __all_sync(0xffffffffu, ptx::mbar_wait(c_empty0 + 8 * cs, ((g / PL::C_RING) - 1) & 1,
                                                          &abort_flag, p.status));
         if (!alive) break;
         const uint8_t* src = smem + PL::OFF_V + vs * PL::TILE_B + k * 128;
@@ -725,33 +727,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       }
       ptx::tc_fence_before();
       if (!rvalid) continue;
-      if (it.w < 0) {
-        bf16* orow = p.out + ((size_t)(b * p.bs + t) * p.n_h + kvh * p.G + gq) * 128 + coff;
-        const float inv = l > 0.f ? (FP8 ? p.v_scale : 1.f) / l : 0.f;
+      // this thread's 64 columns of the row, O / l in bf16: 32-byte stores (a full sector
+      // each) when the destination allows, else 16-byte ones
+      const float inv = l > 0.f ? (FP8 ? p.v_scale : 1.f) / l : 0.f;
+      auto store_row = [&](bf16* dst, bool v8) {
+        if (v8) {
 #pragma unroll
-        for (int k = 0; k < NCOL / 8; ++k) {
-          uint4 w;
-          w.x = pack_bf16(s[8 * k + 0] * inv, s[8 * k + 1] * inv);
-          w.y = pack_bf16(s[8 * k + 2] * inv, s[8 * k + 3] * inv);
-          w.z = pack_bf16(s[8 * k + 4] * inv, s[8 * k + 5] * inv);
-          w.w = pack_bf16(s[8 * k + 6] * inv, s[8 * k + 7] * inv);
-          reinterpret_cast<uint4*>(orow)[k] = w;
+          for (int k = 0; k < NCOL / 16; ++k) {
+            uint32_t w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) w[j] = pack_bf16(s[16 * k + 2 * j] * inv, s[16 * k + 2 * j + 1] * inv);
+            ptx::st_global_v8(dst + 16 * k, w);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < NCOL / 8; ++k) {
+            uint4 w;
+            w.x = pack_bf16(s[8 * k + 0] * inv, s[8 * k + 1] * inv);
+            w.y = pack_bf16(s[8 * k + 2] * inv, s[8 * k + 3] * inv);
+            w.z = pack_bf16(s[8 * k + 4] * inv, s[8 * k + 5] * inv);
+            w.w = pack_bf16(s[8 * k + 6] * inv, s[8 * k + 7] * inv);
+            reinterpret_cast<uint4*>(dst)[k] = w;
+          }
         }
+      };
+      if (it.w < 0) {
+        store_row(p.out + ((size_t)(b * p.bs + t) * p.n_h + kvh * p.G + gq) * 128 + coff, p.out_v8 != 0);
       } else {
         // a split range's partial: its normalised output O / l (bf16, like the final rows)
-        // and its (maximum, sum); the combine weights each by 2^(max - M) * sum
+        // and its (maximum, sum); the combine weights each by 2^(max - M) * sum (the
+        // workspace is 256-byte aligned)
         const size_t prow = ((size_t)it.x * p.max_splits + it.w) * p.R + rt;
-        bf16* a = reinterpret_cast<bf16*>(p.part_acc) + prow * 128 + coff;
-        const float inv = l > 0.f ? (FP8 ? p.v_scale : 1.f) / l : 0.f;
-#pragma unroll
-        for (int k = 0; k < NCOL / 8; ++k) {
-          uint4 w;
-          w.x = pack_bf16(s[8 * k + 0] * inv, s[8 * k + 1] * inv);
-          w.y = pack_bf16(s[8 * k + 2] * inv, s[8 * k + 3] * inv);
-          w.z = pack_bf16(s[8 * k + 4] * inv, s[8 * k + 5] * inv);
-          w.w = pack_bf16(s[8 * k + 6] * inv, s[8 * k + 7] * inv);
-          reinterpret_cast<uint4*>(a)[k] = w;
-        }
+        store_row(reinterpret_cast<bf16*>(p.part_acc) + prow * 128 + coff, true);
         if (half == 0) p.part_ml[prow] = make_float2(m_ref, l);
       }
     }
@@ -931,6 +938,7 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   p.lens = a.lens_out;
   p.lens_new = sp.lens_new;
   p.out = (bf16*)a.out;
+  p.out_v8 = ((uintptr_t)a.out & 31) == 0;
   p.part_acc = a.part_acc;
   p.part_ml = a.part_ml;
   p.items = sp.items;
