@@ -112,3 +112,24 @@ def test_full_size_fp8(name, n, paged):
     w = W[name].replace(kv="fp8")
     _run(w, _sample(w, n, seed=13), paged=paged)
 
+
+
+@pytest.mark.parametrize("name", ["small_gqa_bf16", "small_g8_bf16"])
+def test_output_16_byte_aligned(name):
+    """Output buffers that are 16-byte but not 32-byte aligned (all the API asks for) take
+    the attention's 16-byte store path for whole-range rows: same results."""
+    import torch
+    from speculative_decoding_draft_dflash_gb300.runner import DeviceWorkload
+    w = SMALL[name]
+    dev = DeviceWorkload(w)
+    n = w.batch * w.bs * w.n_h * w.d_h
+    views = []
+    for _ in range(w.n_layers):
+        buf = torch.empty(n + 16, dtype=torch.bfloat16, device="cuda")
+        v = buf[8:8 + n].view(w.batch, w.bs, w.n_h * w.d_h)
+        assert v.data_ptr() % 32 == 16
+        views.append(v)
+    dev.out = views
+    seqs = list(range(w.batch))
+    dev_res, _ = harness.device_rounds(w, seqs, dev=dev)
+    harness.compare(w, dev_res, harness.oracle_rounds(w, seqs), seqs)
