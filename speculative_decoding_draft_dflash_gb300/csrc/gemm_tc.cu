@@ -346,14 +346,16 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
       const bool ropes = n0 / 128 < ep.n_q + ep.n_kv;  // the tile's first head is a Q or K head
       __syncwarp();  // row_slot's search diverges; tcgen05.st is .sync.aligned
       if (ropes) {
-        // the table is 8-byte aligned: float2 loads
-        const float2* cs = ep.rope + (size_t)max(rs.pos, 0) * 64;
+        // the table is 8-byte aligned: float2 loads; rows that are not written (no
+        // position, e.g. a table too short or empty) stage zeros and read nothing
+        const bool has = rs.pos >= 0;
+        const float2* cs = ep.rope + (size_t)(has ? rs.pos : 0) * 64;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float2 f = cs[c * 16 + j];
+            const float2 f = has ? cs[c * 16 + j] : make_float2(0.f, 0.f);
             v[2 * j] = __float_as_uint(f.x);
             v[2 * j + 1] = __float_as_uint(f.y);
           }
