@@ -329,8 +329,9 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
     }
   } else {
     // phase 1: TMEM -> a staging tile in the pipeline's shared memory (free once every
-    // MMA is done), one row per thread; rows padded by 4 floats so the float4 stores of a
-    // warp spread over all banks.
+    // MMA is done), one row per thread. fp32 store: the accumulator row, rows padded by 4
+    // floats so the float4 stores of a warp spread over all banks. heads: the finished
+    // row in its stored form, in the byte tile (rows 2 BN + 16 bytes apart).
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 are this warp's
     const int row = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -383,7 +384,8 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
     } else if (ok) {
       // the finished row: per-head RMSNorm (Q, K heads: sum of squares over the head's
       // 128 dims, then x / rms * gamma) and rotate_half RoPE on the pairs (i, i + 64);
-      // V heads as they are
+      // V heads as they are; each head's 256-byte slot of the byte tile gets the values in
+      // the form the destination stores (put16)
       slots[row] = make_int4(rs.b, rs.t, rs.pos, rs.page);
 #pragma unroll 1
       for (int hd = 0; hd < NH; ++hd) {
