@@ -111,6 +111,12 @@ def _ptr(t):
     return c_void_p(t.data_ptr())
 
 
+def _ptr_array(ts):
+    """C array of device pointers: tensors (checked like _ptr) or raw addresses (ints)."""
+    vals = [(_ptr(t).value or 0) if hasattr(t, "data_ptr") else int(t) for t in ts]
+    return (c_void_p * max(1, len(vals)))(*vals)
+
+
 def _check(st, where):
     if st != OK:
         raise DFlashError(st, where)
@@ -243,8 +249,7 @@ def dflash_workspace_bytes(dims, batch, capacity, max_rows):
 
 
 def dflash_ctx_project(dims, hidden, M, W_fc, gamma_h, C_out, workspace, stream=None):
-    ptrs = (c_void_p * max(1, len(hidden)))(*[t.data_ptr() if hasattr(t, "data_ptr") else int(t)
-                                             for t in hidden])
+    ptrs = _ptr_array(hidden)
     _check(_lib.dflash_ctx_project(ctypes.byref(dims), ptrs, int(M), _ptr(W_fc), _ptr(gamma_h),
                                    _ptr(C_out), _ptr(workspace), workspace.numel() *
                                    workspace.element_size(), _stream(stream)),
@@ -253,8 +258,7 @@ def dflash_ctx_project(dims, hidden, M, W_fc, gamma_h, C_out, workspace, stream=
 
 def dflash_ctx_project_noalloc(dims, hidden, M, W_fc, gamma_h, C_out, stream=None):
     """dflash_ctx_project with the library's fixed scratch array instead of a workspace."""
-    ptrs = (c_void_p * max(1, len(hidden)))(*[t.data_ptr() if hasattr(t, "data_ptr") else int(t)
-                                             for t in hidden])
+    ptrs = _ptr_array(hidden)
     _check(_lib.dflash_ctx_project_noalloc(ctypes.byref(dims), ptrs, int(M), _ptr(W_fc),
                                            _ptr(gamma_h), _ptr(C_out), _stream(stream)),
            "dflash_ctx_project_noalloc")

@@ -237,3 +237,29 @@ def test_fp8_cache_arguments_rejected(D, lib):
     for bad in ((0.5, 0.0, 1.0, 2.0), (0.5, -1.0, 1.0, 2.0), (0.5, 0.25, float("nan"), 2.0),
                 (0.5, 0.25, 1.0, float("inf"))):
         assert call(cache(fp8, bad)) == 1, bad
+
+
+def test_binding_checks_hidden_state_tensors(D):
+    """The k hidden-state pointers go through the same checks as every other tensor argument:
+    a host tensor or a strided view is refused before the library is called."""
+    import torch
+    dims = _dims(D)
+    ws = torch.zeros(256, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA"):
+        D.dflash_ctx_project(dims, [torch.zeros((4, 64))], 4, None, None, None, ws)
+    strided = torch.zeros((64, 8)).t()
+
+    class FakeCuda:                      # a strided "device" tensor, no GPU needed
+        is_cuda = True
+
+        def is_contiguous(self):
+            return strided.is_contiguous()
+
+        def data_ptr(self):
+            return 4096
+
+    with pytest.raises(ValueError, match="contiguous"):
+        D.dflash_ctx_project_noalloc(dims, [FakeCuda()], 8, None, None, None)
+    # raw addresses pass through unchanged
+    arr = D._ptr_array([4096, 8192])
+    assert [arr[0], arr[1]] == [4096, 8192]
