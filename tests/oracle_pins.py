@@ -287,6 +287,67 @@ def pin_fc_selects_layer(O):
 
 
 # ---------------------------------------------------------------------------
+# Head layout of the projections (walkthrough Steps 4.1-4.2)
+# ---------------------------------------------------------------------------
+
+def _head_select(n_heads, d_h, d, offsets):
+    """A weight [n_heads*d_h, d] whose output features h*d_h .. (h+1)*d_h-1 copy input
+    features offsets[h] .. offsets[h]+d_h-1, i.e. head h of the view [n, n_heads, d_h]
+    reads that slice of the input row."""
+    W = np.zeros((n_heads * d_h, d))
+    for h, s in enumerate(offsets):
+        W[h * d_h:(h + 1) * d_h, s:s + d_h] = np.eye(d_h)
+    return W
+
+
+def pin_head_layout_by_selection(O):
+    """Head h of a projection is output features [h*d_h, (h+1)*d_h).
+
+    The walkthrough splits a projected row by view(bsz, q_len, -1, head_dim) (Step 4.1:
+    [4, 512] -> [4, 8, 64]; Step 4.2: [7, 512] -> [7, 8, 64]): the head index is the
+    slower of the two split axes. With a weight whose head-h block of rows copies one
+    slice of the input, head h must hold exactly that slice (V, not normalised), its
+    torch RMSNorm (Q and K at position 0, where RoPE is the identity) or that norm
+    rotated at the row's position (the 2-D rotation per (i, i + d_h/2) pair); every
+    other head reads zeros. Heads use distinct, overlapping slices, so a strided or
+    transposed split, or a wrong head order, moves values between heads.
+    """
+    n_h, n_kv, d_h, d, n = 8, 2, 64, 512, 4
+    H = _rand((n, d), 70)
+    offs_q = [(37 * h + 5) % (d - d_h) for h in range(n_h)]
+    offs_kv = [11, 300]
+    WQ = _head_select(n_h, d_h, d, offs_q)
+    WK = _head_select(n_kv, d_h, d, offs_kv)
+    WV = _head_select(n_kv, d_h, d, offs_kv[::-1])
+    ones = np.ones(d_h)
+    tn = lambda x: F.rms_norm(torch.from_numpy(np.ascontiguousarray(x)), (d_h,), None,
+                              1e-6).numpy()
+    # position 0: RoPE is the identity, so Q = RMSNorm of the selected slice
+    q = O.q_project(H, WQ, ones, n_h, d_h, 1e-6, np.zeros(n, dtype=np.int64), 1e6)
+    assert q.shape == (n_h, n, d_h)
+    for h in range(n_h):
+        _close(q[h], tn(H[:, offs_q[h]:offs_q[h] + d_h]), 1e-12, f"Q head {h}")
+    K, V = O.kv_project(H, WK, WV, ones, n_kv, d_h, 1e-6, np.zeros(n, dtype=np.int64), 1e6)
+    for h in range(n_kv):
+        _close(K[h], tn(H[:, offs_kv[h]:offs_kv[h] + d_h]), 1e-12, f"K head {h}")
+        _close(V[h], H[:, offs_kv[::-1][h]:offs_kv[::-1][h] + d_h], 0, f"V head {h}")
+    # at positions p: the normed slice rotated by p * theta^(-2i/d_h) in plane (i, i + d_h/2)
+    pos = np.array([3, 4, 5, 6])
+    q = O.q_project(H, WQ, ones, n_h, d_h, 1e-6, pos, 1e4)
+    inv = 1e4 ** (-2.0 * np.arange(d_h // 2) / d_h)
+    for h in (0, 5):
+        x = tn(H[:, offs_q[h]:offs_q[h] + d_h])
+        a, b = x[:, :d_h // 2], x[:, d_h // 2:]
+        c, s = np.cos(pos[:, None] * inv), np.sin(pos[:, None] * inv)
+        _close(q[h], np.concatenate([a * c - b * s, a * s + b * c], axis=1), 1e-12,
+               f"Q head {h} roped")
+    # the walkthrough's own split: [4, 512] viewed as [4, 8, 64], heads first
+    x = _rand((n, d), 71)
+    ref = torch.from_numpy(x).view(n, n_h, d_h).transpose(0, 1).numpy()
+    _close(O.split_heads(x, n_h, d_h), ref, 0, "split_heads = view(n, n_h, d_h).transpose")
+
+
+# ---------------------------------------------------------------------------
 # Dual-stream K/V and the cache (walkthrough Steps 4.2-4.3, 7)
 # ---------------------------------------------------------------------------
 

@@ -152,6 +152,16 @@ def _e4m3_bias_8(code):
     return v / 2.0
 
 
+def _split_heads_strided(x, n_heads, d_h):
+    n = x.shape[0]
+    return np.asarray(x, F64).reshape(n, d_h, n_heads).transpose(2, 0, 1)
+
+
+def _split_heads_reversed(x, n_heads, d_h):
+    n = x.shape[0]
+    return np.asarray(x, F64).reshape(n, n_heads, d_h).transpose(1, 0, 2)[::-1]
+
+
 def _fp8_store_drops_scale(x, scale):
     return O.e4m3_dequantize(O.e4m3_quantize(np.asarray(x, np.float64) / scale))
 
@@ -187,6 +197,8 @@ MUTATIONS = {
     "e4m3_overflow_to_nan": ("e4m3_quantize", _e4m3_no_saturation),
     "e4m3_exponent_bias_8": ("e4m3_value", _e4m3_bias_8),
     "fp8_store_drops_scale": ("fp8_store", _fp8_store_drops_scale),
+    "split_heads_strided": ("split_heads", _split_heads_strided),
+    "split_heads_reversed_order": ("split_heads", _split_heads_reversed),
 }
 
 
