@@ -99,22 +99,66 @@ def _stream(stream):
     return c_void_p(int(stream))
 
 
-def _ptr(t):
+def _ptr(t, what="tensor", dtype=None, numel=None):
+    """Device address of a tensor argument after the checks the C ABI cannot make.
+
+    The library sees bare pointers and sizes, so it cannot tell a bf16 buffer from an
+    f32 one or a short buffer from a full one; a mismatch would make a kernel read or
+    write past the tensor. So a torch tensor must be a contiguous CUDA tensor, of
+    element type ``dtype`` when one is given, holding at least ``numel`` elements when
+    that is given. ``None`` stays NULL (the library refuses it where a pointer is
+    required) and an ``int`` is taken as a raw device address, unchecked: a caller who
+    passes addresses vouches for their sizes."""
     if t is None:
         return None
     if isinstance(t, int):
         return c_void_p(t)
     if not t.is_cuda:
-        raise ValueError("expected a CUDA tensor")
+        raise ValueError(f"{what}: expected a CUDA tensor")
     if not t.is_contiguous():
-        raise ValueError("expected a contiguous tensor")
+        raise ValueError(f"{what}: expected a contiguous tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{what}: element type {t.dtype}, the call needs {dtype}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{what}: {t.numel()} elements, the call needs at least {numel}")
     return c_void_p(t.data_ptr())
 
 
-def _ptr_array(ts):
+def _ptr_array(ts, what="hidden", dtype=None, numel=None):
     """C array of device pointers: tensors (checked like _ptr) or raw addresses (ints)."""
-    vals = [(_ptr(t).value or 0) if hasattr(t, "data_ptr") else int(t) for t in ts]
+    vals = [(_ptr(t, f"{what}[{i}]", dtype, numel).value or 0) if hasattr(t, "data_ptr")
+            else int(t) for i, t in enumerate(ts)]
     return (c_void_p * max(1, len(vals)))(*vals)
+
+
+def _ws(workspace):
+    """(pointer, size in bytes) of a workspace tensor (any element type)."""
+    if workspace is None:
+        return None, 0
+    return _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size()
+
+
+def _et(dims):
+    """torch element type of the activations, weights and gammas of a call."""
+    return torch_dtype(dims.dtype)
+
+
+def _desc(dims, cache):
+    """C descriptor of a cache; a KVCache must match the call's dims and element type."""
+    if not isinstance(cache, KVCache):
+        return cache
+    if cache.n_kv != dims.n_kv or cache.d_h != dims.d_h:
+        raise ValueError(f"cache: n_kv {cache.n_kv}, d_h {cache.d_h}; the dims give "
+                         f"n_kv {dims.n_kv}, d_h {dims.d_h}")
+    want = torch.uint8 if cache.fp8 else _et(dims)
+    if cache.k.dtype != want or cache.v.dtype != want:
+        raise ValueError(f"cache: element type {cache.k.dtype}, the dims need {want}")
+    return cache.desc
+
+
+def _rope(dims, rope_table, table_len):
+    """The RoPE table: float32 [table_len][d_h / 2][2]."""
+    return _ptr(rope_table, "rope_table", torch.float32, max(0, int(table_len)) * dims.d_h)
 
 
 def _check(st, where):
@@ -211,16 +255,12 @@ class KVCache:
         x = x.contiguous().view(torch.float8_e4m3fn).to(torch.float32)
         return x if codes else x * float(self.scales[layer, 0 if which == "k" else 1])
 
-    def _store(self, which, layer, X):
-        if not self.fp8:
-            return X
-        s = float(self.scales[layer, 0 if which == "k" else 1])
-        return (X.float() / s).to(torch.float8_e4m3fn).view(torch.uint8)
-
     def set_rows(self, layer, b, K, V):
-        """Writes K, V [n_kv][n][d_h] to logical slots 0 .. n-1 of sequence b."""
+        """Writes K, V [n_kv][n][d_h] to logical slots 0 .. n-1 of sequence b. The rows are
+        given in stored form: the cache's element type, E4M3 codes (uint8) for fp8."""
         n = K.shape[1]
-        K, V = self._store("k", layer, K), self._store("v", layer, V)
+        if K.dtype != self.k.dtype or V.dtype != self.v.dtype:
+            raise ValueError(f"set_rows: rows of type {K.dtype}, the cache holds {self.k.dtype}")
         if not self.paged:
             self.k[layer, b, :, :n] = K
             self.v[layer, b, :, :n] = V
@@ -239,7 +279,9 @@ def status_string(st):
 
 
 def dflash_rope_table_build(theta, d_h, max_pos, table, stream=None):
-    _check(_lib.dflash_rope_table_build(float(theta), int(d_h), int(max_pos), _ptr(table),
+    _check(_lib.dflash_rope_table_build(float(theta), int(d_h), int(max_pos),
+                                        _ptr(table, "table", torch.float32,
+                                             max(0, int(max_pos)) * int(d_h)),
                                         _stream(stream)), "dflash_rope_table_build")
 
 
@@ -248,68 +290,101 @@ def dflash_workspace_bytes(dims, batch, capacity, max_rows):
                                            int(max_rows)))
 
 
+def _ctx_args(dims, hidden, M, W_fc, gamma_h, C_out):
+    et, d, M = _et(dims), dims.d, max(0, int(M))
+    ptrs = _ptr_array(hidden, "hidden", et, M * d)
+    if len(hidden) < dims.k_layers:
+        raise ValueError(f"hidden: {len(hidden)} pointers, the dims give k_layers {dims.k_layers}")
+    return (ptrs, _ptr(W_fc, "W_fc", et, d * dims.k_layers * d),
+            _ptr(gamma_h, "gamma_h", et, d), _ptr(C_out, "C_out", et, M * d))
+
+
 def dflash_ctx_project(dims, hidden, M, W_fc, gamma_h, C_out, workspace, stream=None):
-    ptrs = _ptr_array(hidden)
-    _check(_lib.dflash_ctx_project(ctypes.byref(dims), ptrs, int(M), _ptr(W_fc), _ptr(gamma_h),
-                                   _ptr(C_out), _ptr(workspace), workspace.numel() *
-                                   workspace.element_size(), _stream(stream)),
-           "dflash_ctx_project")
+    ptrs, W, g, C = _ctx_args(dims, hidden, M, W_fc, gamma_h, C_out)
+    _check(_lib.dflash_ctx_project(ctypes.byref(dims), ptrs, int(M), W, g, C, *_ws(workspace),
+                                   _stream(stream)), "dflash_ctx_project")
 
 
 def dflash_ctx_project_noalloc(dims, hidden, M, W_fc, gamma_h, C_out, stream=None):
     """dflash_ctx_project with the library's fixed scratch array instead of a workspace."""
-    ptrs = _ptr_array(hidden)
-    _check(_lib.dflash_ctx_project_noalloc(ctypes.byref(dims), ptrs, int(M), _ptr(W_fc),
-                                           _ptr(gamma_h), _ptr(C_out), _stream(stream)),
-           "dflash_ctx_project_noalloc")
+    ptrs, W, g, C = _ctx_args(dims, hidden, M, W_fc, gamma_h, C_out)
+    _check(_lib.dflash_ctx_project_noalloc(ctypes.byref(dims), ptrs, int(M), W, g, C,
+                                           _stream(stream)), "dflash_ctx_project_noalloc")
+
+
+def _batch(cache):
+    return int(cache.batch)
+
+
+def _kv_args(dims, cache, C, cu_rows, M, W_K, W_V, gamma_k):
+    et, M = _et(dims), max(0, int(M))
+    nkv = dims.n_kv * dims.d_h
+    return (_ptr(C, "C", et, M * dims.d), _ptr(cu_rows, "cu_rows", torch.int32, _batch(cache) + 1),
+            _ptr(W_K, "W_K", et, nkv * dims.d), _ptr(W_V, "W_V", et, nkv * dims.d),
+            _ptr(gamma_k, "gamma_k", et, dims.d_h))
+
+
+def _block_args(dims, cache, H, W_Q, gamma_q, out):
+    et, rows = _et(dims), _batch(cache) * dims.block_size
+    return (_ptr(H, "H", et, rows * dims.d), _ptr(W_Q, "W_Q", et, dims.n_h * dims.d_h * dims.d),
+            _ptr(gamma_q, "gamma_q", et, dims.d_h), _ptr(out, "out", et, rows * dims.n_h * dims.d_h))
 
 
 def dflash_kv_inject(dims, cache, layer, C, cu_rows, M, W_K, W_V, gamma_k, rope_table, table_len,
                      workspace, stream=None):
-    desc = cache.desc if isinstance(cache, KVCache) else cache
-    _check(_lib.dflash_kv_inject(ctypes.byref(dims), ctypes.byref(desc), int(layer), _ptr(C),
-                                 _ptr(cu_rows), int(M), _ptr(W_K), _ptr(W_V), _ptr(gamma_k),
-                                 _ptr(rope_table), int(table_len), _ptr(workspace),
-                                 workspace.numel() * workspace.element_size(), _stream(stream)),
-           "dflash_kv_inject")
+    desc = _desc(dims, cache)
+    c, cu, wk, wv, gk = _kv_args(dims, desc, C, cu_rows, M, W_K, W_V, gamma_k)
+    _check(_lib.dflash_kv_inject(ctypes.byref(dims), ctypes.byref(desc), int(layer), c, cu, int(M),
+                                 wk, wv, gk, _rope(dims, rope_table, table_len), int(table_len),
+                                 *_ws(workspace), _stream(stream)), "dflash_kv_inject")
 
 
 def dflash_block_attn(dims, cache, layer, H, W_Q, W_K, W_V, gamma_q, gamma_k, rope_table,
                       table_len, sliding_window, scaling, out, workspace, stream=None):
-    desc = cache.desc if isinstance(cache, KVCache) else cache
-    _check(_lib.dflash_block_attn(ctypes.byref(dims), ctypes.byref(desc), int(layer), _ptr(H),
-                                  _ptr(W_Q), _ptr(W_K), _ptr(W_V), _ptr(gamma_q), _ptr(gamma_k),
-                                  _ptr(rope_table), int(table_len), int(sliding_window),
-                                  float(scaling), _ptr(out), _ptr(workspace),
-                                  workspace.numel() * workspace.element_size(), _stream(stream)),
-           "dflash_block_attn")
+    desc = _desc(dims, cache)
+    h, wq, gq, o = _block_args(dims, desc, H, W_Q, gamma_q, out)
+    et, nkv = _et(dims), dims.n_kv * dims.d_h
+    _check(_lib.dflash_block_attn(ctypes.byref(dims), ctypes.byref(desc), int(layer), h, wq,
+                                  _ptr(W_K, "W_K", et, nkv * dims.d),
+                                  _ptr(W_V, "W_V", et, nkv * dims.d), gq,
+                                  _ptr(gamma_k, "gamma_k", et, dims.d_h),
+                                  _rope(dims, rope_table, table_len), int(table_len),
+                                  int(sliding_window), float(scaling), o, *_ws(workspace),
+                                  _stream(stream)), "dflash_block_attn")
 
 
 def dflash_draft_layer(dims, cache, layer, C, cu_rows, M, H, W_Q, W_K, W_V, gamma_q, gamma_k,
                        rope_table, table_len, sliding_window, scaling, out, workspace, stream=None):
     """dflash_kv_inject of C's rows followed by dflash_block_attn of H, as one call."""
-    desc = cache.desc if isinstance(cache, KVCache) else cache
-    _check(_lib.dflash_draft_layer(ctypes.byref(dims), ctypes.byref(desc), int(layer), _ptr(C),
-                                   _ptr(cu_rows), int(M), _ptr(H), _ptr(W_Q), _ptr(W_K), _ptr(W_V),
-                                   _ptr(gamma_q), _ptr(gamma_k), _ptr(rope_table), int(table_len),
-                                   int(sliding_window), float(scaling), _ptr(out), _ptr(workspace),
-                                   workspace.numel() * workspace.element_size(), _stream(stream)),
-           "dflash_draft_layer")
+    desc = _desc(dims, cache)
+    c, cu, wk, wv, gk = _kv_args(dims, desc, C, cu_rows, M, W_K, W_V, gamma_k)
+    h, wq, gq, o = _block_args(dims, desc, H, W_Q, gamma_q, out)
+    _check(_lib.dflash_draft_layer(ctypes.byref(dims), ctypes.byref(desc), int(layer), c, cu,
+                                   int(M), h, wq, wk, wv, gq, gk, _rope(dims, rope_table, table_len),
+                                   int(table_len), int(sliding_window), float(scaling), o,
+                                   *_ws(workspace), _stream(stream)), "dflash_draft_layer")
 
 
 def dflash_cache_crop(cache, new_lens, stream=None):
     desc = cache.desc if isinstance(cache, KVCache) else cache
-    _check(_lib.dflash_cache_crop(ctypes.byref(desc), _ptr(new_lens), _stream(stream)),
-           "dflash_cache_crop")
+    _check(_lib.dflash_cache_crop(ctypes.byref(desc),
+                                  _ptr(new_lens, "new_lens", torch.int32, int(desc.batch)),
+                                  _stream(stream)), "dflash_cache_crop")
 
 
 def dflash_accept(block_ids, posterior, ctx_len, accept_len, next_cu_rows, ctx_next, next_anchor,
                   stream=None):
     """Acceptance bookkeeping of a verified round; block_ids / posterior are int32 [batch][bs]."""
     batch, bs = (int(block_ids.shape[0]), int(block_ids.shape[1])) if block_ids.dim() == 2 else (0, 1)
-    _check(_lib.dflash_accept(_ptr(block_ids), _ptr(posterior), batch, bs, _ptr(ctx_len),
-                              _ptr(accept_len), _ptr(next_cu_rows), _ptr(ctx_next),
-                              _ptr(next_anchor), _stream(stream)), "dflash_accept")
+    i32 = torch.int32
+    _check(_lib.dflash_accept(_ptr(block_ids, "block_ids", i32, batch * bs),
+                              _ptr(posterior, "posterior", i32, batch * bs), batch, bs,
+                              _ptr(ctx_len, "ctx_len", i32, batch),
+                              _ptr(accept_len, "accept_len", i32, batch),
+                              _ptr(next_cu_rows, "next_cu_rows", i32, batch + 1),
+                              _ptr(ctx_next, "ctx_next", i32, batch),
+                              _ptr(next_anchor, "next_anchor", i32, batch), _stream(stream)),
+           "dflash_accept")
 
 
 def dflash_layer_out_workspace_bytes(dims, M, d_ff):
@@ -319,15 +394,20 @@ def dflash_layer_out_workspace_bytes(dims, M, d_ff):
 def dflash_layer_out(dims, M, attn_out, x, W_O, gamma_post, d_ff, W_gate, W_up, W_down, x_out,
                      workspace, stream=None):
     """x_out = x1 + MLP(RMSNorm_post(x1)), x1 = x + attn_out W_O^T (rows of the blocks)."""
-    _check(_lib.dflash_layer_out(ctypes.byref(dims), int(M), _ptr(attn_out), _ptr(x), _ptr(W_O),
-                                 _ptr(gamma_post), int(d_ff), _ptr(W_gate), _ptr(W_up),
-                                 _ptr(W_down), _ptr(x_out), _ptr(workspace),
-                                 workspace.numel() * workspace.element_size(), _stream(stream)),
-           "dflash_layer_out")
+    et, d, M, F_ = _et(dims), dims.d, max(0, int(M)), max(0, int(d_ff))
+    hd = dims.n_h * dims.d_h
+    _check(_lib.dflash_layer_out(ctypes.byref(dims), int(M), _ptr(attn_out, "attn_out", et, M * hd),
+                                 _ptr(x, "x", et, M * d), _ptr(W_O, "W_O", et, d * hd),
+                                 _ptr(gamma_post, "gamma_post", et, d), int(d_ff),
+                                 _ptr(W_gate, "W_gate", et, F_ * d), _ptr(W_up, "W_up", et, F_ * d),
+                                 _ptr(W_down, "W_down", et, d * F_), _ptr(x_out, "x_out", et, M * d),
+                                 *_ws(workspace), _stream(stream)), "dflash_layer_out")
 
 
 def dflash_rms_norm(dims, M, x, gamma, out, stream=None):
-    _check(_lib.dflash_rms_norm(ctypes.byref(dims), int(M), _ptr(x), _ptr(gamma), _ptr(out),
+    et, n = _et(dims), max(0, int(M)) * dims.d
+    _check(_lib.dflash_rms_norm(ctypes.byref(dims), int(M), _ptr(x, "x", et, n),
+                                _ptr(gamma, "gamma", et, dims.d), _ptr(out, "out", et, n),
                                 _stream(stream)), "dflash_rms_norm")
 
 

@@ -96,8 +96,9 @@ class DeviceWorkload:
                 n = int(self.L0[b])
                 if n == 0:
                     continue
-                K, V = synth.cache_rows(w, l, b, n)
-                self.cache.set_rows(l, b, _dev(K, self.dt, self.device), _dev(V, self.dt, self.device))
+                K, V = synth.cache_rows_stored(w, l, b, n)
+                et = self.cache.k.dtype
+                self.cache.set_rows(l, b, _dev(K, et, self.device), _dev(V, et, self.device))
         self.cache.lens.copy_(torch.from_numpy(
             np.tile(self.L0.astype(np.int32), (w.n_layers, 1))).to(self.device))
 

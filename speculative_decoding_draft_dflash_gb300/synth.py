@@ -306,3 +306,21 @@ def cache_rows(w: Workload, layer: int, b: int, n: int = None):
     K = _normal(w, (w.n_kv, n, w.d_h), 1.0, _T_CACHE_K, layer, b)
     V = _normal(w, (w.n_kv, n, w.d_h), 0.02 * np.sqrt(w.d), _T_CACHE_V, layer, b)
     return K, V
+
+
+def to_fp8_codes(a: np.ndarray, scale: float) -> np.ndarray:
+    """E4M3 codes (uint8) of a / scale by torch's float8_e4m3fn conversion: how seeded
+    rows are written into an fp8 device cache before a round."""
+    import torch
+    x = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)) / float(scale)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def cache_rows_stored(w: Workload, layer: int, b: int, n: int = None):
+    """cache_rows in the device cache's element form: storage-rounded values, or for an fp8
+    cache the E4M3 codes of the rows divided by the layer's (k, v) scales."""
+    K, V = cache_rows(w, layer, b, n)
+    if w.kv != "fp8":
+        return K, V
+    ks, vs = kv_scales(w)
+    return to_fp8_codes(K, ks[layer]), to_fp8_codes(V, vs[layer])

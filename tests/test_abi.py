@@ -4,6 +4,7 @@ import glob
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -263,3 +264,154 @@ def test_binding_checks_hidden_state_tensors(D):
     # raw addresses pass through unchanged
     arr = D._ptr_array([4096, 8192])
     assert [arr[0], arr[1]] == [4096, 8192]
+
+
+class _FakeDev:
+    """Stands in for a contiguous CUDA tensor of a given element type and shape (CPU only):
+    the binding's checks read these attributes; nothing reaches the library when one fails."""
+    is_cuda = True
+
+    def __init__(self, shape, dtype):
+        import torch
+        self.shape, self.dtype = tuple(shape), dtype
+        self._n = int(np.prod(shape)) if len(shape) else 1
+        self._es = torch.empty((), dtype=dtype).element_size()
+
+    def is_contiguous(self):
+        return True
+
+    def numel(self):
+        return self._n
+
+    def dim(self):
+        return len(self.shape)
+
+    def element_size(self):
+        return self._es
+
+    def data_ptr(self):
+        return 1 << 20
+
+
+def _serve_args(D, dt):
+    """Well-formed fake arguments of the serving shape (d 4096, 32 / 8 heads of 128, k 5,
+    bs 16, batch 4) in element type dt, and the cache descriptor."""
+    import torch
+    d, nh, nkv, dh, k, bs, B, M = 4096, 32, 8, 128, 5, 16, 4, 20
+    a = dict(hidden=[_FakeDev((M, d), dt) for _ in range(k)], W_fc=_FakeDev((d, k * d), dt),
+             g_h=_FakeDev((d,), dt), C=_FakeDev((M, d), dt), cu=_FakeDev((B + 1,), torch.int32),
+             W_Q=_FakeDev((nh * dh, d), dt), W_K=_FakeDev((nkv * dh, d), dt),
+             W_V=_FakeDev((nkv * dh, d), dt), g_q=_FakeDev((dh,), dt), g_k=_FakeDev((dh,), dt),
+             rope=_FakeDev((64, dh // 2, 2), torch.float32), H=_FakeDev((B, bs, d), dt),
+             out=_FakeDev((B, bs, nh * dh), dt), ws=_FakeDev((1 << 20,), torch.uint8), M=M)
+    cache = D.dflash_kv_cache(4096, 8192, 12288, 1, B, 64)
+    return a, cache
+
+
+@pytest.mark.parametrize("field,bad", [
+    ("hidden", "f32"), ("hidden", "short"), ("W_fc", "f32"), ("W_fc", "short"), ("g_h", "short"),
+    ("C", "f32"), ("C", "short")])
+def test_binding_refuses_ctx_project_mismatch(D, field, bad):
+    """ctx_project: every tensor must be of dims.dtype and hold the elements the dims and M
+    imply; an f32 or short tensor where bf16 [M][d] is needed is refused before the call."""
+    import torch
+    a, _ = _serve_args(D, torch.bfloat16)
+    dims = _dims(D)
+
+    def spoil(t):
+        if bad == "f32":
+            return _FakeDev(t.shape, torch.float32)
+        return _FakeDev((t.numel() - 1,), t.dtype)
+
+    if field == "hidden":
+        a["hidden"][2] = spoil(a["hidden"][2])
+    else:
+        a[field] = spoil(a[field])
+    for fn in (lambda: D.dflash_ctx_project(dims, a["hidden"], a["M"], a["W_fc"], a["g_h"], a["C"],
+                                            a["ws"]),
+               lambda: D.dflash_ctx_project_noalloc(dims, a["hidden"], a["M"], a["W_fc"], a["g_h"],
+                                                    a["C"])):
+        with pytest.raises(ValueError, match="element type|elements"):
+            fn()
+
+
+@pytest.mark.parametrize("field,bad", [
+    ("C", "f32"), ("cu", "short"), ("cu", "i64"), ("W_K", "short"), ("W_V", "f32"),
+    ("g_k", "short"), ("rope", "bf16"), ("rope", "short"), ("H", "short"), ("H", "f32"),
+    ("W_Q", "short"), ("g_q", "f32"), ("out", "short"), ("out", "f32")])
+def test_binding_refuses_layer_call_mismatch(D, field, bad):
+    """kv_inject, block_attn and draft_layer refuse a tensor whose element type or size does
+    not match the dims, the cache's batch, M or table_len, before the library is called."""
+    import torch
+    a, cache = _serve_args(D, torch.bfloat16)
+    dims = _dims(D)
+    t = a[field]
+    a[field] = {"f32": lambda: _FakeDev(t.shape, torch.float32),
+                "bf16": lambda: _FakeDev(t.shape, torch.bfloat16),
+                "i64": lambda: _FakeDev(t.shape, torch.int64),
+                "short": lambda: _FakeDev((t.numel() - 1,), t.dtype)}[bad]()
+    calls = [lambda: D.dflash_draft_layer(dims, cache, 0, a["C"], a["cu"], a["M"], a["H"], a["W_Q"],
+                                          a["W_K"], a["W_V"], a["g_q"], a["g_k"], a["rope"], 64, 0,
+                                          0.0, a["out"], a["ws"])]
+    if field in ("C", "cu", "W_K", "W_V", "g_k", "rope"):
+        calls.append(lambda: D.dflash_kv_inject(dims, cache, 0, a["C"], a["cu"], a["M"], a["W_K"],
+                                                a["W_V"], a["g_k"], a["rope"], 64, a["ws"]))
+    if field not in ("C", "cu"):
+        calls.append(lambda: D.dflash_block_attn(dims, cache, 0, a["H"], a["W_Q"], a["W_K"],
+                                                 a["W_V"], a["g_q"], a["g_k"], a["rope"], 64, 0,
+                                                 0.0, a["out"], a["ws"]))
+    for fn in calls:
+        with pytest.raises(ValueError, match="element type|elements"):
+            fn()
+
+
+def test_binding_refuses_small_calls_mismatch(D):
+    """crop, accept, rms_norm, layer_out and the RoPE table builder check their tensors too."""
+    import torch
+    dims = _dims(D)
+    cache = D.dflash_kv_cache(4096, 8192, 12288, 1, 4, 64)
+    with pytest.raises(ValueError, match="elements"):
+        D.dflash_cache_crop(cache, _FakeDev((3,), torch.int32))
+    with pytest.raises(ValueError, match="element type"):
+        D.dflash_cache_crop(cache, _FakeDev((4,), torch.int64))
+    i32 = lambda *s: _FakeDev(s, torch.int32)  # noqa: E731
+    ids = i32(4, 16)
+    with pytest.raises(ValueError, match="elements"):
+        D.dflash_accept(ids, i32(4, 15), i32(4), i32(4), i32(5), i32(4), i32(4))
+    with pytest.raises(ValueError, match="elements"):
+        D.dflash_accept(ids, i32(4, 16), i32(4), i32(4), i32(4), i32(4), i32(4))
+    bf = lambda *s: _FakeDev(s, torch.bfloat16)  # noqa: E731
+    with pytest.raises(ValueError, match="element type"):
+        D.dflash_rms_norm(dims, 8, _FakeDev((8, 4096), torch.float32), bf(4096), bf(8, 4096))
+    with pytest.raises(ValueError, match="elements"):
+        D.dflash_rms_norm(dims, 8, bf(8, 4096), bf(4095), bf(8, 4096))
+    args = [bf(8, 4096), bf(8, 4096), bf(4096, 4096), bf(4096), 12288, bf(12288, 4096),
+            bf(12288, 4096), bf(4096, 12288), bf(8, 4096), _FakeDev((64,), torch.uint8)]
+    for i in (0, 1, 2, 3, 5, 6, 7, 8):
+        bad = list(args)
+        bad[i] = _FakeDev((bad[i].numel() - 1,), torch.bfloat16)
+        with pytest.raises(ValueError, match="elements"):
+            D.dflash_layer_out(dims, 8, *bad)
+    with pytest.raises(ValueError, match="element type"):
+        D.dflash_rope_table_build(1e6, 128, 64, _FakeDev((64, 64, 2), torch.bfloat16))
+    with pytest.raises(ValueError, match="elements"):
+        D.dflash_rope_table_build(1e6, 128, 64, _FakeDev((63, 64, 2), torch.float32))
+
+
+def test_binding_refuses_cache_of_other_dims(D):
+    """A KVCache whose heads, head size or element type differ from the dims is refused."""
+    import torch
+    a, _ = _serve_args(D, torch.bfloat16)
+    dims = _dims(D)
+
+    class FakeCache(D.KVCache):
+        def __init__(self, n_kv, d_h, dt, fp8=False):     # no device buffers are made
+            self.n_kv, self.d_h, self.fp8 = n_kv, d_h, fp8
+            self.k = self.v = _FakeDev((1,), dt)
+            self.desc = D.dflash_kv_cache(4096, 8192, 12288, 1, 4, 64)
+
+    for c in (FakeCache(4, 128, torch.bfloat16), FakeCache(8, 64, torch.bfloat16),
+              FakeCache(8, 128, torch.float32), FakeCache(8, 128, torch.bfloat16, fp8=True)):
+        with pytest.raises(ValueError, match="cache"):
+            D.dflash_kv_inject(dims, c, 0, a["C"], a["cu"], a["M"], a["W_K"], a["W_V"], a["g_k"],
+                               a["rope"], 64, a["ws"])
