@@ -2,7 +2,14 @@
 // fp32 accumulator in tensor memory.
 //
 // One CTA computes a 128 x BN tile over its share of K (split-K across
-// gridDim.z):
+// gridDim.z). When M spans more than one 128-row tile, CTAs run in clusters of
+// two (tcgen05.mma.cta_group::2): the even CTA issues M = 256 MMAs whose A rows
+// come 128 from each CTA's shared memory and whose B rows come half from each,
+// so every SM stages and reads half the weight bytes per MMA (the one-CTA tile
+// is bound by shared-memory bandwidth near two thirds of the tensor rate). Both
+// CTAs' copies complete on the even CTA's full barrier; its commits arrive on
+// both CTAs' empty and done barriers; each CTA's epilogue reads its own 128 TMEM
+// lanes. Roles per CTA:
 //   warp 0      TMA producer: 128 x 64 activation tile + BN x 64 weight tile
 //               per stage, 128-byte swizzle, completion on a "full" mbarrier;
 //   warp 1      allocates BN TMEM columns and issues tcgen05.mma (M=128,
@@ -69,12 +76,15 @@ struct TcGemmParams {
   sched::Params sp;
 };
 
-template <int BN>
+// PAIR: the tile is computed by a cluster of two CTAs (tcgen05.mma.cta_group::2, M = 256):
+// each CTA holds its own 128 rows of A and half of B's BN rows per stage.
+template <int BN, bool PAIR = false>
 struct Cfg {
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;
   static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
   static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int STAGES = PAIR ? ((BN == 256) ? 6 : 8) : ((BN == 256) ? 4 : 6);
   // pipeline stages, barriers (256 B), then gamma_q / gamma_k as fp32 (heads epilogue)
   static constexpr uint32_t OFF_GAMMA = STAGES * STAGE + 256;
   static constexpr size_t SMEM = 1024 + (size_t)OFF_GAMMA + 2 * 128 * 4;
@@ -219,10 +229,10 @@ __device__ __forceinline__ HeadEpilogue pick_epilogue(const TcGemmParams& p, boo
   return e;
 }
 
-template <int BN, bool HEADS>
+template <int BN, bool HEADS, bool PAIR>
 __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const __grid_constant__ TcGemmParams p) {
   constexpr int kThreads = gemm_threads(HEADS);
-  using C = Cfg<BN>;
+  using C = Cfg<BN, PAIR>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -255,7 +265,12 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
   const HeadEpilogue ep = pick_epilogue(p, second);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * BM, n0 = (second ? col - p.ny0 : col) * BN;
-  if (m0 >= M) return;  // grid.x covers the taller problem
+  // grid.x covers the taller problem. A pair leaves only as a whole (both CTAs take the
+  // same branch), since each waits for the other below; a pair's odd CTA may hold no rows
+  // of M (its A tile is zero fill, its epilogue stores nothing).
+  if ((PAIR ? (int)(blockIdx.x & ~1u) * BM : m0) >= M) return;
+  // PAIR: CTA 0 of the cluster issues the MMAs; CTA 1 loads its halves and runs its epilogue
+  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0;
   const int kb0 = blockIdx.z * p.kb_per_split;
   const int nkb = min(p.kb_total, kb0 + p.kb_per_split) - kb0;
   const uint32_t full0 = ptx::smem_u32(bars);
@@ -276,11 +291,20 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
     for (int i = 0; i < w_count; ++i) ptx::prefetch_tmap(&bmap[i]);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), TMEM_COLS);
-    ptx::tmem_relinquish();
+    if (PAIR) {
+      // collective with the peer CTA's warp 1: the same columns in both CTAs' TMEM
+      ptx::tmem_alloc_pair(ptx::smem_u32(&tmem_slot), TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
+  // PAIR: both CTAs' barriers are initialised before either CTA's copies or commits can
+  // reach the other's
+  if (PAIR) ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
@@ -290,6 +314,9 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
 
   if (warp == 0) {
     if (lane == 0) {
+      // PAIR: both CTAs' copies complete on CTA 0's full barrier, which CTA 0 arms for the
+      // bytes of both; CTA 1 loads the second half of the B tile
+      const uint32_t brow = nb + rank * C::B_ROWS;
       int issued = 0;
       for (int i = 0; i < nkb; ++i) {
         const int s = i % STAGES;
@@ -299,18 +326,31 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
         const int seg = kb / kseg_blocks;
         const int kx = (kb - seg * kseg_blocks) * BK;
         const uint32_t sa = ptx::smem_u32(smem + (size_t)s * C::STAGE);
-        ptx::mbar_arrive_expect_tx(full0 + 8 * s, C::STAGE);
-        ptx::tma_load_2d(sa, &amap[seg], full0 + 8 * s, kx, m0);
-        ptx::tma_load_2d(sa + C::A_BYTES, &bmap[wi], full0 + 8 * s, kb * BK, nb);
+        if (!PAIR) {
+          ptx::mbar_arrive_expect_tx(full0 + 8 * s, C::STAGE);
+          ptx::tma_load_2d(sa, &amap[seg], full0 + 8 * s, kx, m0);
+          ptx::tma_load_2d(sa + C::A_BYTES, &bmap[wi], full0 + 8 * s, kb * BK, nb);
+        } else {
+          if (rank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, 2 * C::STAGE);
+          const uint32_t fb = ptx::mapa_shared(full0 + 8 * s, 0);
+          ptx::tma_load_2d_pair(sa, &amap[seg], fb, kx, m0);
+          ptx::tma_load_2d_pair(sa + C::A_BYTES, &bmap[wi], fb, kb * BK, brow);
+        }
         ++issued;
       }
-      // no copy of ours may still be landing when the CTA exits
-      for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
-        drain_wait(full0 + 8 * (i % STAGES), (i / STAGES) & 1, p.status);
+      // no copy of ours may still be landing when the CTA exits: CTA 0 (and a single CTA)
+      // waits for its last stages to fill; CTA 1, whose copies count on CTA 0's barriers,
+      // waits until the MMAs have released its last stages (they read them, so they landed)
+      for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i) {
+        if (rank == 0)
+          drain_wait(full0 + 8 * (i % STAGES), (i / STAGES) & 1, p.status);
+        else
+          drain_wait(empty0 + 8 * (i % STAGES), (i / STAGES) & 1, p.status);
+      }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
       for (int i = 0; i < nkb; ++i) {
         const int s = i % STAGES;
         const uint32_t ph = (i / STAGES) & 1;
@@ -319,12 +359,23 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
         const uint32_t sa = ptx::smem_u32(smem + (size_t)s * C::STAGE);
         const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k)
-          ptx::mma_bf16(tmem, ptx::smem_desc_sw128(sa + 32 * k), ptx::smem_desc_sw128(sb + 32 * k),
-                        idesc, (i > 0 || k > 0) ? 1u : 0u);
-        ptx::mma_commit(empty0 + 8 * s);
+        for (int k = 0; k < BK / 16; ++k) {
+          if (PAIR)
+            ptx::mma_bf16_pair(tmem, ptx::smem_desc_sw128(sa + 32 * k),
+                               ptx::smem_desc_sw128(sb + 32 * k), idesc, (i > 0 || k > 0) ? 1u : 0u);
+          else
+            ptx::mma_bf16(tmem, ptx::smem_desc_sw128(sa + 32 * k), ptx::smem_desc_sw128(sb + 32 * k),
+                          idesc, (i > 0 || k > 0) ? 1u : 0u);
+        }
+        if (PAIR)
+          ptx::mma_commit_pair(empty0 + 8 * s, 3);  // frees stage s in both CTAs
+        else
+          ptx::mma_commit(empty0 + 8 * s);
       }
-      ptx::mma_commit(done);
+      if (PAIR)
+        ptx::mma_commit_pair(done, 3);
+      else
+        ptx::mma_commit(done);
       drain_wait(done, 0, p.status);  // every MMA has finished before TMEM can be freed
     }
   } else {
@@ -494,9 +545,15 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
   }
   ptx::tc_fence_before();
   __syncthreads();
+  // PAIR: neither CTA leaves (or frees TMEM) while the other may still read its shared
+  // memory through the MMAs or receive its commits; every path of both CTAs reaches this
+  if (PAIR) ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, TMEM_COLS);
+    if (PAIR)
+      ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
+    else
+      ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
@@ -523,7 +580,23 @@ EncodeTiledFn encode_fn() {
 
 struct Plan {
   int bn, kb_total, kb_per_split, splits;
+  bool pair;  // CTA pairs (M = 256 per MMA) instead of single CTAs
+  int gx;     // grid.x: CTAs along M (even with pairs)
 };
+
+// CTA pairs halve the shared-memory operand bytes per SM (each CTA reads its own 128 rows
+// of A and half of B) once M spans more than one 128-row tile; DFLASH_PAIR_GEMM=0 keeps
+// single-CTA tiles everywhere (the same arithmetic).
+bool pair_wanted(int M) {
+  const char* env = getenv("DFLASH_PAIR_GEMM");
+  if (env && env[0] == '0') return false;
+  return M > BM;
+}
+
+int grid_x(int M, bool pair) {
+  const int mt = (M + BM - 1) / BM;
+  return pair ? (mt + 1) & ~1 : mt;
+}
 
 // The widest of 256/128/64 that divides every stacked weight (heads: 256 or
 // 128, whole heads per tile). Split-K to about one wave on the GPU.
@@ -534,8 +607,10 @@ Plan plan(int M, const Weights& W, int K, bool heads) {
     while (W.n[i] % pl.bn) pl.bn >>= 1;
   if (heads && pl.bn < 128) pl.bn = 0;  // heads need whole 128-dim heads per tile
   if (pl.bn == 0) return pl;
+  pl.pair = pl.bn >= 128 && pair_wanted(M);
+  pl.gx = grid_x(M, pl.pair);
   pl.kb_total = K / BK;
-  const int tiles = ((M + BM - 1) / BM) * (W.total() / pl.bn);
+  const int tiles = pl.gx * (W.total() / pl.bn);
   int splits = 148 / (tiles > 0 ? tiles : 1);
   const int max_splits = pl.kb_total / 4 > 0 ? pl.kb_total / 4 : 1;
   if (splits > max_splits) splits = max_splits;
@@ -545,15 +620,37 @@ Plan plan(int M, const Weights& W, int K, bool heads) {
   return pl;
 }
 
-template <int BN, bool HEADS>
-cudaError_t launch(const TcGemmParams& p, dim3 grid, cudaStream_t s) {
-  const size_t smem = Cfg<BN>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, HEADS>,
+template <int BN, bool HEADS, bool PAIR>
+cudaError_t launch_one(const TcGemmParams& p, dim3 grid, cudaStream_t s) {
+  const size_t smem = Cfg<BN, PAIR>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, HEADS, PAIR>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   LaunchScope ls_(DFLASH_KERNEL_GEMM, s);
-  gemm_tc_kernel<BN, HEADS><<<grid, gemm_threads(HEADS), smem, s>>>(p);
-  return cudaGetLastError();
+  if constexpr (!PAIR) {
+    gemm_tc_kernel<BN, HEADS, false><<<grid, gemm_threads(HEADS), smem, s>>>(p);
+    return cudaGetLastError();
+  } else {
+    if (grid.x & 1) return cudaErrorInvalidValue;  // whole pairs only
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(gemm_threads(HEADS), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, HEADS, true>, p);
+  }
+}
+
+template <int BN, bool HEADS>
+cudaError_t launch(const TcGemmParams& p, dim3 grid, bool pair, cudaStream_t s) {
+  return pair ? launch_one<BN, HEADS, true>(p, grid, s) : launch_one<BN, HEADS, false>(p, grid, s);
 }
 
 }  // namespace
@@ -602,7 +699,8 @@ cudaError_t fill_common(TcGemmParams& p, const Segments& A, int M, const Weights
   for (int i = A.n; i < 8; ++i) p.a[i] = p.a[0];
   int off = 0;
   for (int i = 0; i < W.count; ++i) {
-    if (!encode_2d_bf16(&p.b[i], W.p[i], W.n[i], K, pl.bn)) return cudaErrorInvalidValue;
+    if (!encode_2d_bf16(&p.b[i], W.p[i], W.n[i], K, pl.pair ? pl.bn / 2 : pl.bn))
+      return cudaErrorInvalidValue;
     p.w_off[i] = off;
     off += W.n[i];
   }
@@ -631,11 +729,11 @@ cudaError_t gemm_tc(const Segments& A, int M, const Weights& W, float* Y, int ld
   p.ldY = ldY;
   p.Y = Y;
   p.status = status;
-  dim3 grid((M + BM - 1) / BM, N / pl.bn, pl.splits);
+  dim3 grid(pl.gx, N / pl.bn, pl.splits);
   switch (pl.bn) {
-    case 256: return launch<256, false>(p, grid, s);
-    case 128: return launch<128, false>(p, grid, s);
-    default: return launch<64, false>(p, grid, s);
+    case 256: return launch<256, false>(p, grid, pl.pair, s);
+    case 128: return launch<128, false>(p, grid, pl.pair, s);
+    default: return launch_one<64, false, false>(p, grid, s);
   }
 }
 
@@ -651,8 +749,9 @@ cudaError_t gemm_tc_heads(const Segments& A, int M, const Weights& W, const Head
   if (e != cudaSuccess) return e;
   p.ep = ep;
   p.status = status;
-  dim3 grid((M + BM - 1) / BM, N / pl.bn, 1);
-  return pl.bn == 256 ? launch<256, true>(p, grid, s) : launch<128, true>(p, grid, s);
+  dim3 grid(pl.gx, N / pl.bn, 1);
+  return pl.bn == 256 ? launch<256, true>(p, grid, pl.pair, s)
+                      : launch<128, true>(p, grid, pl.pair, s);
 }
 
 // Both projections of a draft layer in one launch: the context rows' K/V (inject) and
@@ -689,6 +788,8 @@ cudaError_t gemm_tc_layer(const void* C, int Mc, const Weights& Wkv, const HeadE
   pl.kb_total = K / BK;
   pl.kb_per_split = pl.kb_total;
   pl.splits = 1;
+  // one instantiation serves both problems: pairs when both span more than one M tile
+  pl.pair = pair_wanted(Mc) && pair_wanted(Mb);
   Segments A;
   A.n = 1;
   A.kseg = K;
@@ -701,7 +802,8 @@ cudaError_t gemm_tc_layer(const void* C, int Mc, const Weights& Wkv, const HeadE
   if (!encode_2d_bf16(&p.a1, H, Mb, K, BM)) return cudaErrorInvalidValue;
   int off = 0;
   for (int i = 0; i < Wqkv.count; ++i) {
-    if (!encode_2d_bf16(&p.b1[i], Wqkv.p[i], Wqkv.n[i], K, bn)) return cudaErrorInvalidValue;
+    if (!encode_2d_bf16(&p.b1[i], Wqkv.p[i], Wqkv.n[i], K, pl.pair ? bn / 2 : bn))
+      return cudaErrorInvalidValue;
     p.w1_off[i] = off;
     off += Wqkv.n[i];
   }
@@ -713,9 +815,9 @@ cudaError_t gemm_tc_layer(const void* C, int Mc, const Weights& Wkv, const HeadE
   p.ny1 = Wqkv.total() / bn;
   p.sched_cta = sp != nullptr;
   if (sp) p.sp = *sp;
-  const int mt0 = (Mc + BM - 1) / BM, mt1 = (Mb + BM - 1) / BM;
+  const int mt0 = grid_x(Mc, pl.pair), mt1 = grid_x(Mb, pl.pair);
   dim3 grid(mt0 > mt1 ? mt0 : mt1, p.ny0 + p.ny1 + (sp ? 1 : 0), 1);
-  return bn == 256 ? launch<256, true>(p, grid, s) : launch<128, true>(p, grid, s);
+  return bn == 256 ? launch<256, true>(p, grid, pl.pair, s) : launch<128, true>(p, grid, pl.pair, s);
 }
 
 }  // namespace dflash

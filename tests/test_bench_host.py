@@ -68,3 +68,22 @@ def test_attention_bytes_worked_example():
     assert bench.attention_bytes(w, starts) == 5148 * 4096 + qo == 21872640
     assert bench.attention_bytes(w, starts, 64) == 174 * 4096 + qo == 1499136
     assert bench.attention_bytes(w.replace(kv="fp8"), starts) == 5148 * 2048 + qo == 11329536
+
+
+def test_gemm_roofline_uses_the_burst_peak():
+    """A projection GEMM above the ridge point is reported against the burst bf16 peak (its
+    launches last tens of microseconds at the maximum clock), with the sustained fraction
+    alongside; 85.9 GFLOP in 50 us is 1718 TFLOP/s."""
+    pk = {"hbm_gbs": 6784.5, "bf16_tflops": 1954.5, "bf16_tflops_sustained": 1739.5,
+          "source": "measured"}
+    fl, by = bench.gemm_cost(512, 5 * 4096, 4096)
+    kernels = {"gemm_fc": {"avg_us": 50.0}}
+    r = bench.roofline_for("gemm_fc", kernels, {"gemm_fc": (fl, by)}, 0, pk)
+    assert r["bound"] == "tensor" and r["peak"] == 1954.5
+    assert abs(r["achieved"] - fl / 50e-6 / 1e12) < 1e-9
+    assert abs(r["frac"] - r["achieved"] / 1954.5) < 1e-12
+    assert abs(r["frac_of_sustained"] - r["achieved"] / 1739.5) < 1e-12
+    # a weight-streaming GEMM (M = 16) sits below the ridge: HBM-bound
+    fl, by = bench.gemm_cost(16, 5 * 4096, 4096)
+    r = bench.roofline_for("gemm_fc", {"gemm_fc": {"avg_us": 30.0}}, {"gemm_fc": (fl, by)}, 0, pk)
+    assert r["bound"] == "hbm" and r["peak"] == 6784.5

@@ -32,6 +32,12 @@ SMALL = {
         name="small_gqa_f32", d=96, n_h=6, n_kv=2, d_h=32, k=2, bs=3, batch=3, n_layers=2,
         windows=(0, 5), prefill_lo=0, prefill_hi=600, new_ctx=4, rounds=2, seed=6,
         random_gamma=True),
+    # 20 sequences: 320 block rows and 320 context rows in round 1, so the projections run
+    # on CTA pairs (three 128-row tiles: the second pair's odd CTA holds no rows); round 2
+    # injects a_i rows, a ragged M
+    "small_pairs_bf16": W["serve_b32"].replace(
+        name="small_pairs_bf16", d=256, n_h=4, n_kv=2, k=2, batch=20, n_layers=1, windows=(0,),
+        prefill_lo=0, prefill_hi=400, seed=8, random_gamma=True),
     "small_bs1_f32": W["walkthrough_f32"].replace(
         name="small_bs1_f32", d=64, n_h=2, n_kv=1, d_h=64, k=1, bs=1, batch=2, n_layers=1,
         windows=(0,), prefill_lo=255, prefill_hi=257, new_ctx=1, rounds=2, seed=7),
@@ -133,3 +139,12 @@ def test_output_16_byte_aligned(name):
     seqs = list(range(w.batch))
     dev_res, _ = harness.device_rounds(w, seqs, dev=dev)
     harness.compare(w, dev_res, harness.oracle_rounds(w, seqs), seqs)
+
+
+@pytest.mark.parametrize("pairs", ["0", "1"])
+def test_single_and_paired_projection_tiles(pairs, monkeypatch):
+    """The projections on single-CTA tiles (DFLASH_PAIR_GEMM=0) and on CTA pairs give the
+    same results at shapes where both apply (M > 128 rows)."""
+    monkeypatch.setenv("DFLASH_PAIR_GEMM", pairs)
+    w = SMALL["small_pairs_bf16"]
+    _run(w, list(range(w.batch)))
