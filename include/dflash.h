@@ -143,7 +143,11 @@ size_t dflash_workspace_bytes(const dflash_dims* dims, int batch, int capacity, 
  * (DFlash KV Injection Walkthrough, Step 1: extract_context_feature, layers
  * concatenated on the feature axis in ascending order; Step 2: fc without
  * bias, then hidden_norm.) The concatenation is never formed: each hidden[j]
- * is read as the j-th K-segment of the projection.
+ * is read as the j-th K-segment of the projection. hidden_norm runs as a pass
+ * over the projection's fp32 split partials (bf16 with DFLASH_FUSED_NORM=1 in
+ * the environment: in the projection's epilogue instead, the tiles of a row
+ * block exchanging their rows' sums of squares through the workspace, when all
+ * the projection's CTAs fit on the GPU at once; slower at the measured shapes).
  *   hidden     host array of k_layers device pointers, each [M][d]
  *   M          rows (>= 0; 0 is a no-op)
  *   W_fc       device [d][k_layers * d]
@@ -163,19 +167,25 @@ dflash_status dflash_ctx_project(const dflash_dims* dims, const void* const* hid
  * and a cudaMalloc would break its accounting and stall the device. Same
  * arguments and results as dflash_ctx_project, minus the workspace: the
  * scratch is a fixed array of DFLASH_NOALLOC_SCRATCH_BYTES inside the library,
- * held on every GPU that loads it until the process exits (about 4M fp32
- * values: 1024 rows at d = 4096 in one pass).
+ * held on every GPU that loads it until the process exits.
  *  - No allocation of any kind happens in this call.
- *  - A call needing more scratch than the array returns DFLASH_ERR_WORKSPACE
- *    and launches nothing.
+ *  - Size rule: the fc splits K over several CTAs, each split with its own
+ *    M x d fp32 partial, as many as dflash_ctx_project uses (the array is sized
+ *    so that at d = 4096 it always holds them, and the two calls give the same
+ *    bits); where they would not fit, this call uses fewer splits, down to one.
+ *    So a call fits exactly when its one-split scratch fits: M * d * 4 bytes of
+ *    partial, M * (d / 256) * 4 bytes of per-tile row sums (bf16) and under 2 KB
+ *    of counters, within 20 MiB: up to 1274 rows at d = 4096, and every smaller
+ *    M. A larger call returns DFLASH_ERR_WORKSPACE and launches nothing.
  *  - The first call on each device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
  *  - Every call on a device shares the one array, which keeps whatever the
- *    previous call left in it (nothing in it needs to start at zero). Calls
- *    that can run at the same time on the GPU (other streams, other host
- *    threads) race on it: serialise them.
+ *    previous call left in it; the counters that must start at zero are
+ *    cleared by each call on its own stream. Calls that can run at the same
+ *    time on the GPU (other streams, other host threads) race on it:
+ *    serialise them.
  */
-#define DFLASH_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+#define DFLASH_NOALLOC_SCRATCH_BYTES ((size_t)20 << 20)
 dflash_status dflash_ctx_project_noalloc(const dflash_dims* dims, const void* const* hidden, int M,
                                          const void* W_fc, const void* gamma_h, void* C_out,
                                          cudaStream_t stream);
@@ -357,6 +367,19 @@ dflash_status dflash_trace_stop(int* kinds, float* ms, int capacity, int* count)
 
 /* Number of kernels the library has launched in this process so far. */
 unsigned long long dflash_launch_count(void);
+
+/*
+ * Test aid (no counterpart in the source pages): sets the time limit, in ns, of the
+ * pipeline waits of the tensor-core kernels (the waits of one role of a kernel for
+ * another's data, and the context projection's waits for the other tiles of a row
+ * block) in every launch made after the call, in this process; 0 restores the default
+ * of 2 s. A wait that runs out sets DFLASH_DEV_TIMEOUT and makes its kernel stop: the
+ * waits that let in-flight copies and MMAs finish before the kernel exits keep their
+ * 2 s limit, so a kernel that gives up still frees its tensor memory and returns, and
+ * later launches work. Not for production use: a short limit turns ordinary latency
+ * into errors.
+ */
+void dflash_test_wait_limit(unsigned long long ns);
 
 #ifdef __cplusplus
 }

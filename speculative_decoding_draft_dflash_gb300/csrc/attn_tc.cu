@@ -141,6 +141,7 @@ struct AttnTcParams {
   float sl2;      // scaling * log2(e) (fp8: times k_scale)
   float v_scale;  // fp8: scale of the V codes
   int out_v8;     // out is 32-byte aligned: rows leave in 32-byte stores
+  unsigned long long wait_ns;  // limit of the pipeline waits (2 s unless a test lowers it)
 };
 
 __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity, unsigned* status) {
@@ -330,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (;; ++n) {
         const int slot = n % kRing;
         if (n >= kRing &&
-            !ptx::mbar_wait(it_empty0 + 8 * slot, ((n / kRing) - 1) & 1, &abort_flag, p.status))
+            !ptx::mbar_wait(it_empty0 + 8 * slot, ((n / kRing) - 1) & 1, &abort_flag, p.status, p.wait_ns))
           break;
         const int4 it = idx < n_items ? p.items[idx] : make_int4(-1, 0, 0, 0);
         ring[slot] = it;
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         idx = gridDim.x + atomicAdd(p.next_item, 1);  // prefetch the next item's index
         const int b = it.x / p.n_kv, kvh = it.x - b * p.n_kv;
         const int qb = n & 1;
-        if (n >= 2 && !ptx::mbar_wait(q_empty0 + 8 * qb, ((n >> 1) - 1) & 1, &abort_flag, p.status))
+        if (n >= 2 && !ptx::mbar_wait(q_empty0 + 8 * qb, ((n >> 1) - 1) & 1, &abort_flag, p.status, p.wait_ns))
           break;
         const int qrow = (b * p.n_h + kvh * p.G) * p.bs;
         const uint32_t qd = sbase + PL::q_base(qb);
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           if (j + 1 < ntiles) row_next = tile_row(p, b, kvh, it.y + (j + 1) * TK);
           const int s = gk % PL::K_STAGES, u = gk / PL::K_STAGES;
           if (gk >= PL::K_STAGES &&
-              !ptx::mbar_wait(k_empty0 + 8 * s, (u - 1) & 1, &abort_flag, p.status)) {
+              !ptx::mbar_wait(k_empty0 + 8 * s, (u - 1) & 1, &abort_flag, p.status, p.wait_ns)) {
             stop = true;
             break;
           }
@@ -383,14 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       bool stop = false;
       for (int n = 0; !stop; ++n) {
         const int slot = n % kRing;
-        if (!ptx::mbar_wait(it_full0 + 8 * slot, (n / kRing) & 1, &abort_flag, p.status)) break;
+        if (!ptx::mbar_wait(it_full0 + 8 * slot, (n / kRing) & 1, &abort_flag, p.status, p.wait_ns)) break;
         const int4 it = ring[slot];
         ptx::mbar_arrive(it_empty0 + 8 * slot);
         if (it.x < 0) break;
         // At the start every CTA asks HBM for its first tiles at once, and the first S
         // needs only Q and K_0: V waits until K_0 has landed, so that it is not queued
         // ahead of it (V_0 is needed only after the first tile's softmax).
-        if (n == 0 && !ptx::mbar_wait(k_full0, 0, &abort_flag, p.status)) break;
+        if (n == 0 && !ptx::mbar_wait(k_full0, 0, &abort_flag, p.status, p.wait_ns)) break;
         const int b = it.x / p.n_kv, kvh = it.x - b * p.n_kv;
         const int ntiles = (it.z - it.y + TK - 1) / TK;
         int row_next = tile_row(p, b, kvh, it.y);
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           if (j + 1 < ntiles) row_next = tile_row(p, b, kvh, it.y + (j + 1) * TK);
           const int s = gv % PL::V_STAGES, u = gv / PL::V_STAGES;
           if (gv >= PL::V_STAGES &&
-              !ptx::mbar_wait(v_empty0 + 8 * s, (u - 1) & 1, &abort_flag, p.status)) {
+              !ptx::mbar_wait(v_empty0 + 8 * s, (u - 1) & 1, &abort_flag, p.status, p.wait_ns)) {
             stop = true;
             break;
           }
@@ -425,20 +426,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       bool stop = false, issued = false;
       for (int n = 0; !stop; ++n) {
         const int slot = n % kRing;
-        if (!ptx::mbar_wait(it_full0 + 8 * slot, (n / kRing) & 1, &abort_flag, p.status)) break;
+        if (!ptx::mbar_wait(it_full0 + 8 * slot, (n / kRing) & 1, &abort_flag, p.status, p.wait_ns)) break;
         const int4 it = ring[slot];
         ptx::mbar_arrive(it_empty0 + 8 * slot);
         if (it.x < 0) break;
         const int qb = n & 1;
-        if (!ptx::mbar_wait(q_full0 + 8 * qb, (n >> 1) & 1, &abort_flag, p.status)) break;
+        if (!ptx::mbar_wait(q_full0 + 8 * qb, (n >> 1) & 1, &abort_flag, p.status, p.wait_ns)) break;
         const int T = (it.z - it.y + TK - 1) / TK, base = gt;
         const uint32_t qa = sbase + PL::q_base(qb);
         auto issue_s = [&](int j) -> bool {
           const int g = base + j, s = g & 1, u = g >> 1;
           const int ks = g % PL::K_STAGES, ku = g / PL::K_STAGES;
-          if (g >= 2 && !ptx::mbar_wait(s_free0 + 8 * s, (u - 1) & 1, &abort_flag, p.status))
+          if (g >= 2 && !ptx::mbar_wait(s_free0 + 8 * s, (u - 1) & 1, &abort_flag, p.status, p.wait_ns))
             return false;
-          if (!ptx::mbar_wait(k_full0 + 8 * ks, ku & 1, &abort_flag, p.status)) return false;
+          if (!ptx::mbar_wait(k_full0 + 8 * ks, ku & 1, &abort_flag, p.status, p.wait_ns)) return false;
           ptx::tc_fence_after();
           const uint32_t ka = sbase + PL::OFF_K + ks * PL::TILE_B;
           if (FP8) {
@@ -476,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           const int vs = PL::CONV ? g % PL::C_STAGES : g % PL::V_STAGES;
           const int vu = PL::CONV ? g / PL::C_STAGES : g / PL::V_STAGES;
           const uint32_t vfull = PL::CONV ? c_full0 : v_full0;
-          if (!ptx::mbar_wait(p_full0 + 8 * (g & 1), (g >> 1) & 1, &abort_flag, p.status) ||
-              !ptx::mbar_wait(vfull + 8 * vs, vu & 1, &abort_flag, p.status)) {
+          if (!ptx::mbar_wait(p_full0 + 8 * (g & 1), (g >> 1) & 1, &abort_flag, p.status, p.wait_ns) ||
+              !ptx::mbar_wait(vfull + 8 * vs, vu & 1, &abort_flag, p.status, p.wait_ns)) {
             stop = true;
             break;
           }
@@ -520,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     int gv = 0;
     for (int n = 0;; ++n) {
       const int slot = n % kRing;
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(it_full0 + 8 * slot, (n / kRing) & 1, &abort_flag, p.status)))
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(it_full0 + 8 * slot, (n / kRing) & 1, &abort_flag, p.status, p.wait_ns)))
         break;
       const int4 it = ring[slot];
       ptx::mbar_arrive(it_empty0 + 8 * slot);
@@ -530,10 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (int j = 0; j < T; ++j) {
         const int g = gv + j, vs = g % PL::V_STAGES, cs = g % PL::C_RING;
         alive = __all_sync(0xffffffffu, ptx::mbar_wait(v_full0 + 8 * vs, (g / PL::V_STAGES) & 1,
-                                                       &abort_flag, p.status));
+                                                       &abort_flag, p.status, p.wait_ns));
         if (alive && g >= PL::C_RING)
           alive = __all_sync(0xffffffffu, ptx::mbar_wait(c_empty0 + 8 * cs, ((g / PL::C_RING) - 1) & 1,
-                                                         &abort_flag, p.status));
+                                                         &abort_flag, p.status, p.wait_ns));
         if (!alive) break;
         const uint8_t* src = smem + PL::OFF_V + vs * PL::TILE_B + k * 128;
         uint8_t* dst = smem + PL::OFF_C + cs * TILE + k * 128;
@@ -572,10 +573,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     int gt = 0;
     float s[NCOL];
+    // Abort safety: the softmax threads meet at named barriers, which do not time out, so
+    // a thread whose wait gave up never leaves on its own. It skips its work up to the next
+    // barrier, whose OR of "gave up" flags then sends every softmax thread out together.
     for (int n = 0;; ++n) {
       const int slot = n % kRing;
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(it_full0 + 8 * slot, (n / kRing) & 1, &abort_flag, p.status)))
-        break;
+      const bool got = __all_sync(0xffffffffu, ptx::mbar_wait(it_full0 + 8 * slot, (n / kRing) & 1, &abort_flag, p.status, p.wait_ns));
+      if (ptx::named_sync_or(2, n_soft, !got)) break;
       const int4 it = ring[slot];
       ptx::mbar_arrive(it_empty0 + 8 * slot);
       if (it.x < 0) break;
@@ -583,43 +587,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const int T = (it.z - it.y + TK - 1) / TK;
       const int qpos = p.qstart[b] + t;
       float m_ref = -INFINITY, l = 0.f;
-      bool alive = true;
-      for (int j = 0; j < T && alive; ++j) {
+      bool alive = true, dead = false;
+      for (int j = 0; j < T; ++j) {
         const int g = gt + j, sb = g & 1, u = g >> 1;
-        alive = __all_sync(0xffffffffu, ptx::mbar_wait(s_full0 + 8 * sb, u & 1, &abort_flag, p.status));
-        if (!alive) break;
-        ptx::tc_fence_after();
+        if (alive)
+          alive = __all_sync(0xffffffffu, ptx::mbar_wait(s_full0 + 8 * sb, u & 1, &abort_flag, p.status, p.wait_ns));
+        float mx = -INFINITY;
+        if (alive) {
+          ptx::tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < NCOL / 32; ++cc) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(tmem + lane_base + TM_S + sb * TK + coff + cc * 32, v);
-          ptx::tmem_ld_wait();
+          for (int cc = 0; cc < NCOL / 32; ++cc) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(tmem + lane_base + TM_S + sb * TK + coff + cc * 32, v);
+            ptx::tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(v[e]);
-        }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(s_free0 + 8 * sb);
-        // raw tile maximum over this thread's columns (masked keys -> -inf)
-        const int key0 = it.y + j * TK + coff;
-        const bool full = rvalid && key0 + NCOL <= it.z && (p.window <= 0 || qpos - key0 < p.window);
-        float mx;
-        if (full) {
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(v[e]);
+          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(s_free0 + 8 * sb);
+          // raw tile maximum over this thread's columns (masked keys -> -inf)
+          const int key0 = it.y + j * TK + coff;
+          const bool full = rvalid && key0 + NCOL <= it.z && (p.window <= 0 || qpos - key0 < p.window);
+          if (full) {
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int e = 0; e < NCOL; ++e) m4[e & 3] = fmaxf(m4[e & 3], s[e]);
-          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        } else {
-          mx = -INFINITY;
+            for (int e = 0; e < NCOL; ++e) m4[e & 3] = fmaxf(m4[e & 3], s[e]);
+            mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          } else {
 #pragma unroll
-          for (int e = 0; e < NCOL; ++e) {
-            const int key = key0 + e;
-            const bool vis = rvalid && key < it.z && (p.window <= 0 || qpos - key < p.window);
-            s[e] = vis ? s[e] : -INFINITY;
-            mx = fmaxf(mx, s[e]);
+            for (int e = 0; e < NCOL; ++e) {
+              const int key = key0 + e;
+              const bool vis = rvalid && key < it.z && (p.window <= 0 || qpos - key < p.window);
+              s[e] = vis ? s[e] : -INFINITY;
+              mx = fmaxf(mx, s[e]);
+            }
           }
         }
         xch[j & 1][half][rt] = mx;
-        ptx::named_sync(2, n_soft);
+        if (ptx::named_sync_or(2, n_soft, !alive)) {
+          dead = true;
+          break;
+        }
+        do {  // the rest of the tile; a wait that gives up leaves it (break) for the next barrier
         mx = fmaxf(mx, xch[j & 1][half ^ 1][rt]) * p.sl2;  // log2 domain
         float alpha = 1.f;
         bool resc = false;
@@ -652,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         l = l * alpha + ((a01.x + a01.y) + (a23.x + a23.y));
         if (__any_sync(0xffffffffu, resc) && j > 0) {
           // O holds tiles < j once the previous PV is done; scale this thread's columns
-          alive = __all_sync(0xffffffffu, ptx::mbar_wait(pv_done0 + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1, &abort_flag, p.status));
+          alive = __all_sync(0xffffffffu, ptx::mbar_wait(pv_done0 + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1, &abort_flag, p.status, p.wait_ns));
           if (!alive) break;
           ptx::tc_fence_after();
 #pragma unroll 1
@@ -668,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         }
         // P buffer g & 1 is free once the PV of tile g - 2 is done
         if (g >= 2) {
-          alive = __all_sync(0xffffffffu, ptx::mbar_wait(pv_done0 + 8 * sb, ((g - 2) >> 1) & 1, &abort_flag, p.status));
+          alive = __all_sync(0xffffffffu, ptx::mbar_wait(pv_done0 + 8 * sb, ((g - 2) >> 1) & 1, &abort_flag, p.status, p.wait_ns));
           if (!alive) break;
           ptx::tc_fence_after();
         }
@@ -689,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const int nvalid = it.z - (it.y + j * TK);
         if (!PL::CONV && j == T - 1 && nvalid < TK) {
           const int vs = g % PL::V_STAGES, vu = g / PL::V_STAGES;
-          alive = __all_sync(0xffffffffu, ptx::mbar_wait(v_full0 + 8 * vs, vu & 1, &abort_flag, p.status));
+          alive = __all_sync(0xffffffffu, ptx::mbar_wait(v_full0 + 8 * vs, vu & 1, &abort_flag, p.status, p.wait_ns));
           if (!alive) break;
           uint4* vz = reinterpret_cast<uint4*>(smem + PL::OFF_V + vs * PL::TILE_B);
           const int per_half = (TK - nvalid) * 8;  // 16-byte chunks per half (fp8: per tile)
@@ -706,16 +715,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(p_full0 + 8 * sb);
+        } while (false);
       }
-      if (!alive) break;
+      if (dead) break;
       gt += T;
       // ---- epilogue: this thread's 64 columns of O for this item
       xl[half][rt] = l;
-      ptx::named_sync(2, n_soft);
+      if (ptx::named_sync_or(2, n_soft, !alive)) break;
       l += xl[half ^ 1][rt];
       const int gl = gt - 1;
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(pv_done0 + 8 * (gl & 1), (gl >> 1) & 1, &abort_flag, p.status)))
-        break;
+      // a wait that gives up here skips this item's stores; the next item's barrier ends it
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(pv_done0 + 8 * (gl & 1), (gl >> 1) & 1, &abort_flag, p.status, p.wait_ns)))
+        continue;
       ptx::tc_fence_after();
 #pragma unroll
       for (int cc = 0; cc < NCOL / 32; ++cc) {
@@ -956,6 +967,7 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   p.table_len = a.table_len;
   p.sl2 = a.scaling * 1.4426950408889634f * (a.fp8 ? a.k_scale : 1.f);
   p.v_scale = a.fp8 ? a.v_scale : 1.f;
+  p.wait_ns = wait_limit_ns();
   cudaError_t e = cudaSuccess;
   if (!a.sched_ready) {
     LaunchScope ls_(DFLASH_KERNEL_SCHEDULE, s);

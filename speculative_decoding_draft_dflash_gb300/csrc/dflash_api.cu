@@ -7,9 +7,20 @@
 
 #include "attn_sched.cuh"
 
+#include <atomic>
+
 namespace dflash {
 
 __device__ unsigned int g_status_word;
+
+namespace {
+std::atomic<unsigned long long> g_wait_limit_ns{0};  // 0: the default, 2 s
+}  // namespace
+
+unsigned long long wait_limit_ns() {
+  const unsigned long long v = g_wait_limit_ns.load(std::memory_order_relaxed);
+  return v ? v : 2000000000ull;
+}
 
 unsigned* status_word() {
   static std::mutex mu;
@@ -134,14 +145,22 @@ Weights qkv_weights(const dflash_dims* d, const void* W_Q, const void* W_K, cons
 }
 
 // Scratch of each call, carved in a fixed order (base == nullptr only sizes it).
-struct CtxScratch { float* Y; int splits; };
+struct CtxScratch { float* Y; int splits; float* rowpart; int* counters; };
 struct InjectScratch { float* Y; int splits; };
 struct BlockScratch { float* Y; int splits; void* q; float* part_acc; float2* part_ml; void* sched; };
 
-CtxScratch carve_ctx(Carver& cv, const dflash_dims* d, int M) {
+CtxScratch carve_ctx(Carver& cv, const dflash_dims* d, int M, int split_cap = 0) {
   CtxScratch s;
-  s.splits = gemm_splits(d->dtype, M, ctx_weights(d, nullptr), d->k_layers * d->d);
+  const Weights W = ctx_weights(d, nullptr);
+  const int K = d->k_layers * d->d;
+  s.splits = gemm_splits(d->dtype, M, W, K, split_cap);
   s.Y = cv.take<float>((size_t)s.splits * M * d->d);
+  s.rowpart = nullptr;
+  s.counters = nullptr;
+  if (d->dtype == DFLASH_BF16) {  // the fused hidden_norm's per-tile row sums and counters
+    s.rowpart = cv.take<float>((size_t)M * gemm_tc_norm_tiles_n(M, W, K));
+    s.counters = cv.take<int>((size_t)gemm_tc_norm_counters(M, W, K, split_cap));
+  }
   return s;
 }
 
@@ -192,6 +211,10 @@ cudaError_t project_heads(const dflash_dims* d, const Segments& A, int M, const 
 
 using namespace dflash;
 
+DFLASH_API void dflash_test_wait_limit(unsigned long long ns) {
+  g_wait_limit_ns.store(ns, std::memory_order_relaxed);
+}
+
 DFLASH_API const char* dflash_status_string(dflash_status s) {
   switch (s) {
     case DFLASH_OK: return "ok";
@@ -235,10 +258,13 @@ DFLASH_API dflash_status dflash_rope_table_build(double theta, int d_h, int max_
   return cuda_status(rope_table(theta, d_h, max_pos, table, stream));
 }
 
-DFLASH_API dflash_status dflash_ctx_project(const dflash_dims* d, const void* const* hidden, int M,
-                                            const void* W_fc, const void* gamma_h, void* C_out,
-                                            void* workspace, size_t ws_bytes,
-                                            cudaStream_t stream) {
+namespace dflash {
+
+// The context projection with its scratch carved from `workspace`; split_cap > 0 bounds
+// the fc's K-splits (so the scratch need shrinks with it).
+dflash_status ctx_project_impl(const dflash_dims* d, const void* const* hidden, int M,
+                               const void* W_fc, const void* gamma_h, void* C_out, void* workspace,
+                               size_t ws_bytes, int split_cap, cudaStream_t stream) {
   dflash_status st = check_dims(d);
   if (st != DFLASH_OK) return st;
   if (M < 0) return DFLASH_ERR_INVALID_ARG;
@@ -254,14 +280,42 @@ DFLASH_API dflash_status dflash_ctx_project(const dflash_dims* d, const void* co
   if (!aligned16(W_fc) || !aligned16(C_out) || ((uintptr_t)workspace & 255))
     return DFLASH_ERR_INVALID_ARG;
   Carver cv(workspace, ws_bytes);
-  CtxScratch s = carve_ctx(cv, d, M);
+  CtxScratch s = carve_ctx(cv, d, M, split_cap);
   if (!cv.ok) return DFLASH_ERR_WORKSPACE;
   unsigned* status = status_word();
   if (!status) return DFLASH_ERR_CUDA;
-  cudaError_t e = gemm(d->dtype, A, M, ctx_weights(d, W_fc), s.Y, d->d, status, stream);
+  const Weights W = ctx_weights(d, W_fc);
+  const int K = d->k_layers * d->d;
+  if (d->dtype == DFLASH_BF16 && gemm_tc_norm_ok(M, W, K, split_cap))
+    return cuda_status(gemm_tc_norm(A, M, W, s.Y, s.rowpart, s.counters, gamma_h, d->eps, C_out,
+                                    status, stream, split_cap));
+  cudaError_t e = gemm(d->dtype, A, M, W, s.Y, d->d, status, stream, split_cap);
   if (e == cudaSuccess)
     e = rmsnorm_rows(d->dtype, s.Y, s.splits, M, d->d, gamma_h, d->eps, C_out, stream);
   return cuda_status(e);
+}
+
+// Scratch bytes of a context projection of M rows with at most split_cap K-splits (0: the
+// planner's choice), or 0 for dims the library does not support.
+size_t ctx_scratch_bytes(const dflash_dims* d, int M, int split_cap) {
+  if (check_dims(d) != DFLASH_OK || M < 0) return 0;
+  Carver cv(nullptr, ~size_t(0));
+  carve_ctx(cv, d, M, split_cap);
+  return cv.off;
+}
+
+// K-splits the planner gives a context projection of M rows (1 for the f32 path).
+int ctx_splits(const dflash_dims* d, int M) {
+  return gemm_splits(d->dtype, M, ctx_weights(d, nullptr), d->k_layers * d->d);
+}
+
+}  // namespace dflash
+
+DFLASH_API dflash_status dflash_ctx_project(const dflash_dims* d, const void* const* hidden, int M,
+                                            const void* W_fc, const void* gamma_h, void* C_out,
+                                            void* workspace, size_t ws_bytes,
+                                            cudaStream_t stream) {
+  return ctx_project_impl(d, hidden, M, W_fc, gamma_h, C_out, workspace, ws_bytes, 0, stream);
 }
 
 namespace {

@@ -53,6 +53,10 @@ struct Carver {
   }
 };
 
+// Limit of the pipeline waits of tensor-core kernels launched from now on (2 s unless a
+// test lowered it with dflash_test_wait_limit; dflash_api.cu).
+unsigned long long wait_limit_ns();
+
 // per-device sticky status word (defined in dflash_api.cu)
 unsigned* status_word();
 
@@ -86,16 +90,37 @@ struct Weights {
 };
 
 // Number of K-splits the GEMM of this shape uses (partials summed by the epilogue).
-int gemm_splits(int dtype, int M, const Weights& W, int K);
+// split_cap > 0 bounds the K-splits (a caller with a fixed scratch size).
+int gemm_splits(int dtype, int M, const Weights& W, int K, int split_cap = 0);
 
 // Y[split][M][ldY] (fp32) = X W^T. f32: SIMT FFMA; bf16: tcgen05 tensor cores.
 cudaError_t gemm(int dtype, const Segments& A, int M, const Weights& W, float* Y, int ldY,
-                 unsigned* status, cudaStream_t s);
+                 unsigned* status, cudaStream_t s, int split_cap = 0);
 
 // tcgen05 / TMA GEMM (bf16 inputs, fp32 accumulation); gemm_tc.cu
-int gemm_tc_splits(int M, const Weights& W, int K);
+int gemm_tc_splits(int M, const Weights& W, int K, int split_cap = 0);
 cudaError_t gemm_tc(const Segments& A, int M, const Weights& W, float* Y, int ldY,
-                    unsigned* status, cudaStream_t s);
+                    unsigned* status, cudaStream_t s, int split_cap = 0);
+
+// The context projection with hidden_norm fused into its epilogue (bf16): C = RMSNorm of
+// X W^T, from Y (split partials, [splits][M][N] fp32), rowpart ([M][N / BN] fp32) and
+// gemm_tc_norm_counters() ints of scratch (cleared by the call on its stream). Only for
+// shapes whose CTAs are all resident at once (gemm_tc_norm_ok); gemm_tc + rmsnorm_rows
+// otherwise.
+bool gemm_tc_norm_ok(int M, const Weights& W, int K, int split_cap = 0);
+int gemm_tc_norm_counters(int M, const Weights& W, int K, int split_cap = 0);
+int gemm_tc_norm_tiles_n(int M, const Weights& W, int K);  // N / BN: rowpart is [M][this]
+cudaError_t gemm_tc_norm(const Segments& A, int M, const Weights& W, float* Y, float* rowpart,
+                         int* counters, const void* gamma, float eps, void* C, unsigned* status,
+                         cudaStream_t s, int split_cap = 0);
+
+// The context projection on caller scratch (dflash_api.cu); split_cap > 0 bounds its
+// K-splits, and ctx_scratch_bytes gives the scratch that needs.
+dflash_status ctx_project_impl(const dflash_dims* d, const void* const* hidden, int M,
+                               const void* W_fc, const void* gamma_h, void* C_out, void* workspace,
+                               size_t ws_bytes, int split_cap, cudaStream_t stream);
+size_t ctx_scratch_bytes(const dflash_dims* d, int M, int split_cap);
+int ctx_splits(const dflash_dims* d, int M);
 
 // SIMT fp32-accumulating GEMM for any M, N, K (the f32 path).
 cudaError_t gemm_simt(int dtype, const Segments& A, int M, const Weights& W, float* Y, int ldY,

@@ -25,10 +25,15 @@
 // hidden states of the context projection), each with its own tensor map;
 // the weights as up to three matrices stacked along N (W_Q | W_K | W_V).
 //
-// Two epilogues, both leaving the staged tile by bulk copies (cp.async.bulk, one per
+// Three epilogues, leaving the staged tile by bulk copies (cp.async.bulk, one per
 // contiguous destination row), so the store phase costs a few instructions per row:
-//   fp32 store   the tile (a split-K partial) goes to Y; the context
-//                projection's RMSNorm kernel sums the splits;
+//   fp32 store   the tile (a split-K partial) goes to Y; the consumer sums the splits;
+//   norm         the context projection with hidden_norm fused (DFlash KV Injection
+//                Walkthrough, Step 2: C = RMSNorm(fc(raw))): the last split of a tile
+//                adds the others' partials (published in Y), each tile reports its rows'
+//                sums of squares over its columns, and once all tiles of a 128-row block
+//                have reported (all CTAs resident; bounded waits) each scales its own
+//                tile by 1 / rms(row) and gamma and stores C in bf16;
 //   heads        (no split-K) whole 128-dim heads per tile (BN = 128 or 256).
 //                The row's thread applies the per-head RMSNorm (Q and K heads),
 //                rotates the pair (i, i + 64) at the row's absolute position and
@@ -59,6 +64,7 @@ struct TcGemmParams {
   int w_off[4];       // prefix offsets of the stacked weights along N
   int M, ldY;
   int kb_total, kb_per_split, splits;
+  unsigned long long wait_ns;  // limit of the pipeline waits (2 s unless a test lowers it)
   float* Y;           // fp32 store: [split][M][ldY]
   HeadEpilogue ep;    // heads: norm / RoPE / destination
   unsigned* status;
@@ -67,6 +73,19 @@ struct TcGemmParams {
   // (same K), and with sched_cta one more column whose first CTA builds the
   // attention work list while the tiles run.
   int ny0, ny1, sched_cta;
+  // Fused hidden_norm (fp32-store launches of the context projection, norm != 0): the last
+  // split of each tile to finish adds the other splits' partials (published in Y) to its
+  // own, reports its rows' sums of squares over its BN columns, and once every tile of its
+  // 128-row block has reported, scales its tile by 1 / rms(row) and gamma into C (bf16).
+  // The counters start at zero (cleared before the launch); all CTAs are co-resident.
+  int norm;
+  void* C;              // bf16 [M][ldY]
+  const void* gamma;    // bf16 [ldY]
+  float eps;
+  int* tickets;         // [gx * ny] splits of a tile that have finished
+  int* ready;           // [gx * ny] partials of a tile published in Y
+  int* rowcnt;          // [gx] tiles of a 128-row block whose sums of squares are in
+  float* rowpart;       // [M][ny] per-tile sums of squares of each row
   CUtensorMap a1;
   CUtensorMap b1[3];
   int w1_count;
@@ -112,6 +131,28 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsign
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Waits (bounded, like the pipeline waits) until *p >= target, where other CTAs of the same
+// launch raise *p after publishing data (release); false when it gave up.
+__device__ __forceinline__ bool spin_geq(const int* p, int target, unsigned* status,
+                                         uint64_t limit_ns) {
+  if (ld_acquire(p) >= target) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (ld_acquire(p) < target) {
+    if (ptx::globaltimer() - t0 > limit_ns) {
+      atomicOr(status, DFLASH_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(128);
+  }
+  return true;
 }
 
 // Sixteen finished values (dims d0 .. d0 + 15 of one head) into the head's 256-byte slot
@@ -229,6 +270,154 @@ __device__ __forceinline__ HeadEpilogue pick_epilogue(const TcGemmParams& p, boo
   return e;
 }
 
+// Phase 2 of a fused-norm launch, run by all threads of the CTA with the fp32 tile in the
+// staging area (rows BN + 4 floats apart) and gamma of its columns in `gam`. Every thread
+// reaches every barrier below whatever the outcome of a wait (decisions go through s_flag).
+template <int BN, bool PAIR>
+__device__ __forceinline__ void norm_epilogue(const TcGemmParams& p, float* stg, const float* gam,
+                                              int m0, int n0, int M, volatile int* abort_flag,
+                                              volatile int* s_role, volatile int* s_flag) {
+  using C = Cfg<BN, PAIR>;
+  constexpr int kT = gemm_threads(false);
+  constexpr int Q4 = BN / 4;  // float4 groups of a row
+  const int tid = threadIdx.x;
+  const int ny = (int)gridDim.y, splits = (int)gridDim.z, z = (int)blockIdx.z;
+  const int tile = (int)blockIdx.x * ny + (int)blockIdx.y;
+  const int N = p.ldY;
+  // 1) the last split of the tile to get here finishes it; the others publish their partial
+  if (tid == 0) {
+    int last = 1;
+    if (*abort_flag) {
+      last = -1;
+    } else if (splits > 1) {
+      const int t = atomicAdd(&p.tickets[tile], 1);
+      last = t == splits - 1;
+    }
+    *s_role = last;
+  }
+  ptx::named_sync(1, kT);
+  const int role = *s_role;
+  if (role < 0) return;
+  if (role == 0) {
+    float* y = p.Y + (size_t)z * M * N + n0;
+    for (int u = tid; u < BM * Q4; u += kT) {
+      const int r = u / Q4, c = u - r * Q4;
+      if (m0 + r < M)
+        reinterpret_cast<float4*>(y + (size_t)(m0 + r) * N)[c] =
+            *reinterpret_cast<const float4*>(stg + r * C::LD + 4 * c);
+    }
+    __threadfence();
+    ptx::named_sync(1, kT);
+    if (tid == 0) {  // after every thread's stores and fences
+      __threadfence();
+      atomicAdd(&p.ready[tile], 1);
+    }
+    return;
+  }
+  // 2) last split: add the other splits' partials (in L2) to the tile
+  if (splits > 1) {
+    if (tid == 0) *s_flag = spin_geq(&p.ready[tile], splits - 1, p.status, p.wait_ns) ? 1 : 0;
+    ptx::named_sync(1, kT);
+    if (!*s_flag) {
+      if (tid == 0) *abort_flag = 1;
+      return;
+    }
+    // the splits in index order, this CTA's own from shared memory: the sum does not
+    // depend on which split finished last. Each thread keeps U float4 loads of a split in
+    // flight (L2 latency, not bandwidth, bounds this step).
+    constexpr int U = 16;
+    for (int u0 = tid; u0 < BM * Q4; u0 += U * kT) {
+      float4 v[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < splits; ++s) {
+        float4 a[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          const int u = u0 + k * kT, r = u / Q4, c = u - r * Q4;
+          a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (u < BM * Q4 && m0 + r < M)
+            a[k] = s == z ? *reinterpret_cast<const float4*>(stg + r * C::LD + 4 * c)
+                          : __ldcg(reinterpret_cast<const float4*>(
+                                       p.Y + (size_t)s * M * N + n0 + (size_t)(m0 + r) * N) + c);
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          v[k].x += a[k].x;
+          v[k].y += a[k].y;
+          v[k].z += a[k].z;
+          v[k].w += a[k].w;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const int u = u0 + k * kT, r = u / Q4, c = u - r * Q4;
+        if (u < BM * Q4 && m0 + r < M) *reinterpret_cast<float4*>(stg + r * C::LD + 4 * c) = v[k];
+      }
+    }
+    ptx::named_sync(1, kT);
+  }
+  // 3) each row's sum of squares over this tile's columns, then wait for the row block
+  if (tid < BM && m0 + tid < M) {
+    const float4* r4 = reinterpret_cast<const float4*>(stg + tid * C::LD);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 8
+    for (int c = 0; c < Q4; ++c) {
+      const float4 v = r4[c];
+      a0 = fmaf(v.x, v.x, a0);
+      a1 = fmaf(v.y, v.y, a1);
+      a2 = fmaf(v.z, v.z, a2);
+      a3 = fmaf(v.w, v.w, a3);
+    }
+    p.rowpart[(size_t)(m0 + tid) * ny + blockIdx.y] = (a0 + a1) + (a2 + a3);
+  }
+  __threadfence();
+  ptx::named_sync(1, kT);
+  if (tid == 0) {
+    __threadfence();
+    atomicAdd(&p.rowcnt[blockIdx.x], 1);
+    *s_flag = spin_geq(&p.rowcnt[blockIdx.x], ny, p.status, p.wait_ns) ? 1 : 0;
+  }
+  ptx::named_sync(1, kT);
+  if (!*s_flag) {
+    if (tid == 0) *abort_flag = 1;
+    return;
+  }
+  // 4) C = x / sqrt(mean(x^2) + eps) * gamma, in bf16, written over the row's first half
+  if (tid < BM && m0 + tid < M) {
+    const float* pr = p.rowpart + (size_t)(m0 + tid) * ny;
+    float ss = 0.f;
+    for (int j0 = 0; j0 < ny; j0 += 16) {  // 16 loads in flight, summed in a fixed order
+      float t[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) t[j] = j0 + j < ny ? __ldcg(pr + j0 + j) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) ss += t[j];
+    }
+    const float rn = 1.0f / sqrtf(ss / (float)N + p.eps);
+    float* row = stg + tid * C::LD;
+    uint4* out = reinterpret_cast<uint4*>(row);
+#pragma unroll 4
+    for (int c = 0; c < BN / 8; ++c) {  // 8 values in, 16 bytes out, out never ahead of in
+      const float4 v0 = reinterpret_cast<const float4*>(row)[2 * c];
+      const float4 v1 = reinterpret_cast<const float4*>(row)[2 * c + 1];
+      const float* g = gam + 8 * c;
+      uint4 w;
+      w.x = pack_bf16(v0.x * rn * g[0], v0.y * rn * g[1]);
+      w.y = pack_bf16(v0.z * rn * g[2], v0.w * rn * g[3]);
+      w.z = pack_bf16(v1.x * rn * g[4], v1.y * rn * g[5]);
+      w.w = pack_bf16(v1.z * rn * g[6], v1.w * rn * g[7]);
+      out[c] = w;
+    }
+    ptx::fence_proxy_async_smem();
+  }
+  ptx::named_sync(1, kT);
+  bf16* cb = reinterpret_cast<bf16*>(p.C) + n0;
+  for (int r = tid; r < BM && m0 + r < M; r += kT)
+    ptx::bulk_store(cb + (size_t)(m0 + r) * N, ptx::smem_u32(stg + r * C::LD), BN * 2);
+  ptx::bulk_commit_wait_all();
+}
+
 template <int BN, bool HEADS, bool PAIR>
 __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const __grid_constant__ TcGemmParams p) {
   constexpr int kThreads = gemm_threads(HEADS);
@@ -246,6 +435,7 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
   constexpr uint32_t TMEM_COLS = HEADS ? 2 * BN : BN;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ int s_role, s_flag;  // fused norm: decisions of thread 0 broadcast to the CTA
 
   // problem of this CTA (grouped launches); whole CTAs branch, before any barrier
   const int col = (int)blockIdx.y;
@@ -321,7 +511,7 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
       for (int i = 0; i < nkb; ++i) {
         const int s = i % STAGES;
         const uint32_t ph = (i / STAGES) & 1;
-        if (i >= STAGES && !ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, &abort_flag, p.status)) break;
+        if (i >= STAGES && !ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, &abort_flag, p.status, p.wait_ns)) break;
         const int kb = kb0 + i;
         const int seg = kb / kseg_blocks;
         const int kx = (kb - seg * kseg_blocks) * BK;
@@ -354,7 +544,7 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
       for (int i = 0; i < nkb; ++i) {
         const int s = i % STAGES;
         const uint32_t ph = (i / STAGES) & 1;
-        if (!ptx::mbar_wait(full0 + 8 * s, ph, &abort_flag, p.status)) break;
+        if (!ptx::mbar_wait(full0 + 8 * s, ph, &abort_flag, p.status, p.wait_ns)) break;
         ptx::tc_fence_after();
         const uint32_t sa = ptx::smem_u32(smem + (size_t)s * C::STAGE);
         const uint32_t sb = sa + C::A_BYTES;
@@ -388,6 +578,11 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     float* srow = stg + row * C::LD;
     RowSlot rs{0, 0, -1, -1};
+    if (!HEADS && p.norm) {
+      // while the MMAs run: gamma of the tile's columns, as fp32
+      for (int c = threadIdx.x - 64; c < BN; c += 128)
+        gam[c] = __bfloat162float(((const bf16*)p.gamma)[n0 + c]);
+    }
     if (HEADS) {
       // while the MMAs run: the row's destination, gamma, and the row's RoPE pairs
       // (cos, sin of its position, 128 floats) into TMEM columns BN .. BN + 127
@@ -418,7 +613,7 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
       ptx::named_sync(2, 128);  // gamma staged by all four warps
     }
     // warp-uniform: tcgen05.ld below is a .sync.aligned instruction
-    const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(done, 0, &abort_flag, p.status));
+    const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(done, 0, &abort_flag, p.status, p.wait_ns));
     ptx::tc_fence_after();
     if (ok && !HEADS) {
 #pragma unroll 1
@@ -509,7 +704,9 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
   if (warp >= 2) ptx::fence_proxy_async_smem();  // staged rows leave by bulk copy
   // phase 2, all warps: bulk copies from the staging tile
   ptx::named_sync(1, kThreads);
-  if (!abort_flag) {
+  if (!HEADS && p.norm) {
+    norm_epilogue<BN, PAIR>(p, stg, gam, m0, n0, M, &abort_flag, &s_role, &s_flag);
+  } else if (!abort_flag) {
     if (!HEADS) {
       // fp32 partial rows, one contiguous copy each
       float* ybase = p.Y + (size_t)blockIdx.z * M * p.ldY + n0;
@@ -600,7 +797,7 @@ int grid_x(int M, bool pair) {
 
 // The widest of 256/128/64 that divides every stacked weight (heads: 256 or
 // 128, whole heads per tile). Split-K to about one wave on the GPU.
-Plan plan(int M, const Weights& W, int K, bool heads) {
+Plan plan(int M, const Weights& W, int K, bool heads, int split_cap = 0) {
   Plan pl;
   pl.bn = 256;
   for (int i = 0; i < W.count; ++i)
@@ -614,6 +811,7 @@ Plan plan(int M, const Weights& W, int K, bool heads) {
   int splits = 148 / (tiles > 0 ? tiles : 1);
   const int max_splits = pl.kb_total / 4 > 0 ? pl.kb_total / 4 : 1;
   if (splits > max_splits) splits = max_splits;
+  if (split_cap > 0 && splits > split_cap) splits = split_cap;
   if (splits < 1) splits = 1;
   pl.kb_per_split = (pl.kb_total + splits - 1) / splits;
   pl.splits = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
@@ -682,7 +880,9 @@ bool encode_2d_u8(CUtensorMap* m, const void* base, long long rows, int box_rows
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int gemm_tc_splits(int M, const Weights& W, int K) { return plan(M, W, K, false).splits; }
+int gemm_tc_splits(int M, const Weights& W, int K, int split_cap) {
+  return plan(M, W, K, false, split_cap).splits;
+}
 
 bool gemm_tc_heads_ok(int M, const Weights& W, int K) {
   const Plan pl = plan(M, W, K, true);
@@ -711,17 +911,18 @@ cudaError_t fill_common(TcGemmParams& p, const Segments& A, int M, const Weights
   p.kb_total = pl.kb_total;
   p.kb_per_split = pl.kb_per_split;
   p.splits = pl.splits;
+  p.wait_ns = wait_limit_ns();
   return cudaSuccess;
 }
 
 }  // namespace
 
 cudaError_t gemm_tc(const Segments& A, int M, const Weights& W, float* Y, int ldY,
-                    unsigned* status, cudaStream_t s) {
+                    unsigned* status, cudaStream_t s, int split_cap) {
   const int N = W.total();
   if (M <= 0 || N <= 0) return cudaSuccess;
   const int K = A.n * A.kseg;
-  const Plan pl = plan(M, W, K, false);
+  const Plan pl = plan(M, W, K, false, split_cap);
   if (pl.bn < 64 || A.kseg % BK) return cudaErrorInvalidValue;
   TcGemmParams p;
   cudaError_t e = fill_common(p, A, M, W, pl, K);
@@ -735,6 +936,114 @@ cudaError_t gemm_tc(const Segments& A, int M, const Weights& W, float* Y, int ld
     case 128: return launch<128, false>(p, grid, pl.pair, s);
     default: return launch_one<64, false, false>(p, grid, s);
   }
+}
+
+// Can every CTA of a launch of `pl` over N columns be resident at once (so CTAs may wait
+// for one another)? One CTA per SM (the shared memory of a stage ring); pairs also need two
+// SMs of one cluster slot.
+namespace {
+template <int BN, bool PAIR>
+int max_resident_ctas() {
+  const size_t smem = Cfg<BN, PAIR>::SMEM;
+  if (cudaFuncSetAttribute(gemm_tc_kernel<BN, false, PAIR>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return 0;
+  if constexpr (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(gemm_threads(false), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel<BN, false, true>, &cfg) !=
+        cudaSuccess)
+      return 0;
+    return 2 * clusters;
+  } else {
+    int per_sm = 0, dev = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_tc_kernel<BN, false, false>,
+                                                      gemm_threads(false), smem) != cudaSuccess ||
+        cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return 0;
+    return per_sm * sms;
+  }
+}
+
+int resident_ctas(const Plan& pl) {
+  static std::mutex mu;
+  static int cache[128][2][2];  // [device][bn == 256][pair], 0 = not yet asked
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  int& v = cache[dev][pl.bn == 256][pl.pair];
+  if (!v) {
+    if (pl.bn == 256)
+      v = pl.pair ? max_resident_ctas<256, true>() : max_resident_ctas<256, false>();
+    else
+      v = pl.pair ? max_resident_ctas<128, true>() : max_resident_ctas<128, false>();
+    if (!v) v = -1;
+  }
+  return v;
+}
+}  // namespace
+
+// The fused norm measured slower than the separate pass at every shape tried (the wait for
+// the last tile of a row block puts the slowest CTA's reduction on the critical path), so it
+// runs only when DFLASH_FUSED_NORM=1 asks for it.
+bool gemm_tc_norm_ok(int M, const Weights& W, int K, int split_cap) {
+  const Plan pl = plan(M, W, K, false, split_cap);
+  if (pl.bn < 128 || W.count != 1 || K % BK) return false;
+  const char* env = getenv("DFLASH_FUSED_NORM");
+  if (!(env && env[0] == '1')) return false;
+  const long long ctas = (long long)pl.gx * (W.total() / pl.bn) * pl.splits;
+  return ctas <= resident_ctas(pl);
+}
+
+int gemm_tc_norm_counters(int M, const Weights& W, int K, int split_cap) {
+  const Plan pl = plan(M, W, K, false, split_cap);
+  const int ny = pl.bn > 0 ? W.total() / pl.bn : 0;
+  return 2 * pl.gx * ny + pl.gx;
+}
+
+int gemm_tc_norm_tiles_n(int M, const Weights& W, int K) {
+  const Plan pl = plan(M, W, K, false);
+  return pl.bn > 0 ? W.total() / pl.bn : 0;
+}
+
+cudaError_t gemm_tc_norm(const Segments& A, int M, const Weights& W, float* Y, float* rowpart,
+                         int* counters, const void* gamma, float eps, void* C, unsigned* status,
+                         cudaStream_t s, int split_cap) {
+  const int N = W.total();
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  const int K = A.n * A.kseg;
+  const Plan pl = plan(M, W, K, false, split_cap);
+  if (pl.bn < 128 || A.kseg % BK) return cudaErrorInvalidValue;
+  TcGemmParams p;
+  cudaError_t e = fill_common(p, A, M, W, pl, K);
+  if (e != cudaSuccess) return e;
+  const int ny = N / pl.bn;
+  p.ldY = N;
+  p.Y = Y;
+  p.status = status;
+  p.norm = 1;
+  p.C = C;
+  p.gamma = gamma;
+  p.eps = eps;
+  p.tickets = counters;
+  p.ready = counters + pl.gx * ny;
+  p.rowcnt = counters + 2 * pl.gx * ny;
+  p.rowpart = rowpart;
+  e = cudaMemsetAsync(counters, 0, sizeof(int) * (size_t)(2 * pl.gx * ny + pl.gx), s);
+  if (e != cudaSuccess) return e;
+  dim3 grid(pl.gx, ny, pl.splits);
+  return pl.bn == 256 ? launch<256, false>(p, grid, pl.pair, s) : launch<128, false>(p, grid, pl.pair, s);
 }
 
 cudaError_t gemm_tc_heads(const Segments& A, int M, const Weights& W, const HeadEpilogue& ep,

@@ -15,7 +15,7 @@
 namespace dflash {
 namespace {
 
-constexpr size_t kStaticScratchBytes = DFLASH_NOALLOC_SCRATCH_BYTES;  // 16 MiB per device
+constexpr size_t kStaticScratchBytes = DFLASH_NOALLOC_SCRATCH_BYTES;  // 20 MiB per device
 
 // The array's name in host code is only a host-side handle for the symbol; the
 // device address comes from cudaGetSymbolAddress, once per device.
@@ -51,11 +51,20 @@ DFLASH_API dflash_status dflash_ctx_project_noalloc(const dflash_dims* dims,
                                                     const void* const* hidden, int M,
                                                     const void* W_fc, const void* gamma_h,
                                                     void* C_out, cudaStream_t stream) {
+  // The fc splits K over CTAs, each split with its own fp32 partial tile: when the
+  // planner's split count would not fit the array, fewer splits are used (down to one),
+  // so every M whose single-split scratch fits is served: M * d * 4 bytes plus a few
+  // per-row and per-tile words, 1274 rows at d = 4096.
+  if (!dims) return DFLASH_ERR_INVALID_ARG;
+  if (M <= 0 || ctx_scratch_bytes(dims, M, 0) == 0)  // nothing to do, or refused arguments
+    return ctx_project_impl(dims, hidden, M, W_fc, gamma_h, C_out, nullptr, 0, 0, stream);
+  int cap = ctx_splits(dims, M);
+  while (cap > 1 && ctx_scratch_bytes(dims, M, cap) > kStaticScratchBytes) --cap;
+  if (ctx_scratch_bytes(dims, M, cap) > kStaticScratchBytes) return DFLASH_ERR_WORKSPACE;
   dflash_status st = DFLASH_OK;
   void* scratch = static_scratch(&st);
   if (!scratch) return st;
-  // Same kernels as dflash_ctx_project; a call whose scratch need exceeds the
-  // array is refused there with DFLASH_ERR_WORKSPACE before anything launches.
-  return dflash_ctx_project(dims, hidden, M, W_fc, gamma_h, C_out, scratch, kStaticScratchBytes,
-                            stream);
+  // same kernels as dflash_ctx_project, on the fixed array
+  return ctx_project_impl(dims, hidden, M, W_fc, gamma_h, C_out, scratch, kStaticScratchBytes, cap,
+                          stream);
 }

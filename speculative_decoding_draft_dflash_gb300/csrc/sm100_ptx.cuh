@@ -55,15 +55,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Bounded wait on phase `parity` of an mbarrier. Returns false when the CTA
-// was told to stop (abort flag) or when this wait ran out of time, in which
-// case it raises the abort flag and the device status bit.
+// was told to stop (abort flag) or when this wait ran out of time (limit_ns: 2 s
+// unless a test lowers it), in which case it raises the abort flag and the
+// device status bit.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* status) {
+                                          unsigned* status, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       *abort_flag = 1;
       atomicOr(status, DFLASH_DEV_TIMEOUT);
       return false;
@@ -215,6 +216,21 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
 // Named barrier over `count` threads (id 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier that also ORs one predicate over its `count` threads: every participant
+// gets the same answer, so a group can leave a loop together.
+__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // 2^x on the special-function unit (flushes denormals; ex2.approx of -inf is +0).

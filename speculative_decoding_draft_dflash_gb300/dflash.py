@@ -76,6 +76,7 @@ def _load():
         "dflash_trace_start": (c_int, [c_uint, c_int]),
         "dflash_trace_stop": (c_int, [P, P, c_int, P]),
         "dflash_launch_count": (ctypes.c_ulonglong, []),
+        "dflash_test_wait_limit": (None, [ctypes.c_ulonglong]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -440,3 +441,8 @@ def dflash_trace_stop(capacity=1 << 16):
 
 def dflash_launch_count():
     return int(_lib.dflash_launch_count())
+
+
+def dflash_test_wait_limit(ns):
+    """Test aid: limit (ns) of the kernels' pipeline waits for later launches; 0 = 2 s."""
+    _lib.dflash_test_wait_limit(int(ns))

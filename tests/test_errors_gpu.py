@@ -133,3 +133,46 @@ def test_fp8_refused_rows_leave_cache_untouched():
     b = int(np.argmax(L0))
     tail = dev.cache.k[0, b, :, int(L0[b]):]
     assert torch.all(tail == 0)
+
+
+def test_pipeline_wait_that_runs_out_returns_with_status():
+    """A pipeline wait that runs out: with the test aid's limit at 1 ns, the context
+    projection's GEMM (16 rows: single-CTA tiles, nine K-splits) gives up at its first
+    stage wait. Each CTA drains the copies and MMAs it issued, frees its tensor memory and
+    returns; the status word reports DFLASH_DEV_TIMEOUT. With the default limit back, the
+    next calls on the same GPU (the projection again, then a whole round) are correct."""
+    from speculative_decoding_draft_dflash_gb300 import dflash as D
+    import harness
+    from oracle import dflash_oracle as O
+    w = synth.WORKLOADS["qwen3_8b_b1"]
+    dims = D.make_dims(w.d, w.n_h, w.n_kv, w.d_h, w.k, w.bs, w.eps, w.dtype)
+    M = 16
+    counts = np.full(1, M, dtype=np.int64)
+    hid_np = synth.hidden_states(w, 1, counts)
+    hid = [torch.from_numpy(h).to("cuda", torch.bfloat16) for h in hid_np]
+    W_fc = torch.from_numpy(synth.W_fc(w)).to("cuda", torch.bfloat16)
+    g_h = torch.from_numpy(synth.gamma_h(w)).to("cuda", torch.bfloat16)
+    C = torch.empty((M, w.d), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(D.dflash_workspace_bytes(dims, 1, 64, M), dtype=torch.uint8, device="cuda")
+    assert D.dflash_status_get() == 0
+    st = 0
+    try:
+        D.dflash_test_wait_limit(1)
+        for _ in range(3):               # the first stage of some CTA takes more than 1 ns
+            D.dflash_ctx_project(dims, hid, M, W_fc, g_h, C, ws)
+            st |= D.dflash_status_get()
+            if st & D.DEV_TIMEOUT:
+                break
+    finally:
+        D.dflash_test_wait_limit(0)
+    assert st & D.DEV_TIMEOUT
+    C.fill_(float("nan"))
+    D.dflash_ctx_project(dims, hid, M, W_fc, g_h, C, ws)
+    assert D.dflash_status_get() == 0
+    ref = O.ctx_project(hid_np, synth.W_fc(w), synth.gamma_h(w), w.eps)
+    harness.check_close(C.float().cpu().numpy(), ref, w.dtype, "C after a timed-out launch")
+    # a whole draft round (grouped projections, attention, combine) on the same GPU
+    t = _tiny()
+    seqs = list(range(t.batch))
+    dev_res, _ = harness.device_rounds(t, seqs)
+    harness.compare(t, dev_res, harness.oracle_rounds(t, seqs), seqs)

@@ -148,3 +148,39 @@ def test_single_and_paired_projection_tiles(pairs, monkeypatch):
     monkeypatch.setenv("DFLASH_PAIR_GEMM", pairs)
     w = SMALL["small_pairs_bf16"]
     _run(w, list(range(w.batch)))
+
+
+@pytest.mark.parametrize("fused", ["0", "1"])
+@pytest.mark.parametrize("name", ["small_pairs_bf16", "small_gqa_bf16"])
+def test_fused_and_separate_hidden_norm(name, fused, monkeypatch):
+    """hidden_norm in the fc epilogue (DFLASH_FUSED_NORM=1, where the launch fits) and as a
+    separate pass over the split partials (the default): the same C and round results, on
+    CTA pairs with 2 K-splits (320 rows) and on single CTAs with 4 splits (64 rows)."""
+    monkeypatch.setenv("DFLASH_FUSED_NORM", fused)
+    w = SMALL[name]
+    _run(w, list(range(w.batch)))
+
+
+def test_fused_hidden_norm_at_serving_and_prefill_widths(monkeypatch):
+    """The fused norm at full width (d = 4096, k = 5): 512 rows on CTA pairs with 2 K-splits
+    and 1024 rows with one split, against the oracle row by row on a sample of rows."""
+    import torch
+    from oracle import dflash_oracle as O
+    from speculative_decoding_draft_dflash_gb300 import dflash as D
+    monkeypatch.setenv("DFLASH_FUSED_NORM", "1")
+    w = W["qwen3_8b_b1"]
+    dims = D.make_dims(w.d, w.n_h, w.n_kv, w.d_h, w.k, w.bs, w.eps, w.dtype)
+    W_fc_np, g_np = synth.W_fc(w), synth.gamma_h(w)
+    W_fc = torch.from_numpy(W_fc_np).to("cuda", torch.bfloat16)
+    g_h = torch.from_numpy(g_np).to("cuda", torch.bfloat16)
+    for M in (512, 1024):
+        hid_np = synth.hidden_states(w, 3, np.full(1, M, dtype=np.int64))
+        hid = [torch.from_numpy(h).to("cuda", torch.bfloat16) for h in hid_np]
+        C = torch.full((M, w.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(D.dflash_workspace_bytes(dims, 1, 64, M), dtype=torch.uint8,
+                         device="cuda")
+        D.dflash_ctx_project(dims, hid, M, W_fc, g_h, C, ws)
+        assert D.dflash_status_get() == 0
+        rows = np.unique(np.r_[0, 127, 128, M - 1, np.random.default_rng(M).integers(0, M, 12)])
+        ref = O.ctx_project([h[rows] for h in hid_np], W_fc_np, g_np, w.eps)
+        harness.check_close(C.float().cpu().numpy()[rows], ref, w.dtype, f"C rows, M={M}")

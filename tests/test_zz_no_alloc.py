@@ -23,7 +23,13 @@ def _inputs(w, rnd, M, dt):
     return [torch.from_numpy(h).to("cuda", dt) for h in synth.hidden_states(w, rnd, counts)]
 
 
-@pytest.mark.parametrize("name,M", [("walkthrough_f32", 3), ("qwen3_8b_b1", 512)])
+# f32: the walkthrough shape; bf16 at d = 4096: a block-sized call (9 K-splits), 200 rows
+# (4 splits), 384 and 512 rows (2 splits), 1024 rows and 1274 rows (one split; 1274 is the
+# largest that fits the array)
+@pytest.mark.parametrize("name,M", [("walkthrough_f32", 3), ("qwen3_8b_b1", 128),
+                                    ("qwen3_8b_b1", 200), ("qwen3_8b_b1", 384),
+                                    ("qwen3_8b_b1", 512), ("qwen3_8b_b1", 1024),
+                                    ("qwen3_8b_b1", 1274)])
 def test_noalloc_matches_workspace_entry_point(name, M):
     from speculative_decoding_draft_dflash_gb300 import dflash as D
     w = synth.WORKLOADS[name]
@@ -48,7 +54,7 @@ def test_noalloc_refuses_calls_beyond_its_scratch():
     from speculative_decoding_draft_dflash_gb300 import dflash as D
     w = synth.WORKLOADS["qwen3_8b_b1"]
     dims = D.make_dims(w.d, w.n_h, w.n_kv, w.d_h, w.k, w.bs, w.eps, w.dtype)
-    M = 2048                                 # 2048 x 4096 fp32 partials > 16 MiB
+    M = 1280                                 # one split of 1280 x 4096 fp32 + row sums > 20 MiB
     hid = [torch.zeros((M, w.d), dtype=torch.bfloat16, device="cuda") for _ in range(w.k)]
     W_fc = torch.zeros((w.d, w.k * w.d), dtype=torch.bfloat16, device="cuda")
     g_h = torch.ones(w.d, dtype=torch.bfloat16, device="cuda")
