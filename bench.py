@@ -554,6 +554,17 @@ def run_prefill_gemms(args, w, dev, stream, D, pk):
     for name in ("gemm_fc", "gemm_kv"):
         if name in kernels:
             out[name] = {**roofline_for(name, kernels, costs, 0, pk), "avg_us": kernels[name]["avg_us"]}
+    # the rest of the prefill's launches: hidden_norm and (when the K/V projection splits K)
+    # the per-head epilogue and the length update, per launch
+    out["other_kernels_us"] = {k: v["avg_us"] for k, v in kernels.items() if k not in costs}
+    if "gemm_kv" in kernels:
+        # the whole context K/V projection of one layer: its GEMM and, when the GEMM splits K,
+        # the per-head epilogue kernel (norm, RoPE, cache rows) that finishes it
+        us = kernels["gemm_kv"]["avg_us"] + sum(kernels[k]["avg_us"] for k in ("head_epilogue",)
+                                                if k in kernels)
+        tf = costs["gemm_kv"][0] / (us * 1e-6) / 1e12
+        out["kv_projection"] = {"avg_us": us, "achieved": tf, "unit": "TFLOP/s",
+                                "frac": tf / pk["bf16_tflops"], "peak": pk["bf16_tflops"]}
     return out
 
 

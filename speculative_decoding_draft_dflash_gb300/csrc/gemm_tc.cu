@@ -815,6 +815,19 @@ Plan plan(int M, const Weights& W, int K, bool heads, int split_cap = 0) {
   if (splits < 1) splits = 1;
   pl.kb_per_split = (pl.kb_total + splits - 1) / splits;
   pl.splits = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
+  // heads: where 256-wide tiles need split-K (fp32 partials and a separate epilogue kernel)
+  // but 128-wide ones fill most of the GPU in one pass, take the 128-wide ones, whose fused
+  // heads epilogue writes the rows directly (the 1024-row K/V prefill: 33.6 -> 30.3 us for
+  // GEMM + epilogue; DFLASH_HEADS_NARROW=0 keeps the split)
+  const char* narrow = getenv("DFLASH_HEADS_NARROW");
+  if (heads && pl.bn == 256 && pl.splits > 1 && split_cap == 0 && !(narrow && narrow[0] == '0')) {
+    const int tiles128 = pl.gx * (W.total() / 128);
+    if (tiles128 >= 96 && tiles128 <= 148) {
+      pl.bn = 128;
+      pl.kb_per_split = pl.kb_total;
+      pl.splits = 1;
+    }
+  }
   return pl;
 }
 
