@@ -189,6 +189,9 @@ def compare(w, dev_res, ora_res, seqs):
     return report
 
 
+FP8_CODE_STATS = []  # (what, codes compared, codes that differ from the oracle's rounding)
+
+
 def check_fp8_codes(got, y, what, max_frac=1e-2, rel_delta=2e-3):
     """Device E4M3 values ``got`` (codes read back, before the scale) against the oracle's
     unquantised rows ``y`` (already divided by the scale), [..., d_h].
@@ -209,6 +212,7 @@ def check_fp8_codes(got, y, what, max_frac=1e-2, rel_delta=2e-3):
     want = O.e4m3_dequantize(O.e4m3_quantize(y))
     diff = got != want
     frac = float(diff.mean()) if diff.size else 0.0
+    FP8_CODE_STATS.append((what, int(diff.size), int(diff.sum())))
     assert frac <= max_frac, f"{what}: {frac:.2e} of the codes differ from the oracle's rounding"
     if diff.any():
         delta = rel_delta * np.sqrt(np.mean(y * y, axis=-1, keepdims=True))
