@@ -53,8 +53,9 @@ namespace {
 
 constexpr int BM = 128, BK = 64;
 // warps 0-5: TMA, MMA, 4 x TMEM -> shared memory; all six store in the epilogue's second
-// phase (more warps there measured no faster)
-constexpr int gemm_threads(bool) { return 192; }
+// phase (more warps there measured no faster). Heads epilogue: warps 2-9, two per TMEM lane
+// quarter, each computing one of the tile's two heads.
+constexpr int gemm_threads(bool heads) { return heads ? 320 : 192; }
 
 struct TcGemmParams {
   CUtensorMap a[8];   // activation segments [M][kseg], box {64, 128}
@@ -574,6 +575,7 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
     // floats so the float4 stores of a warp spread over all banks. heads: the finished
     // row in its stored form, in the byte tile (rows 2 BN + 16 bytes apart).
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 are this warp's
+    const int eset = (warp - 2) >> 2;  // heads: warps 2-5 are set 0, warps 6-9 set 1
     const int row = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     float* srow = stg + row * C::LD;
@@ -586,13 +588,16 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
     if (HEADS) {
       // while the MMAs run: the row's destination, gamma, and the row's RoPE pairs
       // (cos, sin of its position, 128 floats) into TMEM columns BN .. BN + 127
-      if (m0 + row < M) rs = row_slot(ep, m0 + row, n0 == 0);
-      const int et = threadIdx.x - 64;  // 0 .. 127
-      gam[et] = ep.gamma_q ? __bfloat162float(((const bf16*)ep.gamma_q)[et]) : 1.f;
-      gam[128 + et] = ep.gamma_k ? __bfloat162float(((const bf16*)ep.gamma_k)[et]) : 1.f;
+      // (set 0; set 1 only computes heads)
+      if (eset == 0 && m0 + row < M) rs = row_slot(ep, m0 + row, n0 == 0);
+      const int et = threadIdx.x - 64;  // 0 .. 127 in set 0
+      if (eset == 0) {
+        gam[et] = ep.gamma_q ? __bfloat162float(((const bf16*)ep.gamma_q)[et]) : 1.f;
+        gam[128 + et] = ep.gamma_k ? __bfloat162float(((const bf16*)ep.gamma_k)[et]) : 1.f;
+      }
       const bool ropes = n0 / 128 < ep.n_q + ep.n_kv;  // the tile's first head is a Q or K head
       __syncwarp();  // row_slot's search diverges; tcgen05.st is .sync.aligned
-      if (ropes) {
+      if (ropes && eset == 0) {
         // the table is 8-byte aligned: float2 loads; rows that are not written (no
         // position, e.g. a table too short or empty) stage zeros and read nothing
         const bool has = rs.pos >= 0;
@@ -610,7 +615,7 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
         }
         ptx::tmem_st_wait();
       }
-      ptx::named_sync(2, 128);  // gamma staged by all four warps
+      ptx::named_sync(2, 256);  // gamma and RoPE pairs staged by set 0, for both sets
     }
     // warp-uniform: tcgen05.ld below is a .sync.aligned instruction
     const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(done, 0, &abort_flag, p.status, p.wait_ns));
@@ -632,9 +637,9 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
       // 128 dims, then x / rms * gamma) and rotate_half RoPE on the pairs (i, i + 64);
       // V heads as they are; each head's 256-byte slot of the byte tile gets the values in
       // the form the destination stores (put16)
-      slots[row] = make_int4(rs.b, rs.t, rs.pos, rs.page);
+      if (eset == 0) slots[row] = make_int4(rs.b, rs.t, rs.pos, rs.page);
 #pragma unroll 1
-      for (int hd = 0; hd < NH; ++hd) {
+      for (int hd = eset; hd < NH; hd += 2) {
         const int head = n0 / 128 + hd;
         const int kind = head < ep.n_q ? 0 : (head < ep.n_q + ep.n_kv ? 1 : 2);  // Q, K, V
         const uint32_t hcol = (uint32_t)(hd * 128);
