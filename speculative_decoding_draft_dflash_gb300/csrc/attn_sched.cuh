@@ -34,6 +34,7 @@ struct Params {
   int* splits;              // [pair]: items of the pair (0 = refused sequence)
   int* merge_list;          // pairs whose rows the combine writes (split or refused),
   int* n_merge;             //   and their count
+  int* ready;               // set to 1 once the list is complete (the attention clears it)
   int32_t* qstart;          // [batch]: first position of the block
   int32_t* lens_new;        // [batch]: length after the call
   int batch, n_kv, bs, window, capacity, table_len, max_splits, n_sm;
@@ -186,6 +187,13 @@ inline __device__ void build(const Params& p) {
       p.items[slot] = make_int4(pr, k, k1, n == 1 ? -1 : s);
       k = k1;
     }
+  }
+  // the list is complete: other CTAs of the launch that builds it may read it now (they
+  // only prefetch from it and never wait for this)
+  __syncthreads();
+  if (threadIdx.x == 0 && p.ready) {
+    __threadfence();
+    atomicExch(p.ready, 1);
   }
 }
 

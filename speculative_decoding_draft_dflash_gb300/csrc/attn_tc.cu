@@ -142,6 +142,7 @@ struct AttnTcParams {
   float v_scale;  // fp8: scale of the V codes
   int out_v8;     // out is 32-byte aligned: rows leave in 32-byte stores
   unsigned long long wait_ns;  // limit of the pipeline waits (2 s unless a test lowers it)
+  int* list_ready;  // the work list's "complete" flag: cleared for the next list
 };
 
 __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity, unsigned* status) {
@@ -274,6 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const uint32_t mma_fin = ptx::smem_u32(bars + PL::B_FIN);
 
   if (threadIdx.x == 0) {
+    // the projection launch that may have prefetched from the list has finished
+    if (blockIdx.x == 0 && p.list_ready) *p.list_ready = 0;
     abort_flag = 0;
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(q_full0 + 8 * i, 1);
@@ -904,6 +907,7 @@ sched::Params attn_sched_params(const AttnParams& a) {
   sp.n_items = sp.splits + pairs;
   sp.next_item = sp.n_items + 1;
   sp.n_merge = sp.n_items + 2;
+  sp.ready = sp.n_items + 3;
   sp.qstart = sp.n_items + 16;
   sp.lens_new = sp.qstart + a.batch;
   sp.merge_list = sp.lens_new + a.batch;
@@ -968,6 +972,7 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   p.sl2 = a.scaling * 1.4426950408889634f * (a.fp8 ? a.k_scale : 1.f);
   p.v_scale = a.fp8 ? a.v_scale : 1.f;
   p.wait_ns = wait_limit_ns();
+  p.list_ready = sp.ready;
   cudaError_t e = cudaSuccess;
   if (!a.sched_ready) {
     LaunchScope ls_(DFLASH_KERNEL_SCHEDULE, s);

@@ -271,6 +271,40 @@ __device__ __forceinline__ HeadEpilogue pick_epilogue(const TcGemmParams& p, boo
   return e;
 }
 
+// The attention's first wave takes items 0 .. n_sm - 1 of the work list, one per CTA; this
+// CTA (one of the grouped launch's GEMM CTAs) prefetches the first two K and V tiles of
+// items L, L + nG, ... of that wave into L2, if the list is complete (its builder sets the
+// flag with release order). Items are checked against the cache bounds first.
+__device__ __noinline__ void prefetch_first_wave(const TcGemmParams& p) {
+  const int* ready = p.sp.ready;
+  if (!ready || ld_acquire(ready) != 1) return;
+  const HeadEpilogue& e = p.ep;
+  const int n_items = *p.sp.n_items;
+  const int wave = min(n_items, p.sp.n_sm);
+  const int nG = (int)gridDim.x * (p.ny0 + p.ny1);
+  const int pairs = p.sp.batch * p.sp.n_kv;
+  const int rowbytes = e.kv_fp8 ? 128 : 256;
+  for (int j = (int)blockIdx.y * (int)gridDim.x + (int)blockIdx.x; j < wave; j += nG) {
+    const int4 it = p.sp.items[j];
+    if (it.x < 0 || it.x >= pairs || it.y < 0 || it.z <= it.y || it.z > e.capacity) continue;
+    const int b = it.x / p.sp.n_kv, kvh = it.x - b * p.sp.n_kv;
+    int keys = min(it.z - it.y, 256);
+    long long row;
+    if (e.block_table) {
+      const int page = e.block_table[(size_t)b * e.pages_per_seq + (it.y >> 7)];
+      keys = min(keys, 128 - (it.y & 127));
+      row = ((long long)page * e.n_kv + kvh) * 128 + (it.y & 127);
+    } else {
+      row = ((long long)b * e.n_kv + kvh) * e.capacity + it.y;
+    }
+    const uint32_t bytes = (uint32_t)keys * rowbytes;
+    const char* k = (const char*)e.cache_k + row * rowbytes;
+    const char* v = (const char*)e.cache_v + row * rowbytes;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(k), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(v), "r"(bytes) : "memory");
+  }
+}
+
 // Phase 2 of a fused-norm launch, run by all threads of the CTA with the fp32 tile in the
 // staging area (rows BN + 4 floats apart) and gamma of its columns in `gam`. Every thread
 // reaches every barrier below whatever the outcome of a wait (decisions go through s_flag).
@@ -529,6 +563,10 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
         }
         ++issued;
       }
+      // grouped launch: once its work-list CTA has finished, ask L2 for the first K and V
+      // tiles of some of the attention's first-wave items (the attention's CTAs would
+      // otherwise all request them from HBM at once); never waits for the list
+      if (HEADS && p.sched_cta) prefetch_first_wave(p);
       // no copy of ours may still be landing when the CTA exits: CTA 0 (and a single CTA)
       // waits for its last stages to fill; CTA 1, whose copies count on CTA 0's barriers,
       // waits until the MMAs have released its last stages (they read them, so they landed)
