@@ -162,6 +162,12 @@ __device__ __forceinline__ int tile_row(const AttnTcParams& p, int b, int kvh, i
   return (b * p.n_kv + kvh) * p.capacity + k0;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -612,10 +618,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           const int key0 = it.y + j * TK + coff;
           const bool full = rvalid && key0 + NCOL <= it.z && (p.window <= 0 || qpos - key0 < p.window);
           if (full) {
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            // three-input max: half the instructions of a pairwise chain (the softmax
+            // sub-partitions are bound by instruction issue)
+            float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-            for (int e = 0; e < NCOL; ++e) m4[e & 3] = fmaxf(m4[e & 3], s[e]);
-            mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            for (int e = 4; e < NCOL; e += 8) {
+              m4[0] = fmax3(m4[0], s[e], s[e + 1]);
+              m4[1] = fmax3(m4[1], s[e + 2], s[e + 3]);
+              m4[2] = fmax3(m4[2], s[e + 4], s[e + 5]);
+              m4[3] = fmax3(m4[3], s[e + 6], s[e + 7]);
+            }
+            mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
           } else {
 #pragma unroll
             for (int e = 0; e < NCOL; ++e) {
