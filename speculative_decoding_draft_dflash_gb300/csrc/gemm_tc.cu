@@ -279,10 +279,11 @@ __device__ __noinline__ void prefetch_first_wave(const TcGemmParams& p) {
   const int* ready = p.sp.ready;
   if (!ready || ld_acquire(ready) != 1) return;
   const HeadEpilogue& e = p.ep;
-  const int n_items = *p.sp.n_items;
-  const int wave = min(n_items, p.sp.n_sm);
-  const int nG = (int)gridDim.x * (p.ny0 + p.ny1);
   const int pairs = p.sp.batch * p.sp.n_kv;
+  // (a workspace never written before may hold a stale flag and count: the item index stays
+  // inside the list's capacity, and each item is checked before use)
+  const int wave = min(min(*p.sp.n_items, p.sp.n_sm), pairs * p.sp.max_splits);
+  const int nG = (int)gridDim.x * (p.ny0 + p.ny1);
   const int rowbytes = e.kv_fp8 ? 128 : 256;
   for (int j = (int)blockIdx.y * (int)gridDim.x + (int)blockIdx.x; j < wave; j += nG) {
     const int4 it = p.sp.items[j];
