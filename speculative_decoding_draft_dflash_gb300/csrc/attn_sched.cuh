@@ -5,15 +5,23 @@
 // (DFlash KV Injection Walkthrough, Step 7: the cache grows by the new context
 // rows, then the block follows them). The keys a query of the block sees are
 // [lo, start + bs): the whole prefix, or the last W positions under a sliding
-// window of W (the window reading of the hybrid layers). Each (sequence, KV
-// head) pair's key range is cut into items of about equal tile counts; the
-// items are listed largest first, which the attention CTAs then take in order
-// from an atomic counter.
+// window of W (the window reading of the hybrid layers).
+//
+// A CTA's time is close to a fixed cost per 128-key tile plus a fixed cost per item
+// (the last tile's V load, the output stores, the next item's first S), so the work is
+// split by that cost: the key ranges of all (sequence, KV head) pairs, laid end to end in
+// pair order, each as an item header followed by its tiles, form one cost stream of
+// total W, and CTA c of n takes the tiles whose centres fall in [c W / n, (c + 1) W / n).
+// A range that straddles a boundary becomes several items (split ranges, merged
+// afterwards by the combine kernel). CTAs whose shares hold many short ranges then get
+// fewer tiles, and all finish at about the same time.
 //
 // The same pass records, per sequence, the block start (read by the attention
 // for the window test) and the cache length after the call, which the combine
 // kernel writes back once the attention has finished with the old lengths.
 #pragma once
+
+#include <climits>
 
 #include "dflash_internal.cuh"
 
@@ -21,16 +29,18 @@ namespace dflash {
 namespace sched {
 
 constexpr int kTileKeys = 128;     // keys per attention tile
-constexpr int kItemMinTiles = 4;   // smallest item worth a pipeline ramp
-constexpr int kMaxClass = 64;      // item sizes in tiles are bucketed up to this
+constexpr int kItemMinTiles = 4;   // smallest share of a CTA worth its pipeline ramp
+constexpr int kTileCost = 8;       // cost of a tile in the partition (even: tile centres)
+constexpr int kMaxSm = 256;        // most CTAs a list is built for
 
 struct Params {
   const int32_t* lens;      // [batch] lengths before the call
   const int32_t* pre_rows;  // cu_rows [batch + 1] of rows injected in the same call, or null
   int pre_M;                // row count of that inject
-  int4* items;              // {pair, k_begin, k_end, split (-1 = whole range)}
-  int* n_items;
-  int* next_item;
+  int4* items;              // [n_sm]: each CTA's first item, then [n_sm + i]: item i of the
+                            // list; an item is {pair, k_begin, k_end, split (-1 = whole range)}
+  int* first;               // [n_sm + 1]: CTA c takes list items first[c] .. first[c + 1] - 1
+  int* n_items;             // list length
   int* splits;              // [pair]: items of the pair (0 = refused sequence)
   int* merge_list;          // pairs whose rows the combine writes (split or refused),
   int* n_merge;             //   and their count
@@ -39,7 +49,16 @@ struct Params {
   int32_t* lens_new;        // [batch]: length after the call
   int batch, n_kv, bs, window, capacity, table_len, max_splits, n_sm;
   int align;                // key ranges start on multiples of this (paged cache: a page)
+  int item_cost;            // cost of an item header, in units of kTileCost per tile
 };
+
+// Bytes of the work-list area for `pairs` (sequence, KV head) pairs of `batch` sequences
+// on n_sm CTAs: items (2 n_sm + pairs), first (n_sm + 1), splits, 16 counters, qstart,
+// lens_new, merge_list. The list has at most pairs + n_sm - 1 items (each CTA boundary
+// cuts at most one range).
+inline size_t area_bytes(size_t pairs, size_t batch, size_t n_sm) {
+  return (2 * n_sm + pairs) * 16 + (n_sm + 1) * 4 + pairs * 4 + 64 + batch * 8 + pairs * 4;
+}
 
 // Rows the inject of the same call appended for sequence b: all of its rows when they
 // fit the cache and the RoPE table (the condition under which the inject advances the
@@ -70,123 +89,135 @@ __device__ __forceinline__ Range seq_range(const Params& p, int b) {
   return r;
 }
 
-__device__ __forceinline__ int cta_sum(int v, int* tmp) {
-  v = __reduce_add_sync(0xffffffffu, v);
+// Exclusive prefix sum of v over the CTA's threads in thread order; *total receives the
+// sum. tmp: 32 ints of shared memory.
+__device__ __forceinline__ int cta_scan(int v, int* tmp, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[w] = x;
+  __syncthreads();
+  int base = 0, tot = 0;
+  for (int i = 0; i < nw; ++i) {
+    base += i < w ? tmp[i] : 0;
+    tot += tmp[i];
+  }
+  __syncthreads();
+  *total = tot;
+  return base + x - v;
+}
+
+__device__ __forceinline__ int cta_max(int v, int* tmp) {
+  v = __reduce_max_sync(0xffffffffu, v);
   if ((threadIdx.x & 31) == 0) tmp[threadIdx.x >> 5] = v;
   __syncthreads();
-  int t = 0;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += tmp[i];
+  int m = 0;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = max(m, tmp[i]);
   __syncthreads();
-  return t;
+  return m;
 }
 
-// Three sums at once (tmp: 3 x 32 ints); every thread gets the totals in v.
-__device__ __forceinline__ void cta_sum3(int (&v)[3], int* tmp) {
-  const int w = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
-  for (int i = 0; i < 3; ++i) {
-    const int x = __reduce_add_sync(0xffffffffu, v[i]);
-    if ((threadIdx.x & 31) == 0) tmp[i * 32 + w] = x;
-  }
-  __syncthreads();
-  for (int i = 0; i < 3; ++i) {
-    int t = 0;
-    for (int j = 0; j < nw; ++j) t += tmp[i * 32 + j];
-    v[i] = t;
-  }
-  __syncthreads();
+// Tiles of pair pr's key range (0 for a refused sequence).
+__device__ __forceinline__ int pair_tiles(const Params& p, int pr) {
+  const Range r = seq_range(p, pr / p.n_kv);
+  return r.ok ? (r.end - r.lo + kTileKeys - 1) / kTileKeys : 0;
 }
 
-// Run by every thread of one CTA (blockDim.x a multiple of 32, at least kMaxClass + 1).
+// Run by every thread of one CTA (blockDim.x a multiple of 32, n_sm <= kMaxSm).
 inline __device__ void build(const Params& p) {
-  __shared__ int tmp[96];
-  __shared__ int s_class_base[kMaxClass + 1];
-  __shared__ int s_class_cnt[kMaxClass + 1];
+  __shared__ int tmp[32];
   __shared__ int s_merge;
+  __shared__ int s_first[kMaxSm + 1];
   const int pairs = p.batch * p.n_kv;
-  // total tiles, then the item size (below); at least kItemMinTiles tiles per item and
-  // never more than max_splits items per range
-  int mine = 0;
+  constexpr int A = kTileCost;
+  const int B = p.item_cost;
   for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
     const Range r = seq_range(p, b);
-    if (r.ok) mine += p.n_kv * ((r.end - r.lo + kTileKeys - 1) / kTileKeys);
     p.qstart[b] = r.start;
     p.lens_new[b] = r.ok ? r.end : r.start;
   }
-  const int total_tiles = cta_sum(mine, tmp);
-  // Item size: about F items per SM for F = 2, 3 or 4. Items are taken greedily, largest
-  // first, so the finish is even when the item count fills whole waves of n_sm CTAs; with
-  // equal sequences (one long context, equal windows) a count just past a wave leaves most
-  // SMs idle at the end. Take the smallest F whose count fills its last wave within 5% of
-  // the best of the three.
-  int cand[3], cnt[3] = {0, 0, 0};
-  for (int f = 0; f < 3; ++f)
-    cand[f] = max(kItemMinTiles, (total_tiles + (f + 2) * p.n_sm - 1) / ((f + 2) * p.n_sm));
-  for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
-    const Range r = seq_range(p, b);
-    if (!r.ok) continue;
-    const int t = (r.end - r.lo + kTileKeys - 1) / kTileKeys;
-    for (int f = 0; f < 3; ++f) cnt[f] += p.n_kv * min(p.max_splits, (t + cand[f] - 1) / cand[f]);
+  for (int c = threadIdx.x; c <= p.n_sm; c += blockDim.x) s_first[c] = INT_MAX;
+  if (threadIdx.x == 0) s_merge = 0;
+  // each thread takes a contiguous run of pairs, so prefix sums over threads follow the
+  // stream order; a range of t > 0 tiles costs B + A t
+  const int per = (pairs + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int u0 = min(pairs, (int)threadIdx.x * per), u1 = min(pairs, u0 + per);
+  int mine = 0, longest = 0;
+  for (int u = u0; u < u1; ++u) {
+    const int t = pair_tiles(p, u);
+    mine += t > 0 ? B + A * t : 0;
+    longest = max(longest, t);
   }
-  cta_sum3(cnt, tmp);
-  float fill[3], best = 0.f;
-  for (int f = 0; f < 3; ++f) {
-    const int waves = (cnt[f] + p.n_sm - 1) / p.n_sm;
-    fill[f] = waves > 0 ? (float)cnt[f] / (float)(waves * p.n_sm) : 1.f;
-    best = fmaxf(best, fill[f]);
+  int W;
+  const int cost0 = cta_scan(mine, tmp, &W);
+  const int t_max = cta_max(longest, tmp);
+  // CTAs in use: shares of at least kItemMinTiles tiles, and far enough apart that no range
+  // is cut into more than max_splits items (tile centres spanning (t - 1) A cross at most
+  // ceil((t - 1) A / share) share boundaries); with max_splits = 1 ranges stay whole and
+  // each goes to the CTA whose share holds its middle
+  const bool cut = p.max_splits >= 2;
+  int share = kItemMinTiles * A + B;
+  if (cut && t_max > 1) share = max(share, ((t_max - 1) * A + p.max_splits - 2) / (p.max_splits - 1));
+  const int n_use = W > 0 ? max(1, min(p.n_sm, W / share)) : 0;
+  // CTA c's share starts at cost y(c); owner(z) is the CTA whose share holds cost z
+  auto y = [&](int c) { return (int)((long long)c * W / n_use); };
+  auto owner = [&](int z) { return (int)(((long long)(z + 1) * n_use + W - 1) / W) - 1; };
+  // centre of tile j of a range whose header starts at cost c0; first tile whose centre
+  // is at or past cost z
+  auto centre = [&](int c0, int j) { return c0 + B + A * j + A / 2; };
+  auto first_tile = [&](int c0, int z) { return max(0, (z - c0 - B - A / 2 + A - 1) / A); };
+  int nseg = 0;
+  {
+    int c0 = cost0;
+    for (int u = u0; u < u1; ++u) {
+      const int t = pair_tiles(p, u);
+      if (t > 0) {
+        nseg += cut ? owner(centre(c0, t - 1)) - owner(centre(c0, 0)) + 1 : 1;
+        c0 += B + A * t;
+      }
+    }
   }
-  int item_tiles = cand[2];
-  for (int f = 2; f >= 0; --f)
-    if (fill[f] >= best - 0.05f) item_tiles = cand[f];
-  if (threadIdx.x <= kMaxClass) s_class_cnt[threadIdx.x] = 0;
-  if (threadIdx.x == 0) {
-    *p.next_item = 0;
-    s_merge = 0;
-  }
-  __syncthreads();
-  // A range of t tiles becomes n = ceil(t / item_tiles) items of floor / ceil(t / n) tiles;
-  // count the items of each size
-  for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x) {
-    const Range r = seq_range(p, pr / p.n_kv);
+  int n_list;
+  const int seg0 = cta_scan(nseg, tmp, &n_list);
+  int c0 = cost0, i = seg0;
+  for (int u = u0; u < u1; ++u) {
+    const Range r = seq_range(p, u / p.n_kv);
+    const int t = r.ok ? (r.end - r.lo + kTileKeys - 1) / kTileKeys : 0;
     int n = 0;
-    if (r.ok) {
-      const int t = (r.end - r.lo + kTileKeys - 1) / kTileKeys;
-      n = (t + item_tiles - 1) / item_tiles;
-      if (n > p.max_splits) n = p.max_splits;
-      const int small = t / n, big_cnt = t - small * n;  // big_cnt items of small + 1 tiles
-      if (big_cnt) atomicAdd(&s_class_cnt[min(small + 1, kMaxClass)], big_cnt);
-      if (n - big_cnt) atomicAdd(&s_class_cnt[min(small, kMaxClass)], n - big_cnt);
+    if (t > 0) {
+      const int o0 = cut ? owner(centre(c0, 0)) : owner(c0 + (B + A * t) / 2);
+      const int o1 = cut ? owner(centre(c0, t - 1)) : o0;
+      n = o1 - o0 + 1;
+      for (int o = o0; o <= o1; ++o, ++i) {
+        const int j0 = o == o0 ? 0 : first_tile(c0, y(o));
+        const int j1 = o == o1 ? t : first_tile(c0, y(o + 1));
+        p.items[p.n_sm + i] = make_int4(u, r.lo + j0 * kTileKeys, min(r.end, r.lo + j1 * kTileKeys),
+                                        n == 1 ? -1 : o - o0);
+        atomicMin(&s_first[o], i);
+      }
+      c0 += B + A * t;
     }
-    p.splits[pr] = n;
-    if (n != 1) p.merge_list[atomicAdd(&s_merge, 1)] = pr;  // any order: pairs are independent
+    p.splits[u] = n;
+    if (n != 1) p.merge_list[atomicAdd(&s_merge, 1)] = u;  // any order: pairs are independent
   }
   __syncthreads();
+  // items are in stream order with non-decreasing owners: CTA c starts at the first item
+  // owned by c or a later CTA
   if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int c = kMaxClass; c >= 0; --c) {  // largest items first
-      s_class_base[c] = acc;
-      acc += s_class_cnt[c];
-    }
-    *p.n_items = acc;
+    s_first[p.n_sm] = n_list;
+    for (int c = p.n_sm - 1; c >= 0; --c) s_first[c] = min(s_first[c], s_first[c + 1]);
+    *p.n_items = n_list;
     *p.n_merge = s_merge;
   }
   __syncthreads();
-  if (threadIdx.x <= kMaxClass) s_class_cnt[threadIdx.x] = 0;
-  __syncthreads();
-  for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x) {
-    const int n = p.splits[pr];
-    if (n == 0) continue;
-    const Range r = seq_range(p, pr / p.n_kv);
-    const int t = (r.end - r.lo + kTileKeys - 1) / kTileKeys;
-    const int small = t / n, big_cnt = t - small * n;
-    int k = r.lo;
-    for (int s = 0; s < n; ++s) {
-      const int tiles = small + (s < big_cnt ? 1 : 0);
-      const int c = min(tiles, kMaxClass);
-      const int slot = s_class_base[c] + atomicAdd(&s_class_cnt[c], 1);
-      const int k1 = min(r.end, k + tiles * kTileKeys);
-      p.items[slot] = make_int4(pr, k, k1, n == 1 ? -1 : s);
-      k = k1;
-    }
+  for (int c = threadIdx.x; c <= p.n_sm; c += blockDim.x) {
+    p.first[c] = s_first[c];
+    if (c < p.n_sm)
+      p.items[c] = s_first[c] < s_first[c + 1] ? p.items[p.n_sm + s_first[c]] : make_int4(-1, 0, 0, 0);
   }
   // the list is complete: other CTAs of the launch that builds it may read it now (they
   // only prefetch from it and never wait for this)

@@ -7,14 +7,15 @@
 // DFlash source guide (II), part 1: query head h reads KV head h / G).
 //
 // Three kernels:
-//   attn_schedule_kernel   one CTA: from the cache lengths, cuts every
-//                          (sequence, KV head) key range into work items of
-//                          near-equal 128-key tiles, sized so the GPU gets a
-//                          few items per SM, and lists them longest first;
-//   attn_tc_kernel         persistent, one CTA per SM; CTA i starts with item i,
-//                          later items come from an atomic counter (greedy
-//                          longest-first). A split range leaves its output
-//                          normalised in bf16 with its (max, sum);
+//   attn_schedule_kernel   one CTA: from the cache lengths, lays the key ranges
+//                          of all (sequence, KV head) pairs end to end as one
+//                          stream of 128-key tiles, each range led by a cost
+//                          for its item, and gives every SM an equal share of
+//                          that cost, a range cut where a share ends;
+//   attn_tc_kernel         persistent, one CTA per SM, each working through
+//                          the items of its share in order. A split range
+//                          leaves its output normalised in bf16 with its
+//                          (max, sum);
 //   attn_combine_kernel    merges the partial results of split ranges.
 //
 // attn_tc_kernel roles (warp: job):
@@ -133,9 +134,9 @@ struct AttnTcParams {
   bf16* out;
   float* part_acc;       // [pair][max_splits][R][128] bf16: a split's normalised output
   float2* part_ml;       // [pair][max_splits][R]
-  const int4* items;     // {pair, k_begin, k_end, split (-1 = whole range)}
-  const int* n_items;
-  int* next_item;
+  const int4* items;     // [grid] first item of each CTA, then the list:
+                         // {pair, k_begin, k_end, split (-1 = whole range)}
+  const int* first;      // [grid + 1]: CTA c takes list items first[c] .. first[c + 1] - 1
   unsigned* status;
   int batch, n_h, n_kv, bs, G, R, capacity, window, table_len, max_splits;
   float sl2;      // scaling * log2(e) (fp8: times k_scale)
@@ -331,22 +332,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       ptx::prefetch_tmap(&p.k);
       ptx::prefetch_tmap(&p.v);
       const uint64_t pol = ptx::policy_evict_first();
-      const int n_items = *p.n_items;
       int gk = 0, n = 0, nq_loads = 0;
-      // the first wave takes items 0 .. grid - 1 in CTA order (the list's largest, which
-      // the counter would hand out first anyway) without a round trip to the counter
-      int idx = blockIdx.x;
+      // this CTA's items: the first one has a slot of its own, so that reading it does not
+      // wait for the list bounds; the others follow in the list, each read one item ahead
+      const int4* list = p.items + gridDim.x;
+      const int f0 = p.first[blockIdx.x], f1 = p.first[blockIdx.x + 1];
+      int4 it_next = p.items[blockIdx.x];
       bool stop = false;
       for (;; ++n) {
         const int slot = n % kRing;
         if (n >= kRing &&
             !ptx::mbar_wait(it_empty0 + 8 * slot, ((n / kRing) - 1) & 1, &abort_flag, p.status, p.wait_ns))
           break;
-        const int4 it = idx < n_items ? p.items[idx] : make_int4(-1, 0, 0, 0);
+        const int4 it = it_next;
         ring[slot] = it;
         ptx::mbar_arrive(it_full0 + 8 * slot);  // release: the ring entry is visible to waiters
         if (it.x < 0) break;
-        idx = gridDim.x + atomicAdd(p.next_item, 1);  // prefetch the next item's index
+        it_next = f0 + n + 1 < f1 ? list[f0 + n + 1] : make_int4(-1, 0, 0, 0);
         const int b = it.x / p.n_kv, kvh = it.x - b * p.n_kv;
         const int qb = n & 1;
         if (n >= 2 && !ptx::mbar_wait(q_empty0 + 8 * qb, ((n >> 1) - 1) & 1, &abort_flag, p.status, p.wait_ns))
@@ -907,20 +909,29 @@ bool encode_2d_u8(CUtensorMap* m, const void* base, long long rows, int box_rows
 
 int attn_tc_chunk() { return TK * sched::kItemMinTiles; }
 
-// Work-list buffers inside AttnParams::sched: items [pairs][n_chunks] int4, splits
-// [pairs], 16 counters, qstart [batch], lens_new [batch], merge_list [pairs].
+// CTAs of the attention grid: one per SM (a work list covers at most sched::kMaxSm)
+int attn_ctas() { return sm_count() < sched::kMaxSm ? sm_count() : sched::kMaxSm; }
+
+size_t attn_sched_bytes(int batch, int n_kv) {
+  return sched::area_bytes((size_t)batch * n_kv, (size_t)batch, (size_t)attn_ctas());
+}
+
+// Work-list buffers inside AttnParams::sched (sched::area_bytes): items [2 n_sm + pairs]
+// int4, first [n_sm + 1], splits [pairs], 16 counters, qstart [batch], lens_new [batch],
+// merge_list [pairs].
 sched::Params attn_sched_params(const AttnParams& a) {
   const int pairs = a.batch * a.n_kv;
+  const int n_sm = attn_ctas();
   sched::Params sp;
   sp.lens = a.lens;
   sp.pre_rows = a.pre_rows;
   sp.pre_M = a.pre_M;
   sp.items = (int4*)a.sched;
-  sp.splits = (int*)(sp.items + (size_t)pairs * a.n_chunks);
+  sp.first = (int*)(sp.items + 2 * (size_t)n_sm + pairs);
+  sp.splits = sp.first + n_sm + 1;
   sp.n_items = sp.splits + pairs;
-  sp.next_item = sp.n_items + 1;
-  sp.n_merge = sp.n_items + 2;
-  sp.ready = sp.n_items + 3;
+  sp.n_merge = sp.n_items + 1;
+  sp.ready = sp.n_items + 2;
   sp.qstart = sp.n_items + 16;
   sp.lens_new = sp.qstart + a.batch;
   sp.merge_list = sp.lens_new + a.batch;
@@ -931,8 +942,12 @@ sched::Params attn_sched_params(const AttnParams& a) {
   sp.capacity = a.capacity;
   sp.table_len = a.table_len;
   sp.max_splits = a.n_chunks;  // ranges are cut into at most this many items
-  sp.n_sm = sm_count();
+  sp.n_sm = n_sm;
   sp.align = a.block_table ? TK : 1;
+  // an item costs about 1.8 tiles of a CTA's time on a bf16 cache and 1.6 on E4M3 codes
+  // (per-CTA timelines at the serving shape: the last tile's V load, the output stores,
+  // the next item's first S)
+  sp.item_cost = a.fp8 ? 13 : 14;
   return sp;
 }
 
@@ -970,8 +985,7 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   p.part_acc = a.part_acc;
   p.part_ml = a.part_ml;
   p.items = sp.items;
-  p.n_items = sp.n_items;
-  p.next_item = sp.next_item;
+  p.first = sp.first;
   p.status = a.status;
   p.batch = a.batch;
   p.n_h = a.n_h;
@@ -993,8 +1007,7 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;
-  const int max_items = pairs * p.max_splits;
-  const int grid = sp.n_sm < max_items ? sp.n_sm : max_items;
+  const int grid = sp.n_sm;  // the work list gives every SM a share (empty ones exit)
   if (a.fp8)
     e = narrow ? launch_attn<true, true>(p, grid, s) : launch_attn<false, true>(p, grid, s);
   else

@@ -188,10 +188,10 @@ BlockScratch carve_block(Carver& cv, const dflash_dims* d, int batch, int capaci
   const size_t part_rows = (size_t)batch * d->n_h * n_chunks * d->block_size;
   s.part_acc = cv.take<float>(part_rows * d->d_h);
   s.part_ml = cv.take<float2>(part_rows);
-  // work items {pair, k_begin, k_end, split}, split count per pair, counters, per
-  // sequence the block start and the length after the call, the pairs to combine
-  const size_t pairs = (size_t)batch * d->n_kv;
-  s.sched = cv.take<char>(pairs * n_chunks * 16 + pairs * 8 + 64 + (size_t)batch * 8);
+  // the attention's work list: items {pair, k_begin, k_end, split}, each CTA's range of
+  // them, split count per pair, counters, per sequence the block start and the length
+  // after the call, the pairs to combine
+  s.sched = cv.take<char>(attn_sched_bytes(batch, d->n_kv));
   return s;
 }
 

@@ -289,6 +289,8 @@ cudaError_t attn_simt(int dtype, const AttnParams& p, cudaStream_t s);
 
 // tcgen05 attention (bf16, d_h = 128); attn_tc.cu
 int attn_tc_chunk();
+// Bytes of the attention work-list area for `batch` sequences of n_kv KV heads.
+size_t attn_sched_bytes(int batch, int n_kv);
 cudaError_t attn_tc(const AttnParams& p, cudaStream_t s);
 
 // Keys per attention chunk and the attention launch for a dtype.

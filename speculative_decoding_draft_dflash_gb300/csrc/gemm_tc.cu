@@ -271,18 +271,18 @@ __device__ __forceinline__ HeadEpilogue pick_epilogue(const TcGemmParams& p, boo
   return e;
 }
 
-// The attention's first wave takes items 0 .. n_sm - 1 of the work list, one per CTA; this
-// CTA (one of the grouped launch's GEMM CTAs) prefetches the first two K and V tiles of
-// items L, L + nG, ... of that wave into L2, if the list is complete (its builder sets the
-// flag with release order). Items are checked against the cache bounds first.
+// Attention CTA c starts with the work list's item c (each CTA's first item has a slot of
+// its own); this CTA (one of the grouped launch's GEMM CTAs) prefetches the first two K and
+// V tiles of items L, L + nG, ... of those into L2, if the list is complete (its builder
+// sets the flag with release order). Items are checked against the cache bounds first.
 __device__ __noinline__ void prefetch_first_wave(const TcGemmParams& p) {
   const int* ready = p.sp.ready;
   if (!ready || ld_acquire(ready) != 1) return;
   const HeadEpilogue& e = p.ep;
   const int pairs = p.sp.batch * p.sp.n_kv;
-  // (a workspace never written before may hold a stale flag and count: the item index stays
-  // inside the list's capacity, and each item is checked before use)
-  const int wave = min(min(*p.sp.n_items, p.sp.n_sm), pairs * p.sp.max_splits);
+  // the first item of each attention CTA (a workspace never written before may hold a stale
+  // flag: each item is checked before use)
+  const int wave = p.sp.n_sm;
   const int nG = (int)gridDim.x * (p.ny0 + p.ny1);
   const int rowbytes = e.kv_fp8 ? 128 : 256;
   for (int j = (int)blockIdx.y * (int)gridDim.x + (int)blockIdx.x; j < wave; j += nG) {
