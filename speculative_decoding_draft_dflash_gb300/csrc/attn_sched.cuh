@@ -32,18 +32,20 @@ constexpr int kTileKeys = 128;     // keys per attention tile
 constexpr int kItemMinTiles = 4;   // smallest share of a CTA worth its pipeline ramp
 constexpr int kTileCost = 8;       // cost of a tile in the partition (even: tile centres)
 constexpr int kMaxSm = 256;        // most CTAs a list is built for
+constexpr int kMergeCountShift = 20;  // merge_list entry: pair | item count << this
 
 struct Params {
   const int32_t* lens;      // [batch] lengths before the call
   const int32_t* pre_rows;  // cu_rows [batch + 1] of rows injected in the same call, or null
   int pre_M;                // row count of that inject
-  int4* items;              // [n_sm]: each CTA's first item, then [n_sm + i]: item i of the
-                            // list; an item is {pair, k_begin, k_end, split (-1 = whole range)}
+  int4* items;              // [n_sm]: the item each CTA takes first (the last of its share),
+                            // then [n_sm + i]: item i of the list; an item is
+                            // {pair, k_begin, k_end, split (-1 = whole range)}
   int* first;               // [n_sm + 1]: CTA c takes list items first[c] .. first[c + 1] - 1
   int* n_items;             // list length
   int* splits;              // [pair]: items of the pair (0 = refused sequence)
-  int* merge_list;          // pairs whose rows the combine writes (split or refused),
-  int* n_merge;             //   and their count
+  int* merge_list;          // pairs whose rows the combine writes (split or refused), each
+  int* n_merge;             //   with its item count (pair | n << kMergeCountShift); how many
   int* ready;               // set to 1 once the list is complete (the attention clears it)
   int32_t* qstart;          // [batch]: first position of the block
   int32_t* lens_new;        // [batch]: length after the call
@@ -202,7 +204,8 @@ inline __device__ void build(const Params& p) {
       c0 += B + A * t;
     }
     p.splits[u] = n;
-    if (n != 1) p.merge_list[atomicAdd(&s_merge, 1)] = u;  // any order: pairs are independent
+    if (n != 1)  // any order: pairs are independent
+      p.merge_list[atomicAdd(&s_merge, 1)] = u | (n << kMergeCountShift);
   }
   __syncthreads();
   // items are in stream order with non-decreasing owners: CTA c starts at the first item
@@ -217,7 +220,7 @@ inline __device__ void build(const Params& p) {
   for (int c = threadIdx.x; c <= p.n_sm; c += blockDim.x) {
     p.first[c] = s_first[c];
     if (c < p.n_sm)
-      p.items[c] = s_first[c] < s_first[c + 1] ? p.items[p.n_sm + s_first[c]] : make_int4(-1, 0, 0, 0);
+      p.items[c] = s_first[c] < s_first[c + 1] ? p.items[p.n_sm + s_first[c + 1] - 1] : make_int4(-1, 0, 0, 0);
   }
   // the list is complete: other CTAs of the launch that builds it may read it now (they
   // only prefetch from it and never wait for this)

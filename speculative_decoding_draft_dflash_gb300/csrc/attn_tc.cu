@@ -134,8 +134,8 @@ struct AttnTcParams {
   bf16* out;
   float* part_acc;       // [pair][max_splits][R][128] bf16: a split's normalised output
   float2* part_ml;       // [pair][max_splits][R]
-  const int4* items;     // [grid] first item of each CTA, then the list:
-                         // {pair, k_begin, k_end, split (-1 = whole range)}
+  const int4* items;     // [grid] first item of each CTA (the last of its share), then
+                         // the list: {pair, k_begin, k_end, split (-1 = whole range)}
   const int* first;      // [grid + 1]: CTA c takes list items first[c] .. first[c + 1] - 1
   unsigned* status;
   int batch, n_h, n_kv, bs, G, R, capacity, window, table_len, max_splits;
@@ -333,8 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       ptx::prefetch_tmap(&p.v);
       const uint64_t pol = ptx::policy_evict_first();
       int gk = 0, n = 0, nq_loads = 0;
-      // this CTA's items: the first one has a slot of its own, so that reading it does not
-      // wait for the list bounds; the others follow in the list, each read one item ahead
+      // this CTA's items f0 .. f1 - 1 of the list, the last one first (the two ends of a
+      // share are the ranges cut at its boundaries; taking both early leaves the whole
+      // ranges, which need no merge, for the end). The first item has a slot of its own,
+      // so that reading it does not wait for the list bounds; the others are read one
+      // item ahead.
       const int4* list = p.items + gridDim.x;
       const int f0 = p.first[blockIdx.x], f1 = p.first[blockIdx.x + 1];
       int4 it_next = p.items[blockIdx.x];
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         ring[slot] = it;
         ptx::mbar_arrive(it_full0 + 8 * slot);  // release: the ring entry is visible to waiters
         if (it.x < 0) break;
-        it_next = f0 + n + 1 < f1 ? list[f0 + n + 1] : make_int4(-1, 0, 0, 0);
+        it_next = f0 + n + 1 < f1 ? list[f0 + n] : make_int4(-1, 0, 0, 0);
         const int b = it.x / p.n_kv, kvh = it.x - b * p.n_kv;
         const int qb = n & 1;
         if (n >= 2 && !ptx::mbar_wait(q_empty0 + 8 * qb, ((n >> 1) - 1) & 1, &abort_flag, p.status, p.wait_ns))
@@ -805,17 +808,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 // ---------------------------------------------------------------------------
 // One query row of a marked pair: log-sum-exp merge of its split partials, or zeros
 // for a refused sequence.
-__device__ __forceinline__ void combine_row(const AttnTcParams& p, const int* splits, int pr,
-                                            int r, int lane) {
-  const int n = splits[pr];
+__device__ __forceinline__ void combine_row(const AttnTcParams& p, int n, int pr, int r, int lane) {
   const int b = pr / p.n_kv, kvh = pr - b * p.n_kv;
   const int gq = r / p.bs, t = r - gq * p.bs;
   bf16* orow = p.out + ((size_t)(b * p.bs + t) * p.n_h + kvh * p.G + gq) * 128;
   float o[4] = {0.f, 0.f, 0.f, 0.f};
   if (n > 1) {
     // each split holds its normalised output (bf16) and (max, sum): the row is
-    // sum_c w_c out_c / sum_c w_c with w_c = 2^(max_c - M) sum_c. Lane-strided (max, sum)
-    // reductions; the rows of the first kPre splits are requested before them.
+    // sum_c w_c out_c / sum_c w_c with w_c = 2^(max_c - M) sum_c. Lane c loads split c's
+    // (max, sum) once (further splits in lane-strided passes) and hands its weight to the
+    // others by shuffle; the rows of the first kPre splits are requested before all that.
     constexpr int kPre = 4;
     const size_t base = (size_t)pr * p.max_splits * p.R + r;
     const uint2* acc = reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(p.part_acc) + base * 128) + lane;
@@ -823,18 +825,24 @@ __device__ __forceinline__ void combine_row(const AttnTcParams& p, const int* sp
     uint2 pre[kPre];
 #pragma unroll
     for (int c = 0; c < kPre; ++c) pre[c] = c < n ? acc[c * acc_stride] : make_uint2(0u, 0u);
-    float M = -INFINITY;
-    for (int c = lane; c < n; c += 32) M = fmaxf(M, p.part_ml[base + (size_t)c * p.R].x);
+    const float2 ml0 = lane < n ? p.part_ml[base + (size_t)lane * p.R] : make_float2(-INFINITY, 0.f);
+    float M = ml0.x;
+    for (int c = lane + 32; c < n; c += 32) M = fmaxf(M, p.part_ml[base + (size_t)c * p.R].x);
     M = warp_max(M);
-    float L = 0.f;
-    for (int c = lane; c < n; c += 32) {
+    const float w0 = ml0.y > 0.f ? ptx::ex2(ml0.x - M) * ml0.y : 0.f;
+    float L = w0;
+    for (int c = lane + 32; c < n; c += 32) {
       const float2 ml = p.part_ml[base + (size_t)c * p.R];
       if (ml.y > 0.f) L += ptx::ex2(ml.x - M) * ml.y;
     }
     L = warp_sum(L);
-    auto add = [&](int c, const uint2& x) {
+    // weight of split c (c is the same in every lane)
+    auto weight = [&](int c) -> float {
+      if (c < 32) return __shfl_sync(0xffffffffu, w0, c);
       const float2 ml = p.part_ml[base + (size_t)c * p.R];
-      const float w = ml.y > 0.f ? ptx::ex2(ml.x - M) * ml.y : 0.f;
+      return ml.y > 0.f ? ptx::ex2(ml.x - M) * ml.y : 0.f;
+    };
+    auto add = [&](float w, const uint2& x) {
       const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
       const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
       o[0] += w * v01.x;
@@ -843,10 +851,12 @@ __device__ __forceinline__ void combine_row(const AttnTcParams& p, const int* sp
       o[3] += w * v23.y;
     };
 #pragma unroll
-    for (int c = 0; c < kPre; ++c)
-      if (c < n) add(c, pre[c]);
+    for (int c = 0; c < kPre; ++c) {
+      const float w = weight(c);
+      if (c < n) add(w, pre[c]);
+    }
 #pragma unroll 4
-    for (int c = kPre; c < n; ++c) add(c, acc[c * acc_stride]);
+    for (int c = kPre; c < n; ++c) add(weight(c), acc[c * acc_stride]);
     const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[e] *= inv;
@@ -860,17 +870,18 @@ __device__ __forceinline__ void combine_row(const AttnTcParams& p, const int* sp
 
 // Persistent grid; each warp takes (pair, query row) units of the pairs the work list
 // marked (split across items, or refused). Rows of whole-range items were written by
-// the attention kernel.
-__global__ void attn_combine_kernel(AttnTcParams p, const int* splits, const int* merge_list,
-                                    const int* n_merge) {
+// the attention kernel. A marked pair's entry carries its item count.
+__global__ void attn_combine_kernel(AttnTcParams p, const int* merge_list, const int* n_merge) {
   // the attention has read the old lengths: publish the lengths after the call
   if (blockIdx.x == 0 && p.lens)
     for (int b = threadIdx.x; b < p.batch; b += blockDim.x) p.lens[b] = p.lens_new[b];
   const int lane = threadIdx.x & 31;
   const int units = *n_merge * p.R;
   const int warps = gridDim.x * (blockDim.x >> 5);
-  for (int u = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units; u += warps)
-    combine_row(p, splits, merge_list[u / p.R], u % p.R, lane);
+  for (int u = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units; u += warps) {
+    const int e = merge_list[u / p.R];
+    combine_row(p, e >> sched::kMergeCountShift, e & ((1 << sched::kMergeCountShift) - 1), u % p.R, lane);
+  }
 }
 
 int sm_count() {
@@ -954,6 +965,10 @@ sched::Params attn_sched_params(const AttnParams& a) {
 cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   if (a.batch <= 0) return cudaSuccess;
   if (a.d_h != 128) return cudaErrorInvalidValue;
+  // a merge-list entry packs the pair and its item count into one int
+  if ((long long)a.batch * a.n_kv >= (1 << sched::kMergeCountShift) ||
+      a.n_chunks >= (1 << (31 - sched::kMergeCountShift)))
+    return cudaErrorInvalidValue;
   AttnTcParams p;
   memset(&p, 0, sizeof(p));
   const int R = (a.n_h / a.n_kv) * a.bs;
@@ -1018,7 +1033,7 @@ cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   int cgrid = (rows + 7) / 8;
   if (cgrid > 4 * sp.n_sm) cgrid = 4 * sp.n_sm;
   LaunchScope ls_(DFLASH_KERNEL_COMBINE, s);
-  attn_combine_kernel<<<cgrid, 256, 0, s>>>(p, (const int*)sp.splits, sp.merge_list, sp.n_merge);
+  attn_combine_kernel<<<cgrid, 256, 0, s>>>(p, sp.merge_list, sp.n_merge);
   return cudaGetLastError();
 }
 
