@@ -500,18 +500,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           const uint32_t va = PL::CONV ? sbase + PL::OFF_C + vs * TILE
                                        : sbase + PL::OFF_V + vs * PL::TILE_B;
           const uint32_t pa = tmem + TM_P + (g & 1) * 64;
+          // Keys past the range end in the last tile (their P is 0): the MMA stops after the
+          // last K-step that holds a key, and that step's rows past the end are zeroed
+          // first (slots past the cache length may hold anything, and 0 * NaN would poison
+          // O). The f16 conversion of a CONV tile already wrote those rows as zeros.
+          constexpr int KS = PL::P_CODES ? 32 : 16;  // keys per K-step
+          int key_end = TK;
+          if (!PL::CONV && j == T - 1) {
+            const int nvalid = it.z - (it.y + j * TK);
+            if (nvalid < TK) {
+              key_end = (nvalid + KS - 1) / KS * KS;
+              uint4* vz = reinterpret_cast<uint4*>(smem + PL::OFF_V + vs * PL::TILE_B);
+              for (int h = 0; h < (FP8 ? 1 : 2); ++h)  // bf16: two 64-column halves
+                for (int c = nvalid * 8; c < key_end * 8; ++c) vz[h * (HALF / 16) + c] = make_uint4(0u, 0u, 0u, 0u);
+              ptx::fence_proxy_async_smem();
+            }
+          }
           if (PL::P_CODES) {
             // O += Pcodes V + Premainder V: P columns 0-31 and 32-63, 32 keys per K-step
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_f8_ts(tmem + TM_O, pa + (kk >> 2) * 32 + (kk & 3) * 8,
-                        ptx::smem_desc_sw128_mn(va + (kk & 3) * 4096, PL::TILE_B), idesc_pv,
-                        (j > 0 || kk > 0) ? 1u : 0u);
+              if ((kk & 3) * KS < key_end)
+                mma_f8_ts(tmem + TM_O, pa + (kk >> 2) * 32 + (kk & 3) * 8,
+                          ptx::smem_desc_sw128_mn(va + (kk & 3) * 4096, PL::TILE_B), idesc_pv,
+                          (j > 0 || kk > 0) ? 1u : 0u);
           } else {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_bf16_ts(tmem + TM_O, pa + kk * 8, ptx::smem_desc_sw128_mn(va + kk * 2048, HALF),
-                          idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+              if (kk * KS < key_end)
+                mma_bf16_ts(tmem + TM_O, pa + kk * 8, ptx::smem_desc_sw128_mn(va + kk * 2048, HALF),
+                            idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
           }
           ptx::mma_commit((PL::CONV ? c_empty0 : v_empty0) + 8 * vs);
           ptx::mma_commit(pv_done0 + 8 * (g & 1));
@@ -714,26 +732,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           ptx::tmem_st_32x32b_x32(tmem + lane_base + TM_P + sb * 64 + half * 32, pk);
         }
         ptx::tmem_st_wait();
-        // keys past the range end in the last tile: zero their V rows (slots past the
-        // cache length may hold anything, and 0 * NaN would poison O)
-        const int nvalid = it.z - (it.y + j * TK);
-        if (!PL::CONV && j == T - 1 && nvalid < TK) {
-          const int vs = g % PL::V_STAGES, vu = g / PL::V_STAGES;
-          alive = __all_sync(0xffffffffu, ptx::mbar_wait(v_full0 + 8 * vs, vu & 1, &abort_flag, p.status, p.wait_ns));
-          if (!alive) break;
-          uint4* vz = reinterpret_cast<uint4*>(smem + PL::OFF_V + vs * PL::TILE_B);
-          const int per_half = (TK - nvalid) * 8;  // 16-byte chunks per half (fp8: per tile)
-          const int me = half * 32 * nq + rt;
-          if (FP8) {
-            for (int idx = me; idx < per_half; idx += n_soft) vz[nvalid * 8 + idx] = make_uint4(0, 0, 0, 0);
-          } else {
-            for (int idx = me; idx < 2 * per_half; idx += n_soft) {
-              const int h = idx / per_half, rem = idx - h * per_half;
-              vz[(h * HALF) / 16 + nvalid * 8 + rem] = make_uint4(0, 0, 0, 0);
-            }
-          }
-          ptx::fence_proxy_async_smem();
-        }
         ptx::tc_fence_before();
         ptx::mbar_arrive(p_full0 + 8 * sb);
         } while (false);
