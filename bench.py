@@ -159,13 +159,14 @@ def mean_attention_bytes(w, starts):
 TRAFFIC_RUN = None  # workload / cache element type / layout of this run
 
 
-def measured_traffic(kernel):
+def measured_traffic(kernel, run=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this run's
-    workload, cache element type and layout, and the kernel source is unchanged."""
+    workload, cache element type and layout (or on `run`), and the kernel source is
+    unchanged."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic_serve_b32.json")) as f:
-            t = json.load(f)["runs"][TRAFFIC_RUN][kernel]
+            t = json.load(f)["runs"][run or TRAFFIC_RUN][kernel]
         with open(os.path.join(ROOT, t["source"]), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest()[:16] != t["sha256_16"]:
                 return None
@@ -706,7 +707,10 @@ def time_fp8_cache(args, w, stream, D, pk):
     out = {"value": whole_job_rate(1, w8, ms), "unit": UNIT, "ms_per_step": ms, "steps": n,
            "attention": {"avg_us": 1e3 * avg, "algorithmic_bytes_per_launch": by,
                          "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": ach / pk["hbm_gbs"]},
+                         "frac": ach / pk["hbm_gbs"],
+                         "traffic": measured_traffic(
+                             "attention",
+                             f"{w8.name}/fp8/{'paged' if args.paged else 'contiguous'}")},
            "cache": "E4M3 codes, one scale per layer for K and for V"}
     del dev
     torch.cuda.empty_cache()
