@@ -381,6 +381,27 @@ unsigned long long dflash_launch_count(void);
  */
 void dflash_test_wait_limit(unsigned long long ns);
 
+/*
+ * Test aid (no counterpart in the source pages): builds on the device the work list the
+ * tensor-core attention (bf16 dims) would use for layer `layer` of cache `c` — its current
+ * lengths, plus the rows a KV inject of the same call appends (cu_rows [batch + 1] and M,
+ * as for dflash_draft_layer; null and 0 for none), and a sliding window (0 = none) — in
+ * `workspace` (dflash_workspace_bytes), then copies it to host memory `out` (int32):
+ *   [0] n_ctas  [1] max_splits  [2] item_cost  [3] n_items  [4] n_merge
+ *   first[n_ctas + 1]                 CTA i takes list items first[i] .. first[i + 1] - 1
+ *   items[n_ctas + n_items][4]        {pair, k_begin, k_end, split (-1 = whole range)}: each
+ *                                     CTA's first item, then the list
+ *   splits[batch * n_kv]              items per pair (0: a refused sequence)
+ *   merge_list[n_merge]               pair | items << 20, the pairs the combine writes
+ * *n_out receives the number of ints written (or needed: DFLASH_ERR_INVALID_ARG when
+ * out_ints is smaller; `out` may be null with out_ints 0 to ask for the size). Synchronises
+ * `stream`; the cache is not modified.
+ */
+dflash_status dflash_test_attn_worklist(const dflash_dims* dims, const dflash_kv_cache* cache,
+                                        int layer, const int32_t* cu_rows, int M, int window,
+                                        void* workspace, size_t workspace_bytes, int32_t* out,
+                                        size_t out_ints, size_t* n_out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -235,5 +235,7 @@ inline __device__ void build(const Params& p) {
 
 // Work-list buffers and parameters of an attention call (attn_tc.cu).
 sched::Params attn_sched_params(const AttnParams& a);
+// Builds that work list on `s` alone (test aid); *sp receives its buffers.
+cudaError_t attn_worklist_build(const AttnParams& a, cudaStream_t s, sched::Params* sp);
 
 }  // namespace dflash

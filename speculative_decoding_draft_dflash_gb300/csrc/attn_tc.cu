@@ -960,6 +960,13 @@ sched::Params attn_sched_params(const AttnParams& a) {
   return sp;
 }
 
+cudaError_t attn_worklist_build(const AttnParams& a, cudaStream_t s, sched::Params* sp) {
+  *sp = attn_sched_params(a);
+  LaunchScope ls_(DFLASH_KERNEL_SCHEDULE, s);
+  attn_schedule_kernel<<<1, 1024, 0, s>>>(*sp);
+  return cudaGetLastError();
+}
+
 cudaError_t attn_tc(const AttnParams& a, cudaStream_t s) {
   if (a.batch <= 0) return cudaSuccess;
   if (a.d_h != 128) return cudaErrorInvalidValue;

@@ -656,6 +656,55 @@ DFLASH_API dflash_status dflash_cache_crop(const dflash_kv_cache* c, const int32
   return cuda_status(crop_lens(c->lens, c->n_layers, c->batch, new_lens, status, stream));
 }
 
+DFLASH_API dflash_status dflash_test_attn_worklist(const dflash_dims* d, const dflash_kv_cache* c,
+                                                   int layer, const int32_t* cu_rows, int M,
+                                                   int window, void* workspace, size_t ws_bytes,
+                                                   int32_t* out, size_t out_ints, size_t* n_out,
+                                                   cudaStream_t stream) {
+  dflash_status st = check_dims(d);
+  if (st != DFLASH_OK) return st;
+  st = check_cache(c, layer);
+  if (st != DFLASH_OK) return st;
+  if (d->dtype != DFLASH_BF16 || (!out && out_ints > 0) || !n_out || !workspace || window < 0 ||
+      M < 0 || (M > 0 && !cu_rows))
+    return DFLASH_ERR_INVALID_ARG;
+  Carver cv(workspace, ws_bytes);
+  BlockScratch s = carve_block(cv, d, c->batch, c->capacity, window);
+  if (!cv.ok) return DFLASH_ERR_WORKSPACE;
+  unsigned* status = status_word();
+  if (!status) return DFLASH_ERR_CUDA;
+  AttnParams p = block_attention(d, c, layer, s, window, 0.f, c->capacity, nullptr, status);
+  p.pre_rows = M > 0 ? cu_rows : nullptr;
+  p.pre_M = M;
+  sched::Params sp;
+  int cnt[2] = {0, 0};
+  cudaError_t e = attn_worklist_build(p, stream, &sp);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(cnt, sp.n_items, sizeof(cnt), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return DFLASH_ERR_CUDA;
+  const size_t n_ctas = (size_t)sp.n_sm, pairs = (size_t)c->batch * d->n_kv;
+  const size_t need = 5 + (n_ctas + 1) + 4 * (n_ctas + (size_t)cnt[0]) + pairs + (size_t)cnt[1];
+  *n_out = need;
+  if (out_ints < need) return DFLASH_ERR_INVALID_ARG;
+  out[0] = (int32_t)n_ctas;
+  out[1] = sp.max_splits;
+  out[2] = sp.item_cost;
+  out[3] = cnt[0];
+  out[4] = cnt[1];
+  int32_t* o = out + 5;
+  e = cudaMemcpyAsync(o, sp.first, (n_ctas + 1) * 4, cudaMemcpyDeviceToHost, stream);
+  o += n_ctas + 1;
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(o, sp.items, (n_ctas + cnt[0]) * 16, cudaMemcpyDeviceToHost, stream);
+  o += 4 * (n_ctas + cnt[0]);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(o, sp.splits, pairs * 4, cudaMemcpyDeviceToHost, stream);
+  o += pairs;
+  if (e == cudaSuccess && cnt[1] > 0)
+    e = cudaMemcpyAsync(o, sp.merge_list, (size_t)cnt[1] * 4, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  return cuda_status(e);
+}
+
 DFLASH_API dflash_status dflash_status_get(unsigned int* out, cudaStream_t stream) {
   if (!out) return DFLASH_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return DFLASH_ERR_CUDA;

@@ -77,6 +77,8 @@ def _load():
         "dflash_trace_stop": (c_int, [P, P, c_int, P]),
         "dflash_launch_count": (ctypes.c_ulonglong, []),
         "dflash_test_wait_limit": (None, [ctypes.c_ulonglong]),
+        "dflash_test_attn_worklist": (c_int, [P, P, c_int, P, c_int, c_int, P, c_size_t, P,
+                                              c_size_t, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -446,3 +448,33 @@ def dflash_launch_count():
 def dflash_test_wait_limit(ns):
     """Test aid: limit (ns) of the kernels' pipeline waits for later launches; 0 = 2 s."""
     _lib.dflash_test_wait_limit(int(ns))
+
+
+def dflash_test_attn_worklist(dims, cache, layer, cu_rows, M, sliding_window, workspace,
+                              stream=None):
+    """Test aid: the tensor-core attention's work list for the cache's current lengths (plus
+    the rows an inject of cu_rows / M would append), as host arrays: n_ctas, max_splits,
+    item_cost, first [n_ctas + 1], items [n_ctas + n_items, 4], splits [pairs], merge_list."""
+    desc = _desc(dims, cache)
+    cu = _ptr(cu_rows, "cu_rows", torch.int32, _batch(desc) + 1) if M > 0 else None
+    need = ctypes.c_size_t(0)
+    args = (ctypes.byref(dims), ctypes.byref(desc), int(layer), cu, int(M), int(sliding_window),
+            *_ws(workspace))
+    st = _lib.dflash_test_attn_worklist(*args, None, 0, ctypes.byref(need), _stream(stream))
+    if st != ERR_INVALID_ARG:
+        _check(st, "dflash_test_attn_worklist")
+    out = np.zeros(need.value, dtype=np.int32)
+    _check(_lib.dflash_test_attn_worklist(*args, out.ctypes.data_as(ctypes.c_void_p), out.size,
+                                          ctypes.byref(need), _stream(stream)),
+           "dflash_test_attn_worklist")
+    n_ctas, max_splits, item_cost, n_items, n_merge = (int(v) for v in out[:5])
+    o = 5
+    first = out[o:o + n_ctas + 1]
+    o += n_ctas + 1
+    items = out[o:o + 4 * (n_ctas + n_items)].reshape(-1, 4)
+    o += 4 * (n_ctas + n_items)
+    pairs = _batch(desc) * dims.n_kv
+    splits = out[o:o + pairs]
+    o += pairs
+    return {"n_ctas": n_ctas, "max_splits": max_splits, "item_cost": item_cost, "first": first,
+            "items": items, "splits": splits, "merge_list": out[o:o + n_merge]}
