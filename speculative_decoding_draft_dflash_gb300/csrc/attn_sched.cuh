@@ -51,7 +51,7 @@ struct Params {
   int32_t* lens_new;        // [batch]: length after the call
   int batch, n_kv, bs, window, capacity, table_len, max_splits, n_sm;
   int align;                // key ranges start on multiples of this (paged cache: a page)
-  int item_cost;            // cost of an item header, in units of kTileCost per tile
+  int item_cost;            // cost of an item's header, on the scale of kTileCost per tile
 };
 
 // Bytes of the work-list area for `pairs` (sequence, KV head) pairs of `batch` sequences
