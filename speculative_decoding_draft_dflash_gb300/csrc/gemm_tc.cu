@@ -512,6 +512,13 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
     ptx::mbar_init(done, 1);
     ptx::fence_mbar_init();
   }
+  // PAIR: both CTAs' barriers are initialised before either CTA's copies or commits can
+  // reach the other's: every thread arrives at the cluster barrier now and waits for it
+  // after the TMEM allocation
+  if (PAIR) {
+    __syncwarp();  // the arrive is a warp-aligned instruction
+    ptx::cluster_arrive();
+  }
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < (second ? 1 : 8); ++i) ptx::prefetch_tmap(&amap[i]);
     for (int i = 0; i < w_count; ++i) ptx::prefetch_tmap(&bmap[i]);
@@ -528,9 +535,7 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
   }
   ptx::tc_fence_before();
   __syncthreads();
-  // PAIR: both CTAs' barriers are initialised before either CTA's copies or commits can
-  // reach the other's
-  if (PAIR) ptx::cluster_sync();
+  if (PAIR) ptx::cluster_wait();
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
@@ -782,7 +787,7 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
         }
       }
     }
-    ptx::bulk_commit_wait_all();
+    ptx::bulk_commit_wait_read();
   }
   ptx::tc_fence_before();
   __syncthreads();

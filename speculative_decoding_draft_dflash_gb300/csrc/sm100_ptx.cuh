@@ -205,6 +205,12 @@ __device__ __forceinline__ void bulk_commit_wait_all() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// The same, waiting only until the copies have read their shared-memory sources (enough
+// before a CTA exits: the writes are complete when the kernel is).
+__device__ __forceinline__ void bulk_commit_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // 32-byte global store (address 32-byte aligned): one full sector per thread.
 __device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
@@ -289,6 +295,13 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The two halves of cluster_sync, for work in between (every thread runs both, in order).
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // shared::cluster address of the same shared-memory location in CTA `rank` of the cluster.
