@@ -28,12 +28,13 @@
 //   9 (7)      MMA: S_j = Q K_j^T (two TMEM S buffers), O += P_j V_j (P from
 //              TMEM, V read MN-major from shared memory); S_{j+2} is issued
 //              before PV_j;
-//   10         TMA: V tiles (released later than K, so on their own thread;
+//   10 (8)     TMA: V tiles (released later than K, so on their own thread;
 //              the first waits for the first K tile, which the first S needs);
-//   2,3,6,7    fp8 cache with R <= 64 only: V tile conversion to f16 (these warps
-//              serve TMEM lanes 64-127, which then hold no query rows).
-// In parentheses: the warp for a bf16 cache with R <= 64, which keeps these
-// single-thread roles off the two sub-partitions the softmax then runs on.
+//   2,3,10,11  fp8 cache with R <= 64 only: V tile conversion to f16 (a twelfth
+//              warp; the softmax leaves lane quarters 2-3 and their warps free).
+// In parentheses: the warp with R <= 64 (for the V loads: fp8 cache with R <= 64),
+// which keeps the single-thread roles off the two sub-partitions the softmax then
+// runs on.
 // O is rescaled in TMEM only when a row's running maximum grows by more than
 // 2^8, so almost every tile skips it.
 //
@@ -62,7 +63,7 @@ constexpr int TK = 128;                    // keys per tile
 constexpr uint32_t TILE = 128 * 128 * 2;   // 32 KB: one bf16 K or V tile (128 keys x 128 dims)
 constexpr uint32_t HALF = TILE / 2;        // one 64-column swizzled box
 constexpr int kSoftmaxWarps = 8;
-constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
+
 constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 384;  // TMEM columns: S[2], O, P[2] (64 each)
 constexpr int kRing = 4;                   // item ring slots
 
@@ -84,12 +85,15 @@ struct Plan {
   static constexpr bool CONV = FP8 && NARROW;
   // Warp roles. A warp issues on sub-partition (warp % 4), and only the warps of
   // sub-partition q can touch TMEM lanes 32q..32q+31. With R <= 64 the softmax lives on
-  // sub-partitions 0-1. bf16: the K/Q producer and the MMA issuer then move to warps 6
-  // and 7 (sub-partitions 2-3) instead of competing with the softmax for issue slots,
-  // and warps 8, 9 stay idle. fp8: warps 2, 3, 6 and 7 convert V (one key row per
-  // thread), which needs all four; the producer and issuer stay on 8 and 9.
-  static constexpr int W_KQ = NARROW && !CONV ? 6 : 8, W_MMA = NARROW && !CONV ? 7 : 9;
-  static constexpr int W_V = 10;
+  // sub-partitions 0-1, and the K/Q producer and the MMA issuer move to warps 6 and 7
+  // (sub-partitions 2-3) instead of competing with the softmax for issue slots. bf16:
+  // warps 2, 3, 8, 9 stay idle. fp8: four warps on sub-partitions 2-3 convert V (one key
+  // row per thread), 2, 3 and a twelfth pair 10, 11, and the V producer moves to warp 8.
+  static constexpr int W_KQ = NARROW ? 6 : 8, W_MMA = NARROW ? 7 : 9;
+  static constexpr int W_V = CONV ? 8 : 10;
+  // CONV: the V converters are warps 2, 3, 10 and 11 (a twelfth warp), so that the K/Q
+  // producer and the MMA issuer keep sub-partitions 2-3 as with a bf16 cache
+  static constexpr int THREADS = 32 * (kSoftmaxWarps + (CONV ? 4 : 3));
   static constexpr uint32_t TILE_B = FP8 ? TK * 128 : TILE;  // one K or V tile (as loaded)
   static constexpr int K_STAGES = FP8 ? 4 : (NARROW ? 3 : 2);
   static constexpr int V_STAGES = FP8 ? 3 : 2;
@@ -250,7 +254,7 @@ __global__ void __launch_bounds__(1024) attn_schedule_kernel(sched::Params p) { 
 // attention
 // ---------------------------------------------------------------------------
 template <bool NARROW, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams p) {
+__global__ void __launch_bounds__(Plan<NARROW, FP8>::THREADS, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams p) {
   using PL = Plan<NARROW, FP8>;
   constexpr int NCOL = 64;  // S columns per softmax thread
   extern __shared__ uint8_t smem_raw[];
@@ -267,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const int n_soft = 64 * nq;                     // softmax threads
   const bool soft = warp < kSoftmaxWarps && (warp & 3) < nq;
   // V converters (PL::CONV): the warps of lane quarters 2 and 3, one key row per thread
-  const bool conv = PL::CONV && warp < kSoftmaxWarps && (warp & 3) >= 2;
+  const bool conv = PL::CONV && (warp & 3) >= 2 && (warp < 4 || warp >= 10);
   constexpr int kConv = PL::CONV ? 128 : 0;
   const uint32_t sbase = ptx::smem_u32(smem);
   // barriers (8 bytes each): q 2+2, k and v full+empty per stage, s 2+2, p 2, pv 2,
@@ -548,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     // thread = key row k of the tile: 8 chunks of 16 codes -> 16 chunks of 8 f16 values,
     // both tiles in the 128-byte swizzled layout the MMA reads (chunk c of row k at
     // c ^ (k & 7)); rows past the key range are written as zeros
-    const int k = (warp >> 2) * 64 + ((warp & 3) - 2) * 32 + lane;
+    const int k = (warp >= 10 ? 64 : 0) + ((warp & 3) - 2) * 32 + lane;
     const int sw = k & 7;
     int gv = 0;
     for (int n = 0;; ++n) {
@@ -905,7 +909,7 @@ cudaError_t launch_attn(const AttnTcParams& p, int grid, cudaStream_t s) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   LaunchScope ls_(DFLASH_KERNEL_ATTENTION, s);
-  attn_tc_kernel<NARROW, FP8><<<grid, kThreads, smem, s>>>(p);
+  attn_tc_kernel<NARROW, FP8><<<grid, Plan<NARROW, FP8>::THREADS, smem, s>>>(p);
   return cudaGetLastError();
 }
 
