@@ -662,7 +662,9 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
       ptx::named_sync(2, 256);  // gamma and RoPE pairs staged by set 0, for both sets
     }
     // warp-uniform: tcgen05.ld below is a .sync.aligned instruction
-    const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(done, 0, &abort_flag, p.status, p.wait_ns));
+    // (the epilogue warps wait for the whole mainloop: suspended, off the issue slots of
+    // the producer and the MMA issuer)
+    const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_idle(done, 0, &abort_flag, p.status, p.wait_ns));
     ptx::tc_fence_after();
     if (ok && !HEADS) {
 #pragma unroll 1

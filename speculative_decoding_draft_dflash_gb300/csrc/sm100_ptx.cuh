@@ -52,6 +52,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, letting the hardware suspend the thread for up to `hint_ns` while the
+// phase is incomplete (it resumes when the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Bounded wait on phase `parity` of an mbarrier. Returns false when the CTA
@@ -63,6 +77,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      *abort_flag = 1;
+      atomicOr(status, DFLASH_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// mbar_wait for waiters off the critical path (many threads waiting long): each test may
+// suspend the thread for up to 20 us, so that the waiting warps take no issue slots from
+// the warps they share a sub-partition with.
+__device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               unsigned* status, uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
     if (*abort_flag) return false;
     if (globaltimer() - t0 > limit_ns) {
       *abort_flag = 1;
