@@ -123,6 +123,23 @@ __device__ __forceinline__ int cta_max(int v, int* tmp) {
   return m;
 }
 
+// Minimum of v over threads threadIdx.x .. blockDim.x - 1 (a suffix minimum in thread
+// order). tmp: 32 ints of shared memory.
+__device__ __forceinline__ int cta_suffix_min(int v, int* tmp) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, x, o);
+    if (lane + o < 32) x = min(x, y);
+  }
+  if (lane == 0) tmp[w] = x;
+  __syncthreads();
+  for (int i = w + 1; i < nw; ++i) x = min(x, tmp[i]);
+  __syncthreads();
+  return x;
+}
+
 // Tiles of pair pr's key range (0 for a refused sequence).
 __device__ __forceinline__ int pair_tiles(const Params& p, int pr) {
   const Range r = seq_range(p, pr / p.n_kv);
@@ -209,10 +226,17 @@ inline __device__ void build(const Params& p) {
   }
   __syncthreads();
   // items are in stream order with non-decreasing owners: CTA c starts at the first item
-  // owned by c or a later CTA
-  if (threadIdx.x == 0) {
+  // owned by c or a later CTA (a suffix minimum over the CTAs; n_sm < blockDim.x, else
+  // one thread walks them)
+  if ((int)blockDim.x > p.n_sm) {
+    const int c = threadIdx.x;
+    const int f = cta_suffix_min(c < p.n_sm ? s_first[c] : n_list, tmp);
+    if (c <= p.n_sm) s_first[c] = f;
+  } else if (threadIdx.x == 0) {
     s_first[p.n_sm] = n_list;
     for (int c = p.n_sm - 1; c >= 0; --c) s_first[c] = min(s_first[c], s_first[c + 1]);
+  }
+  if (threadIdx.x == 0) {
     *p.n_items = n_list;
     *p.n_merge = s_merge;
   }

@@ -64,29 +64,34 @@ __device__ __forceinline__ void store4<bf16>(bf16* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = u;
 }
 
-// Sum of the split-K partials of one row chunk: all loads of two splits are issued
-// before any of them is used, so a row costs one memory round trip per two splits.
-template <int CH>
+// v[k] = sum over the splits of chunk k (thread's columns 4 (threadIdx.x + k NT)), added
+// in pairs of consecutive splits; the loads of SB splits (an even count) are issued
+// before any of them is added, so a row costs one memory round trip per SB splits.
+template <int CH, int NT, int SB>
 __device__ __forceinline__ void sum_splits(const float4* __restrict__ y4, size_t split_stride4,
                                            int splits, int n4, float4 (&v)[CH]) {
+  static_assert(SB % 2 == 0, "splits are added in pairs");
 #pragma unroll
   for (int k = 0; k < CH; ++k) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < splits; s += 2) {
-    float4 a[CH], b[CH];
-    const bool two = s + 1 < splits;
+  for (int s0 = 0; s0 < splits; s0 += SB) {
+    float4 a[SB][CH];
 #pragma unroll
-    for (int k = 0; k < CH; ++k) {
-      const int c = threadIdx.x + k * kNormThreads;
-      a[k] = c < n4 ? y4[s * split_stride4 + c] : make_float4(0.f, 0.f, 0.f, 0.f);
-      b[k] = (two && c < n4) ? y4[(s + 1) * split_stride4 + c] : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    for (int j = 0; j < SB; ++j)
 #pragma unroll
-    for (int k = 0; k < CH; ++k) {
-      v[k].x += a[k].x + b[k].x;
-      v[k].y += a[k].y + b[k].y;
-      v[k].z += a[k].z + b[k].z;
-      v[k].w += a[k].w + b[k].w;
-    }
+      for (int k = 0; k < CH; ++k) {
+        const int c = threadIdx.x + k * NT;
+        a[j][k] = (s0 + j < splits && c < n4) ? y4[(s0 + j) * split_stride4 + c]
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+    for (int j = 0; j < SB; j += 2)
+#pragma unroll
+      for (int k = 0; k < CH; ++k) {
+        v[k].x += a[j][k].x + a[j + 1][k].x;
+        v[k].y += a[j][k].y + a[j + 1][k].y;
+        v[k].z += a[j][k].z + a[j + 1][k].z;
+        v[k].w += a[j][k].w + a[j + 1][k].w;
+      }
   }
 }
 
@@ -102,8 +107,9 @@ __device__ __forceinline__ float4 load_gamma4<bf16>(const bf16* g) {
   return make_float4(a.x, a.y, b.x, b.y);
 }
 
-template <typename T, int CH>
-__global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_vec_kernel(
+// One CTA of NT threads per row; chunk k of a thread is float4 column threadIdx.x + k NT.
+template <typename T, int CH, int NT>
+__global__ void __launch_bounds__(NT) rmsnorm_rows_vec_kernel(
     const float* __restrict__ Y, int splits, int M, int N, const T* __restrict__ gamma, float eps,
     T* __restrict__ out) {
   __shared__ float red[32];
@@ -114,11 +120,11 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_vec_kernel(
   float4 g[CH];
 #pragma unroll
   for (int k = 0; k < CH; ++k) {
-    const int c = threadIdx.x + k * kNormThreads;
+    const int c = threadIdx.x + k * NT;
     g[k] = c < n4 ? load_gamma4(gamma + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   float4 v[CH];
-  sum_splits(y4, split_stride4, splits, n4, v);
+  sum_splits<CH, NT, (CH <= 2 ? 8 : 2)>(y4, split_stride4, splits, n4, v);
   float ss = 0.f;
 #pragma unroll
   for (int k = 0; k < CH; ++k)
@@ -127,7 +133,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_vec_kernel(
   const float r = 1.0f / sqrtf(ss / (float)N + eps);
 #pragma unroll
   for (int k = 0; k < CH; ++k) {
-    const int c = threadIdx.x + k * kNormThreads;
+    const int c = threadIdx.x + k * NT;
     if (c < n4)
       store4<T>(out + (size_t)row * N + 4 * c, make_float4(v[k].x * r * g[k].x, v[k].y * r * g[k].y,
                                                            v[k].z * r * g[k].z, v[k].w * r * g[k].w));
@@ -219,17 +225,22 @@ __global__ void __launch_bounds__(256) head_epilogue_bf16_kernel(HeadEpilogue e)
   if (wid >= e.rows * heads) return;
   const int row = wid / heads, head = wid - row * heads;
   const int kind = head < e.n_q ? 0 : (head < e.n_q + e.n_kv ? 1 : 2);  // Q, K, V
-  // split-K partials of this (row, head): two splits per round trip
+  // split-K partials of this (row, head): eight splits per round trip, added in pairs
   const size_t split_stride4 = (size_t)e.rows * e.ldY / 4;
   const float4* y4 = reinterpret_cast<const float4*>(e.Y + (size_t)row * e.ldY + (size_t)head * 128) + lane;
   float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < e.splits; s += 2) {
-    const float4 a = y4[s * split_stride4];
-    const float4 c = s + 1 < e.splits ? y4[(s + 1) * split_stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
-    x.x += a.x + c.x;
-    x.y += a.y + c.y;
-    x.z += a.z + c.z;
-    x.w += a.w + c.w;
+  for (int s0 = 0; s0 < e.splits; s0 += 8) {
+    float4 a[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      a[j] = s0 + j < e.splits ? y4[(s0 + j) * split_stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      x.x += a[j].x + a[j + 1].x;
+      x.y += a[j].y + a[j + 1].y;
+      x.z += a[j].z + a[j + 1].z;
+      x.w += a[j].w + a[j + 1].w;
+    }
   }
   float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
   if (kind < 2) {  // gamma has no alignment guarantee beyond its element size
@@ -358,18 +369,28 @@ __global__ void rope_table_kernel(double theta, int d_h, int max_pos, float2* ta
   }
 }
 
-// smallest per-thread chunk count (1, 2, 4 or 8 float4) that covers the row
+// smallest per-thread chunk count (1, 2, 4 or 8 float4) that covers the row; with few rows
+// (fewer than 64) a CTA of 1024 threads per row, whose threads then hold one or two chunks
+// and load eight splits at a time
 template <typename T>
-void launch_norm(int need, int M, cudaStream_t s, const float* Y, int splits, int N, const T* gamma,
+void launch_norm(int M, cudaStream_t s, const float* Y, int splits, int N, const T* gamma,
                  float eps, T* out) {
+  if (M < 64 && N / 4 <= 2 * 1024) {
+    if (N / 4 <= 1024)
+      rmsnorm_rows_vec_kernel<T, 1, 1024><<<M, 1024, 0, s>>>(Y, splits, M, N, gamma, eps, out);
+    else
+      rmsnorm_rows_vec_kernel<T, 2, 1024><<<M, 1024, 0, s>>>(Y, splits, M, N, gamma, eps, out);
+    return;
+  }
+  const int need = (N / 4 + kNormThreads - 1) / kNormThreads;
   if (need <= 1)
-    rmsnorm_rows_vec_kernel<T, 1><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, gamma, eps, out);
+    rmsnorm_rows_vec_kernel<T, 1, kNormThreads><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, gamma, eps, out);
   else if (need <= 2)
-    rmsnorm_rows_vec_kernel<T, 2><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, gamma, eps, out);
+    rmsnorm_rows_vec_kernel<T, 2, kNormThreads><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, gamma, eps, out);
   else if (need <= 4)
-    rmsnorm_rows_vec_kernel<T, 4><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, gamma, eps, out);
+    rmsnorm_rows_vec_kernel<T, 4, kNormThreads><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, gamma, eps, out);
   else
-    rmsnorm_rows_vec_kernel<T, 8><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, gamma, eps, out);
+    rmsnorm_rows_vec_kernel<T, 8, kNormThreads><<<M, kNormThreads, 0, s>>>(Y, splits, M, N, gamma, eps, out);
 }
 
 }  // namespace
@@ -380,12 +401,11 @@ cudaError_t rmsnorm_rows(int dtype, const float* Y, int splits, int M, int N, co
   // the vector kernel loads gamma 4 elements at a time (8-byte aligned for bf16)
   if (N % 4 == 0 && N <= 4 * kNormThreads * kNormMaxChunks &&
       (dtype == DFLASH_F32 || ((uintptr_t)gamma & 7) == 0)) {
-    const int need = (N / 4 + kNormThreads - 1) / kNormThreads;
     LaunchScope ls_(DFLASH_KERNEL_RMSNORM, s);
     if (dtype == DFLASH_F32)
-      launch_norm<float>(need, M, s, Y, splits, N, (const float*)gamma, eps, (float*)out);
+      launch_norm<float>(M, s, Y, splits, N, (const float*)gamma, eps, (float*)out);
     else
-      launch_norm<bf16>(need, M, s, Y, splits, N, (const bf16*)gamma, eps, (bf16*)out);
+      launch_norm<bf16>(M, s, Y, splits, N, (const bf16*)gamma, eps, (bf16*)out);
     return cudaGetLastError();
   }
   if (dtype == DFLASH_F32)
