@@ -248,7 +248,12 @@ dflash_status dflash_block_attn(const dflash_dims* dims, const dflash_kv_cache* 
  * 4.2). With bf16 and shapes whose two projections fill the GPU without split-K,
  * both projections (context K/V and block Q/K/V, with their norm / RoPE / store
  * epilogues) and the attention work list run in one launch, followed by the
- * attention and its combine; otherwise it issues the two calls.
+ * attention and its combine. With bf16, d_h = 128 and fewer rows (a few
+ * sequences, M and batch * bs within one 128-row tile), both projections and the
+ * work list run as one split-K launch, then one epilogue launch finishes both,
+ * then the attention and its combine. Otherwise it issues the two calls.
+ * DFLASH_FUSED_LAYER in the environment picks: 0 the two calls, 1 the first
+ * form wherever the shapes allow it, 2 the split-K form wherever it applies.
  *   arguments      as dflash_kv_inject (C, cu_rows, M) and dflash_block_attn
  *   workspace      dflash_workspace_bytes(dims, batch, capacity, max(M, ...))
  */

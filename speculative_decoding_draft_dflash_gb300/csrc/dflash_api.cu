@@ -195,6 +195,31 @@ BlockScratch carve_block(Carver& cv, const dflash_dims* d, int batch, int capaci
   return s;
 }
 
+// A draft layer's two projections as one split-K launch (bf16, few sequences): the block's
+// scratch, then fp32 partials of the context K/V (up to the launch's row tiles) and of the
+// block Q/K/V (the block's own partials when they are large enough). splits = 0: the
+// launch does not apply to this batch.
+struct LayerSplitScratch { BlockScratch b; float* Y0; float* Y1; int splits; };
+
+LayerSplitScratch carve_layer_split(Carver& cv, const dflash_dims* d, int batch, int capacity,
+                                    int window, int M) {
+  LayerSplitScratch s;
+  s.b = carve_block(cv, d, batch, capacity, window);
+  s.Y0 = s.Y1 = nullptr;
+  s.splits = 0;
+  if (d->dtype != DFLASH_BF16 || d->d_h != 128) return s;
+  const int rows = batch * d->block_size;
+  const Weights Wkv = kv_weights(d, nullptr, nullptr), Wqkv = qkv_weights(d, nullptr, nullptr, nullptr);
+  s.splits = gemm_tc_layer_split_splits(rows, Wkv, Wqkv, d->d);
+  if (s.splits == 0) return s;
+  const int mc = M < gemm_tc_layer_split_rows(rows, Wkv, Wqkv, d->d)
+                     ? M : gemm_tc_layer_split_rows(rows, Wkv, Wqkv, d->d);
+  s.Y0 = cv.take<float>((size_t)s.splits * mc * Wkv.total());
+  s.Y1 = s.b.Y && s.b.splits >= s.splits ? s.b.Y
+                                         : cv.take<float>((size_t)s.splits * rows * Wqkv.total());
+  return s;
+}
+
 // Projection + per-head epilogue: fused into the tcgen05 GEMM when no split-K
 // is needed, else fp32 partials (ep.Y) and a separate epilogue kernel.
 cudaError_t project_heads(const dflash_dims* d, const Segments& A, int M, const Weights& W,
@@ -244,6 +269,11 @@ DFLASH_API size_t dflash_workspace_bytes(const dflash_dims* d, int batch, int ca
   {
     Carver cv(nullptr, ~size_t(0));
     carve_block(cv, d, batch, capacity, 0);
+    need = need > cv.off ? need : cv.off;
+  }
+  {
+    Carver cv(nullptr, ~size_t(0));
+    carve_layer_split(cv, d, batch, capacity, 0, max_rows);
     need = need > cv.off ? need : cv.off;
   }
   return need;
@@ -546,7 +576,38 @@ DFLASH_API dflash_status dflash_draft_layer(const dflash_dims* d, const dflash_k
   if (st != DFLASH_OK) return st;
   const int rows = c->batch * d->block_size;
   const Weights Wkv = kv_weights(d, W_K, W_V), Wqkv = qkv_weights(d, W_Q, W_K, W_V);
-  if (d->dtype != DFLASH_BF16 || M == 0 || !gemm_tc_layer_ok(M, Wkv, rows, Wqkv, d->d)) {
+  const bool grouped = d->dtype == DFLASH_BF16 && M > 0 && gemm_tc_layer_ok(M, Wkv, rows, Wqkv, d->d);
+  // few sequences: both projections as one split-K launch, both epilogues as one launch
+  const bool split = d->dtype == DFLASH_BF16 && M > 0 && !grouped && d->d_h == 128 &&
+                     gemm_tc_layer_split_splits(rows, Wkv, Wqkv, d->d) > 0 &&
+                     M <= gemm_tc_layer_split_rows(rows, Wkv, Wqkv, d->d);
+  if (split) {
+    Carver cv(workspace, ws_bytes);
+    LayerSplitScratch s = carve_layer_split(cv, d, c->batch, c->capacity, window, M);
+    if (!cv.ok) return DFLASH_ERR_WORKSPACE;
+    unsigned* status = status_word();
+    if (!status) return DFLASH_ERR_CUDA;
+    const HeadEpilogue ep_kv = inject_epilogue(d, c, layer, cu_rows, M, gamma_k, rope, table_len,
+                                               s.Y0, s.splits, status);
+    HeadEpilogue ep_qkv = block_epilogue(d, c, layer, gamma_q, gamma_k, rope, table_len, s.b.q,
+                                         s.Y1, s.splits, status);
+    ep_qkv.pre_rows = cu_rows;  // the block follows the rows injected here
+    ep_qkv.pre_M = M;
+    AttnParams p = block_attention(d, c, layer, s.b, window, scaling, table_len, out, status);
+    p.pre_rows = cu_rows;
+    p.pre_M = M;
+    p.lens_out = c->lens + (size_t)layer * c->batch;
+    p.sched_ready = true;
+    const sched::Params sp = attn_sched_params(p);
+    cudaError_t e = gemm_tc_layer_split(C, M, Wkv, s.Y0, H, rows, Wqkv, s.Y1, d->d, &sp, status,
+                                        stream);
+    if (e == cudaSuccess)
+      e = head_epilogue_bf16_pair(ep_kv, ep_qkv, stream);
+    if (e == cudaSuccess)
+      e = attention(d->dtype, p, stream);
+    return cuda_status(e);
+  }
+  if (!grouped) {
     // the same work as two calls
     st = dflash_kv_inject(d, c, layer, C, cu_rows, M, W_K, W_V, gamma_k, rope, table_len,
                           workspace, ws_bytes, stream);

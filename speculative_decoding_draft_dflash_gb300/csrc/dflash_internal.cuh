@@ -223,8 +223,21 @@ cudaError_t gemm_tc_layer(const void* C, int Mc, const Weights& Wkv, const HeadE
                           const void* H, int Mb, const Weights& Wqkv, const HeadEpilogue& ep_qkv,
                           int K, const sched::Params* sp, unsigned* status, cudaStream_t s);
 
-// Warp-per-(row, head) epilogue for bf16 with d_h = 128 (sums the split-K partials).
+// The same two projections in one split-K launch (fp32 partials Y0: [splits][Mc][N0],
+// Y1: [splits][Mb][N1]) for batches too small to fill the GPU without split-K, plus
+// optionally the work-list CTA. The plan depends on Mb alone: _splits gives its K splits
+// (0: not applicable) and _rows the most context rows it takes (Mc <= that).
+int gemm_tc_layer_split_splits(int Mb, const Weights& Wkv, const Weights& Wqkv, int K);
+int gemm_tc_layer_split_rows(int Mb, const Weights& Wkv, const Weights& Wqkv, int K);
+cudaError_t gemm_tc_layer_split(const void* C, int Mc, const Weights& Wkv, float* Y0,
+                                const void* H, int Mb, const Weights& Wqkv, float* Y1, int K,
+                                const sched::Params* sp, unsigned* status, cudaStream_t s);
+
+// Warp-per-(row, head) epilogue for bf16 with d_h = 128 (sums the split-K partials);
+// _pair finishes two epilogues (an inject's and the block's) in one launch.
 cudaError_t head_epilogue_bf16(const HeadEpilogue& e, cudaStream_t s);
+cudaError_t head_epilogue_bf16_pair(const HeadEpilogue& e0, const HeadEpilogue& e1,
+                                    cudaStream_t s);
 
 // lens[b] += n_b where the append fitted (same checks as the epilogue)
 cudaError_t lens_advance(int32_t* lens, const int32_t* cu_rows, int batch, int bs, int M,

@@ -218,9 +218,7 @@ __global__ void head_epilogue_kernel(HeadEpilogue e) {
 // depend on the row's sequence (split partials, gamma) are issued first; the
 // sequence is found with one ballot over cu_rows, so the dependent chain is
 // cu_rows -> lens -> RoPE row.
-__global__ void __launch_bounds__(256) head_epilogue_bf16_kernel(HeadEpilogue e) {
-  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+__device__ __forceinline__ void head_row_bf16(const HeadEpilogue& e, int wid, int lane) {
   const int heads = e.n_q + 2 * e.n_kv;
   if (wid >= e.rows * heads) return;
   const int row = wid / heads, head = wid - row * heads;
@@ -327,6 +325,21 @@ __global__ void __launch_bounds__(256) head_epilogue_bf16_kernel(HeadEpilogue e)
   u.x = *reinterpret_cast<uint32_t*>(&lo2);
   u.y = *reinterpret_cast<uint32_t*>(&hi2);
   reinterpret_cast<uint2*>(dst)[lane] = u;
+}
+
+__global__ void __launch_bounds__(256) head_epilogue_bf16_kernel(const __grid_constant__ HeadEpilogue e) {
+  head_row_bf16(e, blockIdx.x * 8 + (threadIdx.x >> 5), threadIdx.x & 31);
+}
+
+// Two epilogues in one launch (an inject's context rows and the block's rows of the same
+// layer): warps [0, w0) finish e0's (row, head) pairs, the rest e1's.
+__global__ void __launch_bounds__(256) head_epilogue_bf16_pair_kernel(
+    const __grid_constant__ HeadEpilogue e0, const __grid_constant__ HeadEpilogue e1, int w0) {
+  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (wid < w0)
+    head_row_bf16(e0, wid, threadIdx.x & 31);
+  else
+    head_row_bf16(e1, wid - w0, threadIdx.x & 31);
 }
 
 __global__ void lens_advance_kernel(int32_t* lens, const int32_t* cu_rows, int batch, int bs,
@@ -447,6 +460,20 @@ cudaError_t head_epilogue_bf16(const HeadEpilogue& e, cudaStream_t s) {
   {
     LaunchScope ls_(DFLASH_KERNEL_HEAD_EPILOGUE, s);
     head_epilogue_bf16_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(e);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t head_epilogue_bf16_pair(const HeadEpilogue& e0, const HeadEpilogue& e1,
+                                    cudaStream_t s) {
+  if (e0.d_h != 128 || e1.d_h != 128) return cudaErrorInvalidValue;
+  const long long w0 = e0.rows > 0 ? (long long)e0.rows * (e0.n_q + 2 * e0.n_kv) : 0;
+  const long long w1 = e1.rows > 0 ? (long long)e1.rows * (e1.n_q + 2 * e1.n_kv) : 0;
+  if (w0 + w1 == 0) return cudaSuccess;
+  if (w0 + w1 >= (1ll << 31) - 8) return cudaErrorInvalidValue;
+  {
+    LaunchScope ls_(DFLASH_KERNEL_HEAD_EPILOGUE, s);
+    head_epilogue_bf16_pair_kernel<<<(unsigned)((w0 + w1 + 7) / 8), 256, 0, s>>>(e0, e1, (int)w0);
   }
   return cudaGetLastError();
 }

@@ -69,10 +69,10 @@ struct TcGemmParams {
   float* Y;           // fp32 store: [split][M][ldY]
   HeadEpilogue ep;    // heads: norm / RoPE / destination
   unsigned* status;
-  // Grouped launch (heads epilogue, no split-K): grid columns [0, ny0) compute the
-  // problem above, columns [ny0, ny0 + ny1) a second one with one activation segment
-  // (same K), and with sched_cta one more column whose first CTA builds the
-  // attention work list while the tiles run.
+  // Grouped launch (heads epilogue without split-K, or fp32 split-K partials): grid
+  // columns [0, ny0) compute the problem above, columns [ny0, ny0 + ny1) a second one
+  // with one activation segment (same K and K split), and with sched_cta one more column
+  // whose first CTA builds the attention work list while the tiles run.
   int ny0, ny1, sched_cta;
   // Fused hidden_norm (fp32-store launches of the context projection, norm != 0): the last
   // split of each tile to finish adds the other splits' partials (published in Y) to its
@@ -93,6 +93,9 @@ struct TcGemmParams {
   int w1_off[4];
   int M1;
   HeadEpilogue ep1;
+  // grouped split-K launch (fp32 store): the second problem's partials [split][M1][ldY1]
+  float* Y1;
+  int ldY1;
   sched::Params sp;
 };
 
@@ -760,9 +763,10 @@ __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const _
   } else if (!abort_flag) {
     if (!HEADS) {
       // fp32 partial rows, one contiguous copy each
-      float* ybase = p.Y + (size_t)blockIdx.z * M * p.ldY + n0;
+      const int ldY = second ? p.ldY1 : p.ldY;
+      float* ybase = (second ? p.Y1 : p.Y) + (size_t)blockIdx.z * M * ldY + n0;
       for (int r = threadIdx.x; r < BM && m0 + r < M; r += kThreads)
-        ptx::bulk_store(ybase + (size_t)(m0 + r) * p.ldY, ptx::smem_u32(stg + r * C::LD), BN * 4);
+        ptx::bulk_store(ybase + (size_t)(m0 + r) * ldY, ptx::smem_u32(stg + r * C::LD), BN * 4);
     } else {
       // one copy per (row, head): the row's Q row, or its cache slot (bf16: 256 bytes;
       // E4M3: 128 bytes of codes, and for Q 128 bytes of remainder codes)
@@ -1137,10 +1141,11 @@ int layer_bn(int Mc, const Weights& Wkv, int Mb, const Weights& Wqkv, int K) {
   const Plan a = plan(Mc, Wkv, K, true), b = plan(Mb, Wqkv, K, true);
   const int bn = a.bn < b.bn ? a.bn : b.bn;
   if (bn < 128) return 0;
-  // DFLASH_FUSED_LAYER=0 never groups, =1 groups whenever the shapes allow (the two are
-  // the same arithmetic); otherwise group when the tiles fill a good part of the GPU
+  // DFLASH_FUSED_LAYER=0 never groups, =1 groups whenever the shapes allow, =2 takes the
+  // split-K grouping wherever it applies (all the same arithmetic); otherwise group when
+  // the tiles fill a good part of the GPU
   const char* env = getenv("DFLASH_FUSED_LAYER");
-  if (env && env[0] == '0') return 0;
+  if (env && (env[0] == '0' || env[0] == '2')) return 0;
   if (env && env[0] == '1') return bn;
   const int tiles = ((Mc + BM - 1) / BM) * (Wkv.total() / bn) + ((Mb + BM - 1) / BM) * (Wqkv.total() / bn);
   return tiles >= 64 ? bn : 0;
@@ -1200,6 +1205,85 @@ cudaError_t gemm_tc_layer(const void* C, int Mc, const Weights& Wkv, const HeadE
   const int mt0 = grid_x(Mc, pl.pair), mt1 = grid_x(Mb, pl.pair);
   dim3 grid(mt0 > mt1 ? mt0 : mt1, p.ny0 + p.ny1 + (sp ? 1 : 0), 1);
   return bn == 256 ? launch<256, true>(p, grid, pl.pair, s) : launch<128, true>(p, grid, pl.pair, s);
+}
+
+// Both projections of a draft layer in one split-K launch, for batches whose tiles fill
+// too little of the GPU to run without split-K (a few sequences): the two problems share
+// one K split, each writes fp32 partials [split][M][N] that one per-head epilogue launch
+// finishes, and (sp != null) one extra CTA builds the attention work list. The plan
+// depends on the block rows alone; the context rows must fit the block's row tiles.
+namespace {
+bool layer_split_plan(int Mb, const Weights& Wkv, const Weights& Wqkv, int K, Plan* out) {
+  if (Mb <= 0 || K % BK) return false;
+  const char* env = getenv("DFLASH_FUSED_LAYER");
+  if (env && env[0] == '0') return false;
+  Plan pl;
+  pl.bn = 256;
+  for (int i = 0; i < Wkv.count; ++i)
+    while (Wkv.n[i] % pl.bn) pl.bn >>= 1;
+  for (int i = 0; i < Wqkv.count; ++i)
+    while (Wqkv.n[i] % pl.bn) pl.bn >>= 1;
+  if (pl.bn < 128) return false;
+  pl.pair = pair_wanted(Mb);
+  pl.gx = grid_x(Mb, pl.pair);
+  pl.kb_total = K / BK;
+  const int tiles = pl.gx * (Wkv.total() / pl.bn + Wqkv.total() / pl.bn);
+  int splits = 148 / tiles;
+  const int max_splits = pl.kb_total / 4 > 0 ? pl.kb_total / 4 : 1;
+  if (splits > max_splits) splits = max_splits;
+  if (splits < 2) return false;  // one pass fills the GPU: the fused-epilogue launches
+  pl.kb_per_split = (pl.kb_total + splits - 1) / splits;
+  pl.splits = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
+  *out = pl;
+  return true;
+}
+}  // namespace
+
+int gemm_tc_layer_split_splits(int Mb, const Weights& Wkv, const Weights& Wqkv, int K) {
+  Plan pl;
+  return layer_split_plan(Mb, Wkv, Wqkv, K, &pl) ? pl.splits : 0;
+}
+
+int gemm_tc_layer_split_rows(int Mb, const Weights& Wkv, const Weights& Wqkv, int K) {
+  Plan pl;
+  return layer_split_plan(Mb, Wkv, Wqkv, K, &pl) ? pl.gx * BM : 0;
+}
+
+cudaError_t gemm_tc_layer_split(const void* C, int Mc, const Weights& Wkv, float* Y0,
+                                const void* H, int Mb, const Weights& Wqkv, float* Y1, int K,
+                                const sched::Params* sp, unsigned* status, cudaStream_t s) {
+  Plan pl;
+  if (Mc <= 0 || !layer_split_plan(Mb, Wkv, Wqkv, K, &pl) || grid_x(Mc, pl.pair) > pl.gx)
+    return cudaErrorInvalidValue;
+  Segments A;
+  A.n = 1;
+  A.kseg = K;
+  A.p[0] = C;
+  TcGemmParams p;
+  cudaError_t e = fill_common(p, A, Mc, Wkv, pl, K);
+  if (e != cudaSuccess) return e;
+  p.Y = Y0;
+  p.ldY = Wkv.total();
+  p.status = status;
+  if (!encode_2d_bf16(&p.a1, H, Mb, K, BM)) return cudaErrorInvalidValue;
+  int off = 0;
+  for (int i = 0; i < Wqkv.count; ++i) {
+    if (!encode_2d_bf16(&p.b1[i], Wqkv.p[i], Wqkv.n[i], K, pl.pair ? pl.bn / 2 : pl.bn))
+      return cudaErrorInvalidValue;
+    p.w1_off[i] = off;
+    off += Wqkv.n[i];
+  }
+  p.w1_off[Wqkv.count] = off;
+  p.w1_count = Wqkv.count;
+  p.M1 = Mb;
+  p.Y1 = Y1;
+  p.ldY1 = Wqkv.total();
+  p.ny0 = Wkv.total() / pl.bn;
+  p.ny1 = Wqkv.total() / pl.bn;
+  p.sched_cta = sp != nullptr;
+  if (sp) p.sp = *sp;
+  dim3 grid(pl.gx, p.ny0 + p.ny1 + (sp ? 1 : 0), pl.splits);
+  return pl.bn == 256 ? launch<256, false>(p, grid, pl.pair, s) : launch<128, false>(p, grid, pl.pair, s);
 }
 
 }  // namespace dflash

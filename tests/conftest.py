@@ -27,13 +27,16 @@ def pytest_collection_modifyitems(config, items):
             item.add_marker(skip)
 
 
-@pytest.fixture(params=["calls", "layer"])
+@pytest.fixture(params=["calls", "layer", "split"])
 def layer_mode(request, monkeypatch):
     """How a draft layer is issued: two calls (kv_inject, block_attn), or one
     dflash_draft_layer call with its single grouped projection launch forced on
-    wherever the shapes allow it. Returns the run_round fused_layer flag."""
-    if request.param == "layer":
-        monkeypatch.setenv("DFLASH_FUSED_LAYER", "1")
+    wherever the shapes allow it ("layer": fused per-head epilogues; "split": both
+    projections as one split-K launch and one epilogue launch for both, where K allows
+    two or more splits and the rows fit one row tile). Returns the run_round fused_layer
+    flag."""
+    if request.param in ("layer", "split"):
+        monkeypatch.setenv("DFLASH_FUSED_LAYER", "1" if request.param == "layer" else "2")
         return True
     monkeypatch.delenv("DFLASH_FUSED_LAYER", raising=False)
     return False

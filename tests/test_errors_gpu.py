@@ -15,7 +15,7 @@ def _dev(w, **kw):
 
 def _tiny(kv="bf16"):
     return synth.WORKLOADS["serve_b32"].replace(
-        name="tiny", d=256, n_h=4, n_kv=2, k=1, batch=3, n_layers=1, windows=(0,),
+        name="tiny", d=512, n_h=4, n_kv=2, k=1, batch=3, n_layers=1, windows=(0,),
         prefill_lo=10, prefill_hi=60, rounds=1, seed=9, kv=kv)
 
 

@@ -28,6 +28,13 @@ SMALL = {
     "small_g8_bf16": W["serve_b32"].replace(
         name="small_g8_bf16", d=256, n_h=16, n_kv=2, k=3, batch=3, n_layers=1, windows=(16,),
         prefill_lo=1, prefill_hi=513, seed=5),
+    # One sequence at a width whose K allows four splits: each layer's two projections run
+    # as one split-K launch (layer modes "split" and the default); the prefill by
+    # projection + inject (200 rows, more than that launch takes) as two calls; round 2
+    # injects a_i rows
+    "small_b1_bf16": W["qwen3_8b_b1"].replace(
+        name="small_b1_bf16", d=1024, n_h=8, n_kv=2, k=2, batch=1, n_layers=2, windows=(0, 64),
+        prefill_lo=200, prefill_hi=200, rounds=2, seed=10, random_gamma=True),
     "small_gqa_f32": W["walkthrough_f32"].replace(
         name="small_gqa_f32", d=96, n_h=6, n_kv=2, d_h=32, k=2, bs=3, batch=3, n_layers=2,
         windows=(0, 5), prefill_lo=0, prefill_hi=600, new_ctx=4, rounds=2, seed=6,
@@ -94,9 +101,10 @@ def test_full_size_paged(name, n):
 
 
 # fp8 (E4M3) cache: the GQA (NARROW tile) case with a window, the MHA case with an odd
-# block and a prefill by projection + inject, and the G = 8 case (128 query rows, WIDE)
+# block and a prefill by projection + inject, the G = 8 case (128 query rows, WIDE), and
+# the one-sequence case
 FP8 = {n.replace("bf16", "fp8"): SMALL[n].replace(name=n.replace("bf16", "fp8"), kv="fp8")
-       for n in ("small_gqa_bf16", "small_mha_bf16", "small_g8_bf16")}
+       for n in ("small_gqa_bf16", "small_mha_bf16", "small_g8_bf16", "small_b1_bf16")}
 
 
 @pytest.mark.parametrize("name", sorted(FP8))
