@@ -29,7 +29,10 @@ namespace dflash {
 namespace sched {
 
 constexpr int kTileKeys = 128;     // keys per attention tile
-constexpr int kItemMinTiles = 4;   // smallest share of a CTA worth its pipeline ramp
+// a key range is cut into at most ceil(keys / (kItemMinTiles * kTileKeys)) items (the
+// partial rows kept per (sequence, KV head) pair)
+constexpr int kItemMinTiles = 4;
+constexpr int kShareMinTiles = 2;  // smallest share of a CTA worth its pipeline ramp
 constexpr int kTileCost = 8;       // cost of a tile in the partition (even: tile centres)
 constexpr int kMaxSm = 256;        // most CTAs a list is built for
 constexpr int kMergeCountShift = 20;  // merge_list entry: pair | item count << this
@@ -174,12 +177,12 @@ inline __device__ void build(const Params& p) {
   int W;
   const int cost0 = cta_scan(mine, tmp, &W);
   const int t_max = cta_max(longest, tmp);
-  // CTAs in use: shares of at least kItemMinTiles tiles, and far enough apart that no range
+  // CTAs in use: shares of at least kShareMinTiles tiles, and far enough apart that no range
   // is cut into more than max_splits items (tile centres spanning (t - 1) A cross at most
   // ceil((t - 1) A / share) share boundaries); with max_splits = 1 ranges stay whole and
   // each goes to the CTA whose share holds its middle
   const bool cut = p.max_splits >= 2;
-  int share = kItemMinTiles * A + B;
+  int share = kShareMinTiles * A + B;
   if (cut && t_max > 1) share = max(share, ((t_max - 1) * A + p.max_splits - 2) / (p.max_splits - 1));
   const int n_use = W > 0 ? max(1, min(p.n_sm, W / share)) : 0;
   // CTA c's share starts at cost y(c); owner(z) is the CTA whose share holds cost z

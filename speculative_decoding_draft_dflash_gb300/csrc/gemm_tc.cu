@@ -101,13 +101,20 @@ struct TcGemmParams {
 
 // PAIR: the tile is computed by a cluster of two CTAs (tcgen05.mma.cta_group::2, M = 256):
 // each CTA holds its own 128 rows of A and half of B's BN rows per stage.
-template <int BN, bool PAIR = false>
+// AR < BM (single CTAs, M <= AR): a stage holds only AR rows of A, so more stages of B
+// (the weights) fit; the MMA still reads 128 rows, and rows AR .. 127 of its A operand
+// are whatever follows in the stage: they reach only accumulator rows >= M, which are
+// never stored (each accumulator row depends on its own A row alone).
+constexpr int kSmallRows = 32;
+template <int BN, bool PAIR = false, int AR = BM>
 struct Cfg {
+  static_assert(AR % 8 == 0 && AR <= BM && (AR == BM || !PAIR), "A rows per stage");
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;
-  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t A_BYTES = AR * BK * 2;
   static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
   static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = PAIR ? ((BN == 256) ? 6 : 8) : ((BN == 256) ? 4 : 6);
+  static constexpr int STAGES = AR < BM ? ((BN == 256) ? 6 : 10)
+                                        : PAIR ? ((BN == 256) ? 6 : 8) : ((BN == 256) ? 4 : 6);
   // pipeline stages, barriers (256 B), then gamma_q / gamma_k as fp32 (heads epilogue)
   static constexpr uint32_t OFF_GAMMA = STAGES * STAGE + 256;
   static constexpr size_t SMEM = 1024 + (size_t)OFF_GAMMA + 2 * 128 * 4;
@@ -457,10 +464,10 @@ __device__ __forceinline__ void norm_epilogue(const TcGemmParams& p, float* stg,
   ptx::bulk_commit_wait_all();
 }
 
-template <int BN, bool HEADS, bool PAIR>
+template <int BN, bool HEADS, bool PAIR, int AR = BM>
 __global__ void __launch_bounds__(gemm_threads(HEADS), 1) gemm_tc_kernel(const __grid_constant__ TcGemmParams p) {
   constexpr int kThreads = gemm_threads(HEADS);
-  using C = Cfg<BN, PAIR>;
+  using C = Cfg<BN, PAIR, AR>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -886,15 +893,15 @@ Plan plan(int M, const Weights& W, int K, bool heads, int split_cap = 0) {
   return pl;
 }
 
-template <int BN, bool HEADS, bool PAIR>
+template <int BN, bool HEADS, bool PAIR, int AR = BM>
 cudaError_t launch_one(const TcGemmParams& p, dim3 grid, cudaStream_t s) {
-  const size_t smem = Cfg<BN, PAIR>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, HEADS, PAIR>,
+  const size_t smem = Cfg<BN, PAIR, AR>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, HEADS, PAIR, AR>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   LaunchScope ls_(DFLASH_KERNEL_GEMM, s);
   if constexpr (!PAIR) {
-    gemm_tc_kernel<BN, HEADS, false><<<grid, gemm_threads(HEADS), smem, s>>>(p);
+    gemm_tc_kernel<BN, HEADS, false, AR><<<grid, gemm_threads(HEADS), smem, s>>>(p);
     return cudaGetLastError();
   } else {
     if (grid.x & 1) return cudaErrorInvalidValue;  // whole pairs only
@@ -914,9 +921,21 @@ cudaError_t launch_one(const TcGemmParams& p, dim3 grid, cudaStream_t s) {
   }
 }
 
+// small: fp32-store launches whose rows fit kSmallRows (one row tile, single CTAs)
 template <int BN, bool HEADS>
-cudaError_t launch(const TcGemmParams& p, dim3 grid, bool pair, cudaStream_t s) {
+cudaError_t launch(const TcGemmParams& p, dim3 grid, bool pair, cudaStream_t s, bool small = false) {
+  if constexpr (!HEADS) {
+    if (small && !pair && grid.x == 1) return launch_one<BN, false, false, kSmallRows>(p, grid, s);
+  }
   return pair ? launch_one<BN, HEADS, true>(p, grid, s) : launch_one<BN, HEADS, false>(p, grid, s);
+}
+
+// Whether an fp32-store launch of M rows (and M1 for a grouped one) takes the small-A
+// stages; DFLASH_SMALL_A=0 keeps the 128-row stages (the same arithmetic).
+bool small_rows(const Plan& pl, int M, int M1 = 0) {
+  const char* env = getenv("DFLASH_SMALL_A");
+  if (env && env[0] == '0') return false;
+  return !pl.pair && pl.bn >= 128 && M <= kSmallRows && M1 <= kSmallRows;
 }
 
 }  // namespace
@@ -960,10 +979,10 @@ bool gemm_tc_heads_ok(int M, const Weights& W, int K) {
 namespace {
 
 cudaError_t fill_common(TcGemmParams& p, const Segments& A, int M, const Weights& W, const Plan& pl,
-                        int K) {
+                        int K, int a_rows = BM) {
   memset(&p, 0, sizeof(p));
   for (int i = 0; i < A.n; ++i)
-    if (!encode_2d_bf16(&p.a[i], A.p[i], M, A.kseg, BM)) return cudaErrorInvalidValue;
+    if (!encode_2d_bf16(&p.a[i], A.p[i], M, A.kseg, a_rows)) return cudaErrorInvalidValue;
   for (int i = A.n; i < 8; ++i) p.a[i] = p.a[0];
   int off = 0;
   for (int i = 0; i < W.count; ++i) {
@@ -992,16 +1011,17 @@ cudaError_t gemm_tc(const Segments& A, int M, const Weights& W, float* Y, int ld
   const int K = A.n * A.kseg;
   const Plan pl = plan(M, W, K, false, split_cap);
   if (pl.bn < 64 || A.kseg % BK) return cudaErrorInvalidValue;
+  const bool small = small_rows(pl, M);
   TcGemmParams p;
-  cudaError_t e = fill_common(p, A, M, W, pl, K);
+  cudaError_t e = fill_common(p, A, M, W, pl, K, small ? kSmallRows : BM);
   if (e != cudaSuccess) return e;
   p.ldY = ldY;
   p.Y = Y;
   p.status = status;
   dim3 grid(pl.gx, N / pl.bn, pl.splits);
   switch (pl.bn) {
-    case 256: return launch<256, false>(p, grid, pl.pair, s);
-    case 128: return launch<128, false>(p, grid, pl.pair, s);
+    case 256: return launch<256, false>(p, grid, pl.pair, s, small);
+    case 128: return launch<128, false>(p, grid, pl.pair, s, small);
     default: return launch_one<64, false, false>(p, grid, s);
   }
 }
@@ -1259,13 +1279,15 @@ cudaError_t gemm_tc_layer_split(const void* C, int Mc, const Weights& Wkv, float
   A.n = 1;
   A.kseg = K;
   A.p[0] = C;
+  const bool small = small_rows(pl, Mc, Mb);
+  const int a_rows = small ? kSmallRows : BM;
   TcGemmParams p;
-  cudaError_t e = fill_common(p, A, Mc, Wkv, pl, K);
+  cudaError_t e = fill_common(p, A, Mc, Wkv, pl, K, a_rows);
   if (e != cudaSuccess) return e;
   p.Y = Y0;
   p.ldY = Wkv.total();
   p.status = status;
-  if (!encode_2d_bf16(&p.a1, H, Mb, K, BM)) return cudaErrorInvalidValue;
+  if (!encode_2d_bf16(&p.a1, H, Mb, K, a_rows)) return cudaErrorInvalidValue;
   int off = 0;
   for (int i = 0; i < Wqkv.count; ++i) {
     if (!encode_2d_bf16(&p.b1[i], Wqkv.p[i], Wqkv.n[i], K, pl.pair ? pl.bn / 2 : pl.bn))
@@ -1283,7 +1305,8 @@ cudaError_t gemm_tc_layer_split(const void* C, int Mc, const Weights& Wkv, float
   p.sched_cta = sp != nullptr;
   if (sp) p.sp = *sp;
   dim3 grid(pl.gx, p.ny0 + p.ny1 + (sp ? 1 : 0), pl.splits);
-  return pl.bn == 256 ? launch<256, false>(p, grid, pl.pair, s) : launch<128, false>(p, grid, pl.pair, s);
+  return pl.bn == 256 ? launch<256, false>(p, grid, pl.pair, s, small)
+                      : launch<128, false>(p, grid, pl.pair, s, small);
 }
 
 }  // namespace dflash
