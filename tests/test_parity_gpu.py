@@ -35,6 +35,12 @@ SMALL = {
     "small_b1_bf16": W["qwen3_8b_b1"].replace(
         name="small_b1_bf16", d=1024, n_h=8, n_kv=2, k=2, batch=1, n_layers=2, windows=(0, 64),
         prefill_lo=200, prefill_hi=200, rounds=2, seed=10, random_gamma=True),
+    # One sequence injecting 100 context rows: the split-K grouping with more context rows
+    # than block rows (both within one 128-row tile)
+    "small_b1_inject100_bf16": W["qwen3_8b_b1"].replace(
+        name="small_b1_inject100_bf16", d=1024, n_h=8, n_kv=2, k=2, batch=1, n_layers=1,
+        windows=(0,), prefill_lo=300, prefill_hi=300, prefill_inject=False, new_ctx=100,
+        rounds=1, seed=12),
     "small_gqa_f32": W["walkthrough_f32"].replace(
         name="small_gqa_f32", d=96, n_h=6, n_kv=2, d_h=32, k=2, bs=3, batch=3, n_layers=2,
         windows=(0, 5), prefill_lo=0, prefill_hi=600, new_ctx=4, rounds=2, seed=6,
