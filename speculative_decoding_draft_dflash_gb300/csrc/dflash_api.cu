@@ -256,15 +256,27 @@ DFLASH_API size_t dflash_workspace_bytes(const dflash_dims* d, int batch, int ca
                                          int max_rows) {
   if (check_dims(d) != DFLASH_OK || batch < 0 || capacity < 0 || max_rows < 0) return 0;
   size_t need = 256;
-  {
-    Carver cv(nullptr, ~size_t(0));
-    carve_ctx(cv, d, max_rows);
-    need = need > cv.off ? need : cv.off;
-  }
-  {
-    Carver cv(nullptr, ~size_t(0));
-    carve_inject(cv, d, max_rows);
-    need = need > cv.off ? need : cv.off;
+  // every row count up to max_rows: the projections' K-split counts change with the
+  // 128-row tiles M spans (fewer rows can mean more splits, each with its own partials),
+  // and within one tile count the scratch grows with M, so the top of each tile count's
+  // range bounds it; once both projections run unsplit, more rows only need more
+  const Weights Wc = ctx_weights(d, nullptr), Wkv = kv_weights(d, nullptr, nullptr);
+  for (long long m = 128; ; m += 128) {
+    if (m < max_rows && gemm_splits(d->dtype, (int)m, Wc, d->k_layers * d->d) == 1 &&
+        gemm_splits(d->dtype, (int)m, Wkv, d->d) == 1)
+      m = max_rows;
+    const int rows = m < max_rows ? (int)m : max_rows;
+    {
+      Carver cv(nullptr, ~size_t(0));
+      carve_ctx(cv, d, rows);
+      need = need > cv.off ? need : cv.off;
+    }
+    {
+      Carver cv(nullptr, ~size_t(0));
+      carve_inject(cv, d, rows);
+      need = need > cv.off ? need : cv.off;
+    }
+    if (m >= max_rows) break;
   }
   {
     Carver cv(nullptr, ~size_t(0));

@@ -75,6 +75,17 @@ def test_workspace_bytes_host_logic(D):
     assert D.dflash_workspace_bytes(dims, -1, 64, 16) == 0
 
 
+@pytest.mark.parametrize("batch", [1, 2, 4, 8])
+def test_workspace_bytes_never_shrink_with_more_rows(D, batch):
+    """A workspace sized for max_rows serves every call with fewer context rows: the need
+    (including the few-sequence layer launch's context partials, which grow with M until
+    the launch's row tile is full) never decreases as max_rows grows."""
+    dims = _dims(D)
+    need = [D.dflash_workspace_bytes(dims, batch, 1088, m) for m in range(1, 400, 3)]
+    assert all(b >= a for a, b in zip(need, need[1:]))
+    assert need[0] >= D.dflash_workspace_bytes(dims, batch, 1088, 0)
+
+
 @pytest.mark.parametrize("kw,expect", [
     (dict(n_h=30), 2), (dict(d_h=64), 2), (dict(block_size=17), 2), (dict(k_layers=9), 2),
     (dict(dtype=7), 2), (dict(d=0), 1), (dict(eps=-1.0), 1), (dict(d=4100), 2),
