@@ -212,8 +212,8 @@ LayerSplitScratch carve_layer_split(Carver& cv, const dflash_dims* d, int batch,
   const Weights Wkv = kv_weights(d, nullptr, nullptr), Wqkv = qkv_weights(d, nullptr, nullptr, nullptr);
   s.splits = gemm_tc_layer_split_splits(rows, Wkv, Wqkv, d->d);
   if (s.splits == 0) return s;
-  const int mc = M < gemm_tc_layer_split_rows(rows, Wkv, Wqkv, d->d)
-                     ? M : gemm_tc_layer_split_rows(rows, Wkv, Wqkv, d->d);
+  const int cap = gemm_tc_layer_split_rows(rows, Wkv, Wqkv, d->d);
+  const int mc = M < cap ? M : cap;
   s.Y0 = cv.take<float>((size_t)s.splits * mc * Wkv.total());
   s.Y1 = s.b.Y && s.b.splits >= s.splits ? s.b.Y
                                          : cv.take<float>((size_t)s.splits * rows * Wqkv.total());
