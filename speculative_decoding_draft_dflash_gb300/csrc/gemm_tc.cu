@@ -921,11 +921,16 @@ cudaError_t launch_one(const TcGemmParams& p, dim3 grid, cudaStream_t s) {
   }
 }
 
-// small: fp32-store launches whose rows fit kSmallRows (one row tile, single CTAs)
+// small: fp32-store launches whose rows fit kSmallRows (one row tile, single CTAs), with
+// activation maps of kSmallRows-row boxes; anything else is refused, since the stage byte
+// count the copies are awaited for follows the box
 template <int BN, bool HEADS>
 cudaError_t launch(const TcGemmParams& p, dim3 grid, bool pair, cudaStream_t s, bool small = false) {
-  if constexpr (!HEADS) {
-    if (small && !pair && grid.x == 1) return launch_one<BN, false, false, kSmallRows>(p, grid, s);
+  if (small) {
+    if constexpr (!HEADS) {
+      if (!pair && grid.x == 1) return launch_one<BN, false, false, kSmallRows>(p, grid, s);
+    }
+    return cudaErrorInvalidValue;
   }
   return pair ? launch_one<BN, HEADS, true>(p, grid, s) : launch_one<BN, HEADS, false>(p, grid, s);
 }
